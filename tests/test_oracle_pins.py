@@ -1,0 +1,449 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself.
+
+Each test checks the oracle against something the pages print (fixtures in
+tests/golden/, each with its citation), a closed form, an invariant the pages
+state, a special case that reduces to a library routine, or brute force on
+tiny inputs.  No expected value here comes from the CUDA path.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import logsumexp
+
+import oracle
+from paged_kv_cache_41_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rows(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+
+
+# ------------------------------------------------------------------ index math
+def test_block_counts_printed_in_pages():
+    rows = _rows("block_counts.txt")
+    assert len(rows) == 5
+    for t, p, nb, tail in rows:
+        assert oracle.num_blocks(int(t), int(p)) == int(nb)
+        if tail != "-":
+            assert oracle.tail_rows(int(t), int(p)) == int(tail)
+
+
+def test_block_count_edges():
+    # T = k*P fills its last block; T = k*P + 1 spills one row; T = 0 has none
+    assert oracle.num_blocks(32, 16) == 2 and oracle.tail_rows(32, 16) == 16
+    assert oracle.num_blocks(33, 16) == 3 and oracle.tail_rows(33, 16) == 1
+    assert oracle.num_blocks(0, 16) == 0 and oracle.tail_rows(0, 16) == 0
+    assert oracle.num_blocks(1, 16) == 1 and oracle.tail_rows(1, 16) == 1
+
+
+def test_checked_address_trace():
+    kv = {r[0]: r[1:] for r in _rows("address_trace.txt") if r[0] != "slot_id"}
+    shape = [int(x) for x in kv["shape"]]
+    coord = [int(x) for x in kv["coord"]]
+    # the printed strides are the offsets of the unit coordinates
+    for a, stride in enumerate(int(x) for x in kv["strides"]):
+        unit = [0] * len(shape)
+        unit[a] = 1
+        assert oracle.row_major_offset(shape, unit) == stride
+    e = oracle.row_major_offset(shape, coord)
+    assert e == int(kv["element_offset"][0])
+    assert int(kv["scalar_bytes"][0]) * e == int(kv["byte_offset"][0])
+    assert int(kv["k_base"][0]) + int(kv["byte_offset"][0]) == int(kv["byte_address"][0])
+    # the slot id and the byte address are different quantities
+    assert oracle.slot_id(6, 16, 0) != int(kv["byte_address"][0])
+    # an out-of-range coordinate is rejected
+    assert oracle.row_major_offset(shape, [0, 8, 0, 1, 5]) == -1
+
+
+def test_slot_ids_printed_in_pages():
+    for r in _rows("address_trace.txt"):
+        if r[0] == "slot_id":
+            slot, p, off, want = map(int, r[1:])
+            assert oracle.slot_id(slot, p, off) == want
+
+
+def test_resolve_visibility_printed_in_pages():
+    nb = 64
+    table = [11, 40, 7]
+    for ctx, p, tok, expect, lb, off in _rows("visibility.txt"):
+        st, blk, o = oracle.resolve(table, int(ctx), int(p), nb, int(tok))
+        if expect == "ok":
+            assert st == oracle.OK
+            assert blk == table[int(lb)] and o == int(off)
+        else:
+            assert st == oracle.REJECT_VISIBILITY
+
+
+def test_resolve_rejection_order():
+    # visibility is checked before the table bound, the table bound before identity
+    assert oracle.resolve([3], 16, 16, 8, 20)[0] == oracle.REJECT_VISIBILITY
+    assert oracle.resolve([3], 40, 16, 8, 20)[0] == oracle.REJECT_TABLE
+    assert oracle.resolve([3, 99], 40, 16, 8, 20)[0] == oracle.REJECT_PHYSICAL
+    assert oracle.resolve([3, -1], 40, 16, 8, 20)[0] == oracle.REJECT_PHYSICAL
+    assert oracle.resolve([3, 5], 40, 16, 8, 20)[:2] == (oracle.OK, 5)
+
+
+def test_slot_mapping_of_the_35_token_example():
+    # "7. Memory Management and Local Model State": logical blocks 0, 1, 2 of a
+    # 35-token sequence sit in physical blocks 7, 2, 19.  Enumerate the slots as
+    # whole physical row ranges and compare position by position.
+    table = [7, 2, 19]
+    expect = list(range(7 * 16, 8 * 16)) + list(range(2 * 16, 3 * 16)) + list(range(19 * 16, 19 * 16 + 3))
+    got = [oracle.slot_for_position(table, 16, t) for t in range(35)]
+    assert got == expect
+
+
+def test_slot_ids_widen_to_int64():
+    # a page id whose slot exceeds int32 range ("widen page ids to int64 before
+    # multiplying by pool strides")
+    big = 2**31 - 5
+    assert oracle.slot_for_position([big], 64, 63) == big * 64 + 63
+
+
+# ------------------------------------------------------------------ append / copy
+def _rand_cache(nb, p, hkv, d, dtype, rng):
+    if dtype == "f32":
+        return rng.standard_normal((nb, p, hkv, d)).astype(np.float32)
+    return rng.integers(0, 2**16, size=(nb, p, hkv, d), dtype=np.uint16)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_append_matches_fancy_index_scatter(dtype):
+    rng = np.random.default_rng(7)
+    nb, p, hkv, d = 6, 16, 2, 8
+    kc, vc = _rand_cache(nb, p, hkv, d, dtype, rng), _rand_cache(nb, p, hkv, d, dtype, rng)
+    n = 20
+    slots = rng.choice(nb * p, size=n, replace=False).astype(np.int64)
+    slots[[3, 11]] = -1  # skip sentinel
+    k = _rand_cache(n, hkv, d, 1, dtype, rng).reshape(n, hkv, d)
+    v = _rand_cache(n, hkv, d, 1, dtype, rng).reshape(n, hkv, d)
+    ek, ev = kc.copy().reshape(nb * p, hkv, d), vc.copy().reshape(nb * p, hkv, d)
+    keep = slots >= 0
+    ek[slots[keep]] = k[keep]
+    ev[slots[keep]] = v[keep]
+    assert oracle.kv_append(kc, vc, k, v, slots) == oracle.OK
+    assert np.array_equal(kc.reshape(nb * p, hkv, d).view(np.uint8), ek.view(np.uint8))
+    assert np.array_equal(vc.reshape(nb * p, hkv, d).view(np.uint8), ev.view(np.uint8))
+
+
+def test_append_rejects_slot_past_pool():
+    rng = np.random.default_rng(8)
+    kc = np.zeros((2, 16, 1, 4), np.float32)
+    vc = np.zeros_like(kc)
+    k = rng.standard_normal((2, 1, 4)).astype(np.float32)
+    st = oracle.kv_append(kc, vc, k, k, np.array([5, 32], np.int64))
+    assert st == oracle.BAD_SLOT
+    assert np.array_equal(kc[0, 5], k[0]) and not kc[1].any()
+
+
+def test_block_copy_matches_slicing_in_order():
+    rng = np.random.default_rng(9)
+    nb, p, hkv, d = 8, 16, 2, 4
+    kc = _rand_cache(nb, p, hkv, d, "bf16", rng)
+    vc = _rand_cache(nb, p, hkv, d, "bf16", rng)
+    ek, ev = kc.copy(), vc.copy()
+    pairs = [(1, 4), (4, 6), (2, 0)]
+    for s, t in pairs:
+        ek[t] = ek[s]
+        ev[t] = ev[s]
+    assert oracle.kv_block_copy(kc, vc, pairs) == oracle.OK
+    assert np.array_equal(kc, ek) and np.array_equal(vc, ev)
+    assert np.array_equal(kc[6], kc[1])  # chained copies apply in order
+    assert oracle.kv_block_copy(kc, vc, [(0, 8)]) == oracle.BAD_BLOCK
+
+
+# ------------------------------------------------------------------ decode
+def _oracle_pool_from_batch(b: wl.PagedBatch):
+    """Fill an oracle-side pool from the logical history, with slots derived by
+    the oracle's own translation of the block tables."""
+    kh, vh = wl.to_numpy_storage(b.k_hist), wl.to_numpy_storage(b.v_hist)
+    fill = np.nan if b.dtype == "f32" else 0x7FC0  # NaN poison in unused rows
+    shape = (b.num_blocks, b.block_size, b.num_kv_heads, b.head_dim)
+    kc = np.full(shape, fill, dtype=kh.dtype)
+    vc = np.full(shape, fill, dtype=kh.dtype)
+    slots = np.concatenate([
+        np.array([oracle.slot_for_position(b.block_tables[r], b.block_size, t)
+                  for t in range(int(b.seq_lens[r]))], dtype=np.int64)
+        for r in range(b.num_seqs)]) if b.num_seqs else np.zeros(0, np.int64)
+    assert oracle.kv_append(kc, vc, kh, vh, slots) == oracle.OK
+    return kc, vc
+
+
+def _scipy_attention(b: wl.PagedBatch):
+    """Attention over the logical (never paged) history with library routines."""
+    kh, vh, q = b.k_hist.double().numpy(), b.v_hist.double().numpy(), b.q.double().numpy()
+    g = b.num_q_heads // b.num_kv_heads
+    out = np.zeros((b.num_seqs, b.num_q_heads, b.head_dim))
+    lse = np.full((b.num_seqs, b.num_q_heads), -np.inf)
+    for r in range(b.num_seqs):
+        lo, hi = b.hist_offsets[r], b.hist_offsets[r + 1]
+        if hi == lo:
+            continue
+        for h in range(b.num_q_heads):
+            s = b.scale * (kh[lo:hi, h // g, :] @ q[r, h])
+            lse[r, h] = logsumexp(s)
+            out[r, h] = np.exp(s - lse[r, h]) @ vh[lo:hi, h // g, :]
+    return out, lse
+
+
+@pytest.mark.parametrize("maker", ["tiny", "bf16_small"])
+def test_decode_matches_library_softmax_on_logical_history(maker):
+    if maker == "tiny":
+        b = wl.tiny_batch()
+    else:
+        b = wl.custom_batch([1, 15, 16, 17, 40, 0, 64], dtype="bf16", hq=8, hkv=2, d=32, p=16,
+                            seed=11)
+    kc, vc = _oracle_pool_from_batch(b)
+    out, lse = oracle.paged_decode(wl.to_numpy_storage(b.q), kc, vc, b.block_tables,
+                                   b.seq_lens, b.scale)
+    ref, ref_lse = _scipy_attention(b)
+    assert np.isfinite(out).all()
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, rtol=1e-12, atol=1e-12)
+
+
+def test_decode_permutation_invariance_is_bitwise():
+    b = wl.custom_batch([37, 5, 80], dtype="bf16", hq=4, hkv=2, d=16, p=16, seed=12)
+    kc, vc = _oracle_pool_from_batch(b)
+    q = wl.to_numpy_storage(b.q)
+    out, lse = oracle.paged_decode(q, kc, vc, b.block_tables, b.seq_lens, b.scale)
+    perm = np.random.default_rng(3).permutation(b.num_blocks)  # new id of old block i
+    kc2, vc2 = np.empty_like(kc), np.empty_like(vc)
+    kc2[perm], vc2[perm] = kc, vc
+    bt2 = np.where(b.block_tables >= 0, perm[np.maximum(b.block_tables, 0)], -1).astype(np.int32)
+    out2, lse2 = oracle.paged_decode(q, kc2, vc2, bt2, b.seq_lens, b.scale)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+def _one_seq(k, v, q, scale, p=4):
+    """Pack one sequence (rows [T, 1, D]) into a pool with reversed block order."""
+    t, d = k.shape[0], k.shape[-1]
+    n = max(1, oracle.num_blocks(t, p))
+    kc = np.full((n, p, 1, d), np.nan, np.float32)
+    vc = np.full((n, p, 1, d), np.nan, np.float32)
+    table = np.arange(n - 1, -1, -1, dtype=np.int32)
+    slots = np.array([oracle.slot_for_position(table, p, i) for i in range(t)], np.int64)
+    oracle.kv_append(kc, vc, k.reshape(t, 1, d), v.reshape(t, 1, d), slots)
+    return oracle.paged_decode(q.reshape(1, 1, d), kc, vc, table.reshape(1, -1),
+                               np.array([t], np.int32), scale)
+
+
+def test_single_token_returns_its_value_row():
+    rng = np.random.default_rng(1)
+    k, v, q = (rng.standard_normal((1, 8)).astype(np.float32) for _ in range(3))
+    out, lse = _one_seq(k, v, q, 0.3)
+    assert np.array_equal(out[0, 0], v[0].astype(np.float64))
+    assert lse[0, 0] == pytest.approx(0.3 * float(np.dot(q[0].astype(np.float64), k[0])), rel=1e-15)
+
+
+def test_equal_keys_average_the_values():
+    rng = np.random.default_rng(2)
+    t = 11
+    k = np.repeat(rng.standard_normal((1, 8)).astype(np.float32), t, axis=0)
+    v = rng.standard_normal((t, 8)).astype(np.float32)
+    q = rng.standard_normal((1, 8)).astype(np.float32)
+    out, lse = _one_seq(k, v, q, 0.5)
+    np.testing.assert_allclose(out[0, 0], v.astype(np.float64).mean(axis=0), rtol=0, atol=1e-15)
+    s = 0.5 * float(np.dot(q[0].astype(np.float64), k[0]))
+    assert lse[0, 0] == pytest.approx(s + math.log(t), rel=1e-14)
+
+
+def test_two_token_closed_form():
+    # softmax of two scores is the logistic function of their difference
+    rng = np.random.default_rng(4)
+    k, v = rng.standard_normal((2, 6)).astype(np.float32), rng.standard_normal((2, 6)).astype(np.float32)
+    q = rng.standard_normal((1, 6)).astype(np.float32)
+    scale = 0.7
+    s0, s1 = (scale * float(np.dot(q[0].astype(np.float64), k[i])) for i in range(2))
+    w1 = 1.0 / (1.0 + math.exp(s0 - s1))
+    want = v[0].astype(np.float64) * (1 - w1) + v[1].astype(np.float64) * w1
+    out, lse = _one_seq(k, v, q, scale)
+    np.testing.assert_allclose(out[0, 0], want, rtol=0, atol=1e-14)
+    assert lse[0, 0] == pytest.approx(max(s0, s1) + math.log1p(math.exp(-abs(s0 - s1))), rel=1e-14)
+
+
+def test_dominant_key_selects_its_value():
+    rng = np.random.default_rng(5)
+    t, d = 9, 4
+    k = np.zeros((t, d), np.float32)
+    k[6] = 1.0
+    v = rng.standard_normal((t, d)).astype(np.float32)
+    q = np.ones((1, d), np.float32)
+    out, _ = _one_seq(k, v, q, 200.0)  # scores 800 vs 0: the other weights are e^-800
+    assert np.array_equal(out[0, 0], v[6].astype(np.float64))
+
+
+def test_gqa_groups_are_contiguous():
+    # q heads h use kv head h // (Hq / Hkv): with Hq=4, Hkv=2 heads 0,1 read kv
+    # head 0 (all values +1) and heads 2,3 read kv head 1 (all values -1)
+    t, d, p = 5, 4, 4
+    rng = np.random.default_rng(6)
+    k = rng.standard_normal((t, 2, d)).astype(np.float32)
+    v = np.empty((t, 2, d), np.float32)
+    v[:, 0], v[:, 1] = 1.0, -1.0
+    kc = np.zeros((2, p, 2, d), np.float32)
+    vc = np.zeros_like(kc)
+    table = np.array([[1, 0]], np.int32)
+    oracle.kv_append(kc, vc, k, v, np.array([oracle.slot_for_position(table[0], p, i)
+                                             for i in range(t)], np.int64))
+    q = rng.standard_normal((1, 4, d)).astype(np.float32)
+    out, _ = oracle.paged_decode(q, kc, vc, table, np.array([t], np.int32), 0.5)
+    np.testing.assert_allclose(out[0, :2], 1.0, atol=1e-15)
+    np.testing.assert_allclose(out[0, 2:], -1.0, atol=1e-15)
+
+
+def test_empty_sequence_is_zero_with_minus_inf_lse():
+    kc = np.zeros((2, 16, 1, 4), np.float32)
+    out, lse = oracle.paged_decode(np.ones((1, 1, 4), np.float32), kc, kc,
+                                   np.full((1, 1), -1, np.int32), np.array([0], np.int32), 1.0)
+    assert not out.any() and lse[0, 0] == -np.inf
+
+
+def test_stale_tail_rows_are_never_read():
+    # NaN-poisoned unused rows (tail of the last block, unused blocks) must not
+    # reach the result; the clean pool gives the same bits.
+    b = wl.custom_batch([35, 100, 16, 1], dtype="f32", hq=4, hkv=2, d=64, p=16, num_blocks=32,
+                        seed=1, scale=0.125)
+    kc, vc = _oracle_pool_from_batch(b)  # NaN-filled outside the history
+    q = wl.to_numpy_storage(b.q)
+    out, lse = oracle.paged_decode(q, kc, vc, b.block_tables, b.seq_lens, b.scale)
+    assert np.isfinite(out).all()
+    kc0, vc0 = np.nan_to_num(kc, nan=0.0), np.nan_to_num(vc, nan=0.0)
+    out0, lse0 = oracle.paged_decode(q, kc0, vc0, b.block_tables, b.seq_lens, b.scale)
+    assert np.array_equal(out, out0) and np.array_equal(lse, lse0)
+
+
+# ------------------------------------------------------------------ shared prefix
+def _shared_prefix_pools(sp: wl.SharedPrefixBatch):
+    pk, pv = wl.to_numpy_storage(sp.parent_k), wl.to_numpy_storage(sp.parent_v)
+    ck, cv = wl.to_numpy_storage(sp.child_k), wl.to_numpy_storage(sp.child_v)
+    shape = (sp.num_blocks, sp.block_size, sp.num_kv_heads, sp.head_dim)
+    kc = np.full(shape, 0x7FC0, np.uint16)
+    vc = np.full(shape, 0x7FC0, np.uint16)
+    n_par = sp.prefix_len + sp.shared_tail
+    ps = np.array([oracle.slot_for_position(sp.parent_table, sp.block_size, t)
+                   for t in range(n_par)], np.int64)
+    oracle.kv_append(kc, vc, pk, pv, ps)
+    assert oracle.kv_block_copy(kc, vc, sp.cow_pairs) == oracle.OK
+    npre = sp.prefix_len // sp.block_size
+    for r in range(sp.num_seqs):
+        table = np.concatenate([sp.prefix_block_ids, sp.suffix_tables[r]])
+        lo, hi = sp.child_offsets[r], sp.child_offsets[r + 1]
+        cs = np.array([oracle.slot_for_position(table, sp.block_size, n_par + i)
+                       for i in range(hi - lo)], np.int64)
+        oracle.kv_append(kc, vc, np.ascontiguousarray(ck[lo:hi]), np.ascontiguousarray(cv[lo:hi]), cs)
+    return kc, vc, npre
+
+
+def test_shared_prefix_equals_private_copies():
+    sp = wl.shared_prefix_batch(batch=6, prefix_len=64, shared_tail=5, suffix_lo=5, suffix_hi=40,
+                                hq=4, hkv=2, d=16, p=16, seed=21)
+    kc, vc, npre = _shared_prefix_pools(sp)
+    q = wl.to_numpy_storage(sp.q)
+    out, lse = oracle.shared_prefix(q, kc, vc, sp.prefix_block_ids, sp.prefix_len,
+                                    sp.suffix_tables, sp.suffix_lens, sp.scale)
+    # private layout: every request owns a copy of the prefix blocks
+    nb = sp.num_blocks
+    extra = sp.num_seqs * npre
+    kc2 = np.concatenate([kc, np.zeros((extra,) + kc.shape[1:], kc.dtype)])
+    vc2 = np.concatenate([vc, np.zeros((extra,) + vc.shape[1:], vc.dtype)])
+    tables, lens = [], []
+    for r in range(sp.num_seqs):
+        own = np.arange(nb + r * npre, nb + (r + 1) * npre, dtype=np.int32)
+        kc2[own], vc2[own] = kc[sp.prefix_block_ids], vc[sp.prefix_block_ids]
+        tables.append(np.concatenate([own, sp.suffix_tables[r]]))
+        lens.append(sp.prefix_len + sp.suffix_lens[r])
+    out2, lse2 = oracle.paged_decode(q, kc2, vc2, np.array(tables, np.int32),
+                                     np.array(lens, np.int32), sp.scale)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+    # and the CoW left every child with private copies of the shared tail rows
+    assert len(sp.cow_pairs) == sp.num_seqs - 1
+
+
+def _lse_merge(parts):
+    """Hydragen-coordinate merge of (O_p, LSE_p) partitions, numpy fp64."""
+    lses = np.array([l for _, l in parts])
+    mx = lses.max()
+    w = np.exp(lses - mx)
+    o = sum(wi * oi for wi, (oi, _) in zip(w, parts)) / w.sum()
+    return o, mx + np.log(w.sum())
+
+
+def test_loop9_tree_partitioned_schedule_agrees_with_oracle():
+    kv = {}
+    for r in _rows("ledgers.txt"):
+        if r[0] == "loop9":
+            kv.setdefault(r[1], []).append(r[2:])
+    chunks = dict((c.split(":")[0], int(c.split(":")[1])) for c in kv["chunks"][0])
+    paths = [p.split(":")[1].split(",") for p in kv["paths"][0]]
+    counts = ["logical"] + kv["logical"][0]
+    want = dict(zip(counts[::2], counts[1::2]))
+    d = 2
+    rng = np.random.default_rng(99)
+    ck = {c: rng.standard_normal((n, d)).astype(np.float32) for c, n in chunks.items()}
+    cv = {c: rng.standard_normal((n, d)).astype(np.float32) for c, n in chunks.items()}
+    q = rng.standard_normal((len(paths), 1, d)).astype(np.float32)
+    # page the tree with block size 1: every chunk row is one physical block
+    ids, nxt = {}, 0
+    for c, n in chunks.items():
+        ids[c] = list(range(nxt, nxt + n))
+        nxt += n
+    kc = np.zeros((nxt, 1, 1, d), np.float32)
+    vc = np.zeros_like(kc)
+    for c in chunks:
+        kc[ids[c], 0, 0] = ck[c]
+        vc[ids[c], 0, 0] = cv[c]
+    lens = [sum(chunks[c] for c in p) for p in paths]
+    width = max(lens)
+    tables = np.full((len(paths), width), -1, np.int32)
+    for r, p in enumerate(paths):
+        row = sum((ids[c] for c in p), [])
+        tables[r, :len(row)] = row
+    scale = 1.0 / math.sqrt(d)
+    out, lse = oracle.paged_decode(q, kc, vc, tables, np.array(lens, np.int32), scale)
+    # the page's counts
+    lo, un = oracle.row_ledger(tables, np.array(lens, np.int32), nxt, 1)
+    assert (lo, un, lo - un) == (int(want["logical"]), int(want["unique"]), int(want["saved"]))
+    cover = {c: sum(c in p for p in paths) for c in chunks}
+    assert sum(v for v in cover.values() if v > 1) == int(want["partial_rows"])
+    # Hydragen coordinates: attention per chunk with its LSE, then the merge
+    qd = q.astype(np.float64)
+    for r, p in enumerate(paths):
+        parts = []
+        for c in p:
+            s = scale * (ck[c].astype(np.float64) @ qd[r, 0])
+            l = logsumexp(s)
+            parts.append((np.exp(s - l) @ cv[c].astype(np.float64), l))
+        o, l = _lse_merge(parts)
+        # the page reports agreement within 2.3e-16 on its values; these are
+        # other values of magnitude ~1, so allow a few units in the last place
+        assert np.abs(o - out[r, 0]).max() <= 1e-15
+        assert abs(l - lse[r, 0]) <= 4e-16 * max(1.0, abs(l))
+
+
+def test_loop10_shared_work_ledger():
+    row = next(r for r in _rows("ledgers.txt") if r[0] == "loop10")
+    prefix = int(row[2])
+    i = row.index("suffixes")
+    j = row.index("logical")
+    suffixes = [int(x) for x in row[i + 1:j]]
+    logical, unique, saved = int(row[j + 1]), int(row[row.index("unique") + 1]), int(row[-1])
+    for p in (16, 32, 64):
+        npre = prefix // p
+        nxt = npre
+        tables, lens = [], []
+        for u in suffixes:
+            own = list(range(nxt, nxt + oracle.num_blocks(u, p)))
+            nxt += len(own)
+            tables.append(list(range(npre)) + own)
+            lens.append(prefix + u)
+        width = max(len(t) for t in tables)
+        bt = np.array([t + [-1] * (width - len(t)) for t in tables], np.int32)
+        lo, un = oracle.row_ledger(bt, np.array(lens, np.int32), nxt, p)
+        assert (lo, un, lo - un) == (logical, unique, saved)
