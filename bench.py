@@ -1,0 +1,428 @@
+"""Benchmark of the paged-KV decode step on GB300.
+
+A step is one pass of the decode hot path over one batch: kv_append of each
+sequence's newest K/V row, then paged_attention_decode (split-K partial kernel
+plus log-sum-exp reduction).  Default workload: the Llama-3-8B-shaped decode
+layer (bf16, batch 64, 32/8 heads, head_dim 128, block size 16, lengths
+uniform in [512, 8192], 1.25x pool from a shuffled free FIFO).
+
+Prints one JSON line (rank 0).  `value` is decode KV GB/s: algorithmic K/V
+bytes of the visible rows (4096 B per token row for this layer) per step over
+the device-timed step time.  `e2e` is the same metric through the C ABI with
+the per-step inputs copied from pinned host memory and the output read back
+inside the timed region.
+
+--impl reference times the CPU oracle on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import signal
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOADS = ("llama", "long_bs16", "long_bs64", "shared")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--workload", default="llama", choices=WORKLOADS)
+    ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", 6800.0)), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_traffic(kernel_file, summary):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    src = os.path.join(ROOT, "paged_kv_cache_41_gb300", "csrc", "kernels", kernel_file)
+    summ = os.path.join(ROOT, "profiles", summary)
+    if not (os.path.exists(src) and os.path.exists(summ)):
+        return None
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    text = open(summ).read()
+    m_h = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+    m_t = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_h or not m_t or m_h.group(1) != h:
+        return None
+    return float(m_t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"pkv_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.send_signal(signal.SIGTERM)
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for ln in open(self.path):
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_setup(args):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def all_max(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def make_batch(name, device, seed_offset=0):
+    from paged_kv_cache_41_gb300 import workloads as wl
+    if name == "llama":
+        return wl.llama_batch(device=device, seed=2 + seed_offset)
+    if name == "long_bs16":
+        return wl.long_batch(device=device, block_size=16, seed=3 + seed_offset)
+    if name == "long_bs64":
+        return wl.long_batch(device=device, block_size=64, seed=3 + seed_offset)
+    raise ValueError(name)
+
+
+def kv_row_bytes(b):
+    return 2 * b.num_kv_heads * b.head_dim * (2 if b.dtype == "bf16" else 4)
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+def oracle_sample(b, seconds, nthreads):
+    """Time the CPU oracle decoding whole sequences of the batch until about
+    `seconds` of CPU work; returns (kv_bytes, rows, elapsed, sample description)."""
+    import oracle
+    from paged_kv_cache_41_gb300 import workloads as wl
+    order = np.random.default_rng(0).permutation(b.num_seqs)
+    kh_all, vh_all = b.k_hist, b.v_hist
+    q_all = wl.to_numpy_storage(b.q)
+    shape_blk = (b.block_size, b.num_kv_heads, b.head_dim)
+    done_bytes = done_rows = 0
+    elapsed = 0.0
+    used = []
+    for r in order:
+        t = int(b.seq_lens[r])
+        lo, hi = int(b.hist_offsets[r]), int(b.hist_offsets[r + 1])
+        nblk = max(1, oracle.num_blocks(t, b.block_size))
+        # a private pool holding only this sequence, paged through its own table
+        table = np.arange(nblk, dtype=np.int32)
+        kh = wl.to_numpy_storage(kh_all[lo:hi])
+        vh = wl.to_numpy_storage(vh_all[lo:hi])
+        kc = np.zeros((nblk,) + shape_blk, dtype=kh.dtype)
+        vc = np.zeros_like(kc)
+        slots = np.array([oracle.slot_for_position(table, b.block_size, i) for i in range(t)],
+                         np.int64)
+        oracle.kv_append(kc, vc, kh, vh, slots)
+        q = np.ascontiguousarray(q_all[r:r + 1])
+        t0 = time.perf_counter()
+        oracle.paged_decode(q, kc, vc, table.reshape(1, -1), np.array([t], np.int32), b.scale,
+                            nthreads=nthreads)
+        elapsed += time.perf_counter() - t0
+        done_bytes += t * kv_row_bytes(b)
+        done_rows += 1
+        used.append(int(r))
+        if elapsed >= seconds:
+            break
+    desc = (f"{done_rows} of {b.num_seqs} sequences ({done_bytes / 1e6:.1f} MB of K/V), "
+            f"all {b.num_q_heads} heads, fp64 oracle")
+    return done_bytes, done_rows, elapsed, desc
+
+
+def cpu_baseline(b, seconds):
+    nthreads = len(os.sched_getaffinity(0))
+    nbytes, rows, el, desc = oracle_sample(b, seconds, nthreads)
+    return {"value": nbytes / el / 1e9, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+            "sample": desc, "rows_per_s": rows / el}
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_pkv(args, rank, world, local):
+    import torch
+    from paged_kv_cache_41_gb300 import pkv
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    pkv.load_library()
+    b = make_batch(args.workload, dev, seed_offset=rank)
+    B = b.num_seqs
+    shape = (b.num_blocks, b.block_size, b.num_kv_heads, b.head_dim)
+    dt = b.k_hist.dtype
+    kc = torch.zeros(shape, dtype=dt, device=dev)
+    vc = torch.zeros(shape, dtype=dt, device=dev)
+    slots = torch.from_numpy(b.slots).to(dev)
+    pre = torch.from_numpy(b.prefill_rows()).to(dev)
+    pkv.kv_append(kc, vc, b.k_hist[pre], b.v_hist[pre], slots[pre])
+    last_np = b.last_rows()
+    last = torch.from_numpy(last_np).to(dev)
+    new_k = b.k_hist[last].contiguous()
+    new_v = b.v_hist[last].contiguous()
+    step_slots = slots[last].contiguous()
+    bt = torch.from_numpy(b.block_tables).to(dev)
+    sl = torch.from_numpy(b.seq_lens).to(dev)
+    q = b.q.contiguous()
+    out = torch.empty_like(q)
+    psize = args.partition_size
+    if psize == 0:
+        psize = pkv.decode_auto_partition(kc, B, b.num_q_heads, b.max_blocks)
+    ws_bytes = pkv.decode_workspace_bytes(kc, B, b.num_q_heads, b.max_blocks, psize)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    del b.k_hist, b.v_hist
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    stream = torch.cuda.current_stream()
+
+    def step():
+        pkv.kv_append(kc, vc, new_k, new_v, step_slots)
+        pkv.paged_attention_decode(q, kc, vc, bt, sl, b.scale, out=out, partition_size=psize,
+                                   workspace=ws)
+
+    kv_bytes = int(b.seq_lens.astype(np.int64).sum()) * kv_row_bytes(b)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        ea, eb, ec = ev[i]
+        ea.record(stream)
+        pkv.kv_append(kc, vc, new_k, new_v, step_slots)
+        eb.record(stream)
+        pkv.paged_attention_decode(q, kc, vc, bt, sl, b.scale, out=out, partition_size=psize,
+                                   workspace=ws)
+        ec.record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = all_max(t0.elapsed_time(t1), world)
+    decode_ms = float(np.mean([ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]))
+    append_ms = float(np.mean([ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]))
+    assert pkv.get_device_error() == 0
+    ms_step = total_ms / args.steps
+
+    # ---- end to end through the C ABI with host buffers
+    h_q = q.cpu().pin_memory()
+    h_k = new_k.cpu().pin_memory()
+    h_v = new_v.cpu().pin_memory()
+    h_slots = step_slots.cpu().pin_memory()
+    h_bt = bt.cpu().pin_memory()
+    h_sl = sl.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(new_k), torch.empty_like(new_v)
+    d_slots, d_bt, d_sl = torch.empty_like(step_slots), torch.empty_like(bt), torch.empty_like(sl)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_bt, h_sl))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        d_slots.copy_(h_slots, non_blocking=True)
+        d_bt.copy_(h_bt, non_blocking=True)
+        d_sl.copy_(h_sl, non_blocking=True)
+        pkv.kv_append(kc, vc, d_k, d_v, d_slots)
+        pkv.paged_attention_decode(d_q, kc, vc, d_bt, d_sl, b.scale, out=out,
+                                   partition_size=psize, workspace=ws)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = all_max(s0.elapsed_time(s1), world) / args.steps
+    assert pkv.get_device_error() == 0
+
+    peak, peak_kind = load_peaks()
+    achieved = kv_bytes / (decode_ms * 1e-3) / 1e9
+    traffic = kernel_traffic("decode.cu", "decode_partial_llama.md") if args.workload == "llama" else None
+    parts = math.ceil(b.max_blocks * b.block_size / psize)
+    res = {
+        "metric": "paged-decode KV GB/s (% of HBM peak) and decode rows/s at 1 GB300",
+        "value": world * kv_bytes / (ms_step * 1e-3) / 1e9,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": b.dtype,
+        "data": "synthetic (seeded N(0,1) q/k/v, seeded lengths and block placement)",
+        "config": {
+            "workload": {"llama": "llama3-8b-shaped decode layer",
+                         "long_bs16": "long-context decode, block size 16",
+                         "long_bs64": "long-context decode, block size 64"}[args.workload],
+            "batch": B, "num_q_heads": b.num_q_heads, "num_kv_heads": b.num_kv_heads,
+            "head_dim": b.head_dim, "block_size": b.block_size,
+            "seq_len_min": int(b.seq_lens.min()), "seq_len_max": int(b.seq_lens.max()),
+            "total_tokens": int(b.seq_lens.sum()), "pool_blocks": b.num_blocks,
+            "partition_size": psize, "max_partitions": parts,
+            "kv_bytes_per_step": kv_bytes,
+            "l2": "inputs larger than L2 (K/V read per step >> 129 MB)",
+            "parallelism": f"replicas x{world} (sequences shard, no collective)",
+        },
+        "rows_per_s": world * B / (ms_step * 1e-3),
+        "pct_of_hbm_peak": 100.0 * (kv_bytes / (ms_step * 1e-3) / 1e9) / peak,
+        "decode_ms": decode_ms,
+        "append_ms": append_ms,
+        "roofline": {"bound": "hbm", "kernel": "decode_partial_kernel + decode_reduce_kernel",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs (copy)",
+                     "traffic": traffic,
+                     "algorithmic_bytes_per_launch": kv_bytes},
+        "e2e": {"value": world * kv_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * (2 if parts <= 1 else 3),
+        "clocks": clk,
+    }
+    return res, b
+
+
+def main():
+    args = parse()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_setup(args)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        res = run_reference(args)
+        print(json.dumps(res), flush=True)
+        return
+    res, b = run_pkv(args, rank, world, local)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            cb = cpu_baseline(b, args.cpu_sample_seconds)
+            res["cpu_baseline"] = cb
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The CPU oracle, as it stands, on bounded samples of the same workload."""
+    b = make_batch(args.workload, "cpu")
+    nthreads = len(os.sched_getaffinity(0))
+    per_step = max(1.0, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(b, per_step / 4, nthreads)
+    tot_b = tot_r = tot_t = 0.0
+    desc = ""
+    for _ in range(args.steps):
+        nb_, nr_, el, desc = oracle_sample(b, per_step, nthreads)
+        tot_b += nb_
+        tot_r += nr_
+        tot_t += el
+    v = tot_b / tot_t / 1e9
+    return {
+        "impl": "reference",
+        "metric": "paged-decode KV GB/s (% of HBM peak) and decode rows/s at 1 GB300",
+        "value": v, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload},
+        "rows_per_s": tot_r / tot_t,
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+                         "sample": f"per step: {desc}"},
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,154 @@
+/*
+ * pkv.h -- C ABI of libpkv: attention decode over a paged KV cache on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * A request's logically contiguous K/V history lives in fixed-size physical
+ * blocks of `block_size` token rows scattered through one pool; a per-request
+ * block table maps logical block j to a physical block id, and the last block
+ * holds a valid-row tail ("M5.3 - KV Memory Layout and Exact Reuse", 0x03A,
+ * 0x03C, 0x0A; "7. Memory Management and Local Model State", "Logical tokens,
+ * physical blocks").
+ *
+ * CACHE LAYOUT.  One layer; K and V are separate device tensors with the
+ * declared row-major axis order [num_blocks, block_size, num_kv_heads,
+ * head_dim] (the token-major order of the checked address trace in M5.3
+ * 0x03F, without its layer axis; strides follow 0x03E).  Element (b, o, h, c)
+ * sits at ((b * block_size + o) * num_kv_heads + h) * head_dim + c.  All
+ * offsets are computed in 64-bit integers ("Cache Concepts: Prefix Matching
+ * vs. Storage": widen page ids to int64 before multiplying by pool strides).
+ *
+ * CONVENTIONS (every call).
+ *   - Every pointer argument is a DEVICE pointer unless stated otherwise; the
+ *     caller allocates and owns all device memory.  The library allocates
+ *     nothing and keeps no state between calls except one device error word
+ *     per device (see pkv_get_device_error).
+ *   - Every call is asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *     default stream) and returns after enqueuing its kernels.
+ *   - Arguments are validated on the host before any launch; a rejected call
+ *     launches nothing and returns PKV_ERR_INVALID_ARG or PKV_ERR_UNSUPPORTED.
+ *   - Device data the host cannot see (slot ids, block ids, lengths) is
+ *     checked by the kernels: an out-of-range item sets a bit of the device
+ *     error word and is skipped.  No kernel traps, asserts or waits without a
+ *     time limit.
+ *   - dtype is PKV_F32 or PKV_BF16; q, k, v, caches and out share it.
+ *     Attention arithmetic is fp32 (accumulators, softmax state) whatever the
+ *     storage type; bf16 results are rounded to nearest even.
+ *   - Pointers to the caches, q, k, v and out must be 16-byte aligned.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,  /* bad pointer, size, shape or workspace        */
+  PKV_ERR_UNSUPPORTED = 2,  /* valid but not compiled (head_dim, group ...) */
+  PKV_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed          */
+  PKV_ERR_DEVICE = 4        /* pkv_get_device_error found a device-side error */
+} pkv_status;
+
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Bits of the device error word. */
+#define PKV_DEVERR_SLOT 1u     /* a slot id >= num_blocks * block_size          */
+#define PKV_DEVERR_BLOCK 2u    /* a block id outside [0, num_blocks)             */
+#define PKV_DEVERR_LENGTH 4u   /* a length < 0 or beyond its block table row     */
+#define PKV_DEVERR_TIMEOUT 8u  /* a bounded wait inside a kernel ran out         */
+
+/* Shape of one paged K/V pool (host struct, passed by pointer). */
+typedef struct {
+  int64_t num_blocks;   /* physical blocks in the pool, >= 1                   */
+  int32_t block_size;   /* token rows per block (P)                            */
+  int32_t num_kv_heads; /* KV heads per token row (Hkv)                        */
+  int32_t head_dim;     /* elements per head (D)                               */
+  int32_t dtype;        /* pkv_dtype                                           */
+} pkv_cache_desc;
+
+/* Write new token rows into their slots (K/V append scatter).
+ *   k, v:          [num_tokens, Hkv, D] rows to write.
+ *   slot_mapping:  int64 [num_tokens]; row i goes to slot s = slot_mapping[i],
+ *                  i.e. block s / P, offset s % P.  s < 0 skips the row (the
+ *                  -1 skip sentinel of "Cache Concepts: Prefix Matching vs.
+ *                  Storage"); s >= num_blocks * P sets PKV_DEVERR_SLOT and
+ *                  skips it.  Slots must be distinct (one writer per slot).
+ * The slot invariant table[req, pos // P] * P + pos % P and the append paths
+ * follow M5.3 0x03D and 0x04E.  Any block_size >= 1; Hkv * D * elem must be a
+ * multiple of 16 bytes.  Result is bit-exact (a byte copy). */
+pkv_status pkv_kv_append(const pkv_cache_desc* cache, void* k_cache,
+                         void* v_cache, const void* k, const void* v,
+                         const int64_t* slot_mapping, int64_t num_tokens,
+                         void* stream);
+
+/* Copy-on-write block copy (M5.3 0x04C, 0x05A; the fused block-copy kernel of
+ * PagedAttention): for each pair i, the whole block src = pairs[2i] of K and V
+ * is copied to block dst = pairs[2i + 1].
+ *   src_dst_pairs: int64 [num_pairs, 2].  Destinations must be pairwise
+ *                  distinct and no destination may also be a source in the
+ *                  same call (pairs run in parallel); ids outside the pool
+ *                  set PKV_DEVERR_BLOCK and the pair is skipped.
+ * Bit-exact. */
+pkv_status pkv_kv_block_copy(const pkv_cache_desc* cache, void* k_cache,
+                             void* v_cache, const int64_t* src_dst_pairs,
+                             int64_t num_pairs, void* stream);
+
+/* Bytes of device workspace pkv_paged_attention_decode needs for these sizes
+ * (0 when one partition covers every sequence).  partition_size as below. */
+size_t pkv_decode_workspace_bytes(const pkv_cache_desc* cache, int32_t num_seqs,
+                                  int32_t num_q_heads,
+                                  int32_t max_blocks_per_seq,
+                                  int32_t partition_size);
+
+/* Partition size (tokens) the library picks when partition_size == 0. */
+int32_t pkv_decode_auto_partition(const pkv_cache_desc* cache, int32_t num_seqs,
+                                  int32_t num_q_heads,
+                                  int32_t max_blocks_per_seq);
+
+/* Paged attention decode (M5.3 0x0A, 0x0BA): one query row per sequence and
+ * query head against the sequence's full logical history,
+ *   out[r, h] = sum_t softmax_t(scale * q[r, h] . K_r[t]) V_r[t],
+ *   lse[r, h] = log sum_t exp(scale * q[r, h] . K_r[t]),
+ * where K_r[t], V_r[t] is token row t < seq_lens[r] of kv head
+ * h / (Hq / Hkv), found in block block_tables[r, t / P] at offset t % P.  Rows
+ * at offsets >= the request's tail are never read (M5.3 0x03G).
+ *   out:           [num_seqs, Hq, D] (cache dtype).
+ *   lse:           float [num_seqs, Hq] natural-log LSE, or NULL.  An empty
+ *                  sequence gives out = 0 and lse = -inf.
+ *   q:             [num_seqs, Hq, D].
+ *   block_tables:  int32 [num_seqs, max_blocks_per_seq]; entries past
+ *                  ceil(seq_lens[r] / P) are never read.
+ *   seq_lens:      int32 [num_seqs].
+ *   partition_size: tokens per split-K partition (a multiple of block_size),
+ *                  or 0 for the library's choice.  A sequence is split into
+ *                  ceil(T / partition_size) partitions whose (output, LSE)
+ *                  states are merged by log-sum-exp in a second kernel
+ *                  (M5.3 0x0A: allocator block, kernel block and reduction
+ *                  partition are three levels).
+ *   workspace:     device scratch of at least pkv_decode_workspace_bytes
+ *                  bytes (may be NULL when that is 0), 256-byte aligned.
+ * Supported: block_size a multiple of 16 in [16, 256]; head_dim 64 or 128;
+ * Hq / Hkv in {1, 2, 4, 8}; num_seqs <= 65535. */
+pkv_status pkv_paged_attention_decode(
+    const pkv_cache_desc* cache, void* out, float* lse, const void* q,
+    const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
+    int32_t num_q_heads, float scale, int32_t partition_size, void* workspace,
+    size_t workspace_bytes, void* stream);
+
+/* Read and clear the device error word of the current device.  Synchronises
+ * `stream` first.  *code_out receives the PKV_DEVERR_* bits seen since the
+ * last call.  Returns PKV_ERR_DEVICE if any bit was set, else PKV_OK. */
+pkv_status pkv_get_device_error(int32_t* code_out, void* stream);
+
+/* Static string for a status code. */
+const char* pkv_status_string(pkv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

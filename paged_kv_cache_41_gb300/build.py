@@ -85,7 +85,7 @@ def build_cuda(force=False, extra_flags=()) -> str:
         msg = "\n".join(f"--- {s}\n{o}" for s, o in failed)
         raise RuntimeError(f"nvcc failed:\n{msg}")
     tmp = LIB + ".tmp"
-    subprocess.check_call([NVCC, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"])
+    subprocess.check_call([NVCC, *ARCH, "-shared", "-o", tmp, *objs])
     os.replace(tmp, LIB)
     return LIB
 

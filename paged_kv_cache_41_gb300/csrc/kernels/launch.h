@@ -1,0 +1,56 @@
+// launch.h -- internal launchers behind the libpkv C ABI (not exported).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k, const void* v,
+                             const int64_t* slots, int64_t num_tokens, int64_t num_slots,
+                             int64_t row_bytes, unsigned int* err, cudaStream_t stream);
+
+cudaError_t launch_kv_block_copy(void* k_cache, void* v_cache, const int64_t* pairs,
+                                 int64_t num_pairs, int64_t num_blocks, int64_t block_bytes,
+                                 unsigned int* err, cudaStream_t stream);
+
+// Arguments of the split-K paged decode kernels.
+struct DecodeArgs {
+  const void* q;                // [B, Hq, D]
+  const int32_t* block_tables;  // [B, max_blocks]
+  const int32_t* seq_lens;      // [B]
+  float* part_o;                // [B, Hq, parts_stride, D] normalised partial outputs
+  float* part_lse;              // [B, Hq, parts_stride] partial LSE, base 2
+  void* out;                    // [B, Hq, D]
+  float* lse_out;               // [B, Hq] natural log, or null
+  unsigned int* err;
+  int64_t num_blocks;
+  int32_t max_blocks;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t block_size;
+  int32_t blocks_per_part;
+  int32_t max_parts;     // partitions per sequence at most (grid.y)
+  int32_t part_offset;   // partial slots before the first decode partition
+  int32_t parts_stride;  // partial slots per (sequence, head)
+  int32_t num_stages;
+  float qscale;          // softmax scale * log2(e)
+  int32_t direct;        // 1: a single partition per sequence writes out/lse itself
+};
+
+// Launch the partial kernel (and the LSE reduction unless args.direct).
+cudaError_t launch_paged_decode(int dtype, int head_dim, int group, const CUtensorMap& tmk,
+                                const CUtensorMap& tmv, const DecodeArgs& args,
+                                cudaStream_t stream);
+
+// LSE reduction over the partial states (also used after the shared prefix).
+cudaError_t launch_decode_reduce(int dtype, int head_dim, const DecodeArgs& args,
+                                 cudaStream_t stream);
+
+// Stage count and dynamic shared memory of the partial kernel.
+int decode_num_stages(int block_size, int head_dim, int elem_bytes);
+size_t decode_smem_bytes(int block_size, int head_dim, int elem_bytes, int group, int stages);
+
+}  // namespace pkv

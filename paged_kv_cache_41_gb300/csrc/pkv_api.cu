@@ -1,0 +1,276 @@
+// pkv_api.cu -- the C ABI of libpkv: host-side validation, TMA descriptors,
+// workspace sizing, the per-device error word and the kernel launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <math.h>
+#include <mutex>
+
+#include "kernels/launch.h"
+#include "pkv.h"
+
+namespace {
+
+// One error word per device; kernels get its device address.
+__device__ unsigned int g_device_error;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int* g_err_ptr[kMaxDevices] = {};
+
+unsigned int* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+int elem_bytes(int dtype) { return dtype == PKV_BF16 ? 2 : 4; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pkv_status check_cache(const pkv_cache_desc* c) {
+  if (!c) return PKV_ERR_INVALID_ARG;
+  if (c->num_blocks <= 0 || c->block_size <= 0 || c->num_kv_heads <= 0 || c->head_dim <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (c->dtype != PKV_F32 && c->dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  return PKV_OK;
+}
+
+// Shapes the attention kernels are compiled for.
+pkv_status check_attention_shape(const pkv_cache_desc* c, int32_t num_q_heads) {
+  if (c->head_dim != 64 && c->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  const int P = c->block_size;
+  if (P % 16 != 0 || P > 256 || (P > 64 && P % 64 != 0)) return PKV_ERR_UNSUPPORTED;
+  if (num_q_heads <= 0 || num_q_heads % c->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  const int G = num_q_heads / c->num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return PKV_ERR_UNSUPPORTED;
+  if (c->num_kv_heads > 65535 || c->num_blocks > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  return PKV_OK;
+}
+
+// 4-D map over the pool [NB, P, Hkv, D] whose box is one kv head x `rows`
+// token rows x head_dim.
+pkv_status encode_cache_map(CUtensorMap* map, const pkv_cache_desc* c, const void* base,
+                            int rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return PKV_ERR_CUDA;
+  const cuuint64_t es = (cuuint64_t)elem_bytes(c->dtype);
+  cuuint64_t dims[4] = {(cuuint64_t)c->head_dim, (cuuint64_t)c->num_kv_heads,
+                        (cuuint64_t)c->block_size, (cuuint64_t)c->num_blocks};
+  cuuint64_t strides[3] = {dims[0] * es, dims[0] * dims[1] * es, dims[0] * dims[1] * dims[2] * es};
+  cuuint32_t box[4] = {(cuuint32_t)c->head_dim, 1, (cuuint32_t)rows, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, c->dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                   4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_UNSUPPORTED;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
+int32_t auto_partition(const pkv_cache_desc* c, int32_t num_seqs, int32_t max_blocks) {
+  // Enough CTAs (kv head x partition x sequence) for several waves of the
+  // ~3 resident CTAs per SM, without splitting rows finer than 16 blocks.
+  const int64_t target = (int64_t)sm_count() * 3 * 4;
+  const int64_t rows = (int64_t)num_seqs * c->num_kv_heads;
+  int32_t bpp = max_blocks > 0 ? max_blocks : 1;
+  const int32_t min_bpp = c->block_size >= 64 ? 4 : 16;
+  while (bpp > min_bpp && rows * ((max_blocks + bpp - 1) / bpp) < target) bpp = (bpp + 1) / 2;
+  if (bpp < 1) bpp = 1;
+  return bpp * c->block_size;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Partial-state workspace: [B, Hq, parts] x (D floats of output + 1 LSE).
+size_t partial_bytes(int64_t rows, int64_t parts, int64_t head_dim) {
+  return align256((size_t)(rows * parts * head_dim) * 4) + align256((size_t)(rows * parts) * 4);
+}
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_DEVICE: return "device-side error reported by a kernel";
+  }
+  return "unknown status";
+}
+
+pkv_status pkv_kv_append(const pkv_cache_desc* cache, void* k_cache, void* v_cache,
+                         const void* k, const void* v, const int64_t* slot_mapping,
+                         int64_t num_tokens, void* stream) {
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0) return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !k || !v || !slot_mapping) return PKV_ERR_INVALID_ARG;
+  const int64_t row_bytes = (int64_t)cache->num_kv_heads * cache->head_dim * elem_bytes(cache->dtype);
+  if (row_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k) || !aligned16(v))
+    return PKV_ERR_INVALID_ARG;
+  if ((num_tokens + 7) / 8 > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  unsigned int* err = device_error_word();
+  if (!err) return PKV_ERR_CUDA;
+  cudaError_t e = pkv::launch_kv_append(k_cache, v_cache, k, v, slot_mapping, num_tokens,
+                                        cache->num_blocks * cache->block_size, row_bytes, err,
+                                        as_stream(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_kv_block_copy(const pkv_cache_desc* cache, void* k_cache, void* v_cache,
+                             const int64_t* src_dst_pairs, int64_t num_pairs, void* stream) {
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (num_pairs < 0) return PKV_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !src_dst_pairs) return PKV_ERR_INVALID_ARG;
+  const int64_t block_bytes = (int64_t)cache->block_size * cache->num_kv_heads * cache->head_dim *
+                              elem_bytes(cache->dtype);
+  if (block_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_INVALID_ARG;
+  if (num_pairs > INT32_MAX || block_bytes / 16 / 1024 + 1 > 65535) return PKV_ERR_UNSUPPORTED;
+  unsigned int* err = device_error_word();
+  if (!err) return PKV_ERR_CUDA;
+  cudaError_t e = pkv::launch_kv_block_copy(k_cache, v_cache, src_dst_pairs, num_pairs,
+                                            cache->num_blocks, block_bytes, err, as_stream(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int32_t pkv_decode_auto_partition(const pkv_cache_desc* cache, int32_t num_seqs,
+                                  int32_t num_q_heads, int32_t max_blocks_per_seq) {
+  (void)num_q_heads;
+  if (check_cache(cache) != PKV_OK || max_blocks_per_seq <= 0 || num_seqs <= 0) return 0;
+  return auto_partition(cache, num_seqs, max_blocks_per_seq);
+}
+
+size_t pkv_decode_workspace_bytes(const pkv_cache_desc* cache, int32_t num_seqs,
+                                  int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                  int32_t partition_size) {
+  if (check_cache(cache) != PKV_OK || num_seqs <= 0 || num_q_heads <= 0 ||
+      max_blocks_per_seq <= 0 || partition_size < 0)
+    return 0;
+  if (partition_size == 0) partition_size = auto_partition(cache, num_seqs, max_blocks_per_seq);
+  if (partition_size % cache->block_size != 0) return 0;
+  const int64_t bpp = partition_size / cache->block_size;
+  const int64_t parts = (max_blocks_per_seq + bpp - 1) / bpp;
+  if (parts <= 1) return 0;
+  return partial_bytes((int64_t)num_seqs * num_q_heads, parts, cache->head_dim);
+}
+
+pkv_status pkv_paged_attention_decode(const pkv_cache_desc* cache, void* out, float* lse,
+                                      const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* seq_lens, int32_t num_seqs,
+                                      int32_t num_q_heads, float scale, int32_t partition_size,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || max_blocks_per_seq <= 0 || partition_size < 0 || !isfinite(scale))
+    return PKV_ERR_INVALID_ARG;
+  if ((st = check_attention_shape(cache, num_q_heads)) != PKV_OK) return st;
+  if (num_seqs == 0) return PKV_OK;
+  if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_INVALID_ARG;
+  if (partition_size == 0) partition_size = auto_partition(cache, num_seqs, max_blocks_per_seq);
+  if (partition_size % cache->block_size != 0) return PKV_ERR_INVALID_ARG;
+  const int32_t bpp = partition_size / cache->block_size;
+  const int64_t parts = (max_blocks_per_seq + (int64_t)bpp - 1) / bpp;
+  if (parts > 65535) return PKV_ERR_UNSUPPORTED;
+  const size_t need = parts > 1 ? partial_bytes((int64_t)num_seqs * num_q_heads, parts,
+                                                cache->head_dim) : 0;
+  if (workspace_bytes < need || (need > 0 && !workspace)) return PKV_ERR_INVALID_ARG;
+  if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PKV_ERR_INVALID_ARG;
+
+  const int rows = cache->block_size < 64 ? cache->block_size : 64;
+  CUtensorMap tmk, tmv;
+  if ((st = encode_cache_map(&tmk, cache, k_cache, rows)) != PKV_OK) return st;
+  if ((st = encode_cache_map(&tmv, cache, v_cache, rows)) != PKV_OK) return st;
+  unsigned int* err = device_error_word();
+  if (!err) return PKV_ERR_CUDA;
+
+  pkv::DecodeArgs a{};
+  a.q = q;
+  a.block_tables = block_tables;
+  a.seq_lens = seq_lens;
+  const size_t rows_parts = (size_t)num_seqs * num_q_heads * (size_t)parts;
+  a.part_o = need ? static_cast<float*>(workspace) : nullptr;
+  a.part_lse = need ? reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) +
+                                               align256(rows_parts * cache->head_dim * 4))
+                    : nullptr;
+  a.out = out;
+  a.lse_out = lse;
+  a.err = err;
+  a.num_blocks = cache->num_blocks;
+  a.max_blocks = max_blocks_per_seq;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.block_size = cache->block_size;
+  a.blocks_per_part = bpp;
+  a.max_parts = (int32_t)parts;
+  a.part_offset = 0;
+  a.parts_stride = (int32_t)parts;
+  a.num_stages = pkv::decode_num_stages(cache->block_size, cache->head_dim, elem_bytes(cache->dtype));
+  a.qscale = scale * 1.4426950408889634f;
+  a.direct = parts <= 1 ? 1 : 0;
+  cudaError_t e = pkv::launch_paged_decode(cache->dtype, cache->head_dim,
+                                           num_q_heads / cache->num_kv_heads, tmk, tmv, a,
+                                           as_stream(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_get_device_error(int32_t* code_out, void* stream) {
+  if (!code_out) return PKV_ERR_INVALID_ARG;
+  unsigned int* err = device_error_word();
+  if (!err) return PKV_ERR_CUDA;
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return PKV_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpy(&v, err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return PKV_ERR_CUDA;
+  const unsigned int zero = 0;
+  if (cudaMemcpy(err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  *code_out = (int32_t)v;
+  return v ? PKV_ERR_DEVICE : PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,172 @@
+"""Thin Python binding of libpkv (``include/pkv.h``) with the same names.
+
+Argument marshalling only: torch tensors supply device memory and the current
+CUDA stream; every step of the computation runs in the library's kernels.
+There is no fallback: if ``libpkv.so`` is missing or a call is rejected, the
+binding raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA, PKV_ERR_DEVICE = range(5)
+PKV_F32, PKV_BF16 = 0, 1
+DEVERR_SLOT, DEVERR_BLOCK, DEVERR_LENGTH, DEVERR_TIMEOUT = 1, 2, 4, 8
+
+EXPORTED = [
+    "pkv_kv_append",
+    "pkv_kv_block_copy",
+    "pkv_decode_workspace_bytes",
+    "pkv_decode_auto_partition",
+    "pkv_paged_attention_decode",
+    "pkv_get_device_error",
+    "pkv_status_string",
+]
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load_library():
+    """Load libpkv.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing; build it with paged_kv_cache_41_gb300.build")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+    dp = ctypes.POINTER(CacheDesc)
+    lib.pkv_kv_append.restype = ctypes.c_int
+    lib.pkv_kv_append.argtypes = [dp, vp, vp, vp, vp, vp, i64, vp]
+    lib.pkv_kv_block_copy.restype = ctypes.c_int
+    lib.pkv_kv_block_copy.argtypes = [dp, vp, vp, vp, i64, vp]
+    lib.pkv_decode_workspace_bytes.restype = ctypes.c_size_t
+    lib.pkv_decode_workspace_bytes.argtypes = [dp, i32, i32, i32, i32]
+    lib.pkv_decode_auto_partition.restype = i32
+    lib.pkv_decode_auto_partition.argtypes = [dp, i32, i32, i32]
+    lib.pkv_paged_attention_decode.restype = ctypes.c_int
+    lib.pkv_paged_attention_decode.argtypes = [dp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, f32,
+                                               i32, vp, ctypes.c_size_t, vp]
+    lib.pkv_get_device_error.restype = ctypes.c_int
+    lib.pkv_get_device_error.argtypes = [ctypes.POINTER(i32), vp]
+    lib.pkv_status_string.restype = ctypes.c_char_p
+    lib.pkv_status_string.argtypes = [ctypes.c_int]
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().pkv_status_string(status).decode()
+
+
+def _check(status: int, what: str):
+    if status != PKV_OK:
+        raise PkvError(status, what)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def cache_desc(k_cache: torch.Tensor) -> CacheDesc:
+    """Descriptor of a [num_blocks, block_size, num_kv_heads, head_dim] pool."""
+    if k_cache.dim() != 4 or not k_cache.is_contiguous():
+        raise ValueError("cache must be a contiguous [NB, P, Hkv, D] tensor")
+    if k_cache.dtype == torch.bfloat16:
+        dt = PKV_BF16
+    elif k_cache.dtype == torch.float32:
+        dt = PKV_F32
+    else:
+        raise TypeError(f"unsupported cache dtype {k_cache.dtype}")
+    nb, p, hkv, d = k_cache.shape
+    return CacheDesc(nb, p, hkv, d, dt)
+
+
+def kv_append(k_cache, v_cache, k, v, slot_mapping, stream=None) -> None:
+    """Scatter rows k[i], v[i] ([N, Hkv, D]) into slot slot_mapping[i] (int64)."""
+    desc = cache_desc(k_cache)
+    _check(load_library().pkv_kv_append(ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache),
+                                        _ptr(k.contiguous()), _ptr(v.contiguous()),
+                                        _ptr(slot_mapping), slot_mapping.numel(), _stream(stream)),
+           "pkv_kv_append")
+
+
+def kv_block_copy(k_cache, v_cache, src_dst_pairs, stream=None) -> None:
+    """Copy whole blocks src -> dst for each row of int64 [n, 2] pairs."""
+    desc = cache_desc(k_cache)
+    n = src_dst_pairs.shape[0] if src_dst_pairs.numel() else 0
+    _check(load_library().pkv_kv_block_copy(ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache),
+                                            _ptr(src_dst_pairs), n, _stream(stream)),
+           "pkv_kv_block_copy")
+
+
+def decode_workspace_bytes(k_cache, num_seqs, num_q_heads, max_blocks_per_seq,
+                           partition_size=0) -> int:
+    desc = cache_desc(k_cache)
+    return load_library().pkv_decode_workspace_bytes(ctypes.byref(desc), num_seqs, num_q_heads,
+                                                     max_blocks_per_seq, partition_size)
+
+
+def decode_auto_partition(k_cache, num_seqs, num_q_heads, max_blocks_per_seq) -> int:
+    desc = cache_desc(k_cache)
+    return load_library().pkv_decode_auto_partition(ctypes.byref(desc), num_seqs, num_q_heads,
+                                                    max_blocks_per_seq)
+
+
+def paged_attention_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, *, out=None,
+                           lse=None, partition_size=0, workspace=None, stream=None):
+    """Attention of q [B, Hq, D] over each sequence's paged history.
+
+    block_tables: int32 [B, max_blocks]; seq_lens: int32 [B].  Returns out
+    (and writes lse [B, Hq] float32 when given).  The workspace is allocated
+    here through torch when not supplied.
+    """
+    desc = cache_desc(k_cache)
+    b, hq, _ = q.shape
+    max_blocks = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    need = load_library().pkv_decode_workspace_bytes(ctypes.byref(desc), b, hq, max_blocks,
+                                                     partition_size) if b else 0
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load_library().pkv_paged_attention_decode(
+        ctypes.byref(desc), _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), max_blocks, _ptr(seq_lens), b, hq, float(scale), partition_size,
+        _ptr(workspace), ws_bytes, _stream(stream)), "pkv_paged_attention_decode")
+    return out
+
+
+def get_device_error(stream=None) -> int:
+    """Synchronise, read and clear the device error word (PKV_DEVERR_* bits)."""
+    code = ctypes.c_int32(0)
+    st = load_library().pkv_get_device_error(ctypes.byref(code), _stream(stream))
+    if st not in (PKV_OK, PKV_ERR_DEVICE):
+        raise PkvError(st, "pkv_get_device_error")
+    return code.value

@@ -1,0 +1,187 @@
+"""GPU parity: libpkv (through its C ABI) against the CPU oracle.
+
+Appends and block copies are compared bit for bit over the whole pool
+(including the NaN-poisoned rows nobody wrote); attention outputs and LSEs
+element by element within |gpu - ref| <= 2e-3 + 1e-2 |ref|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_41_gb300 import pkv
+from paged_kv_cache_41_gb300 import workloads as wl
+
+import parity_util as pu
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_batch(b, partition_size=0, rows=None, check_pool=True):
+    kc, vc = pu.device_pool(b)
+    pu.device_fill(b, kc, vc)
+    hk, hv = pu.host_pool(b)
+    pu.oracle_fill(b, hk, hv)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    if check_pool:
+        assert pu.pools_equal_bytes(kc, hk), "K pool differs from the oracle's after kv_append"
+        assert pu.pools_equal_bytes(vc, hv), "V pool differs from the oracle's after kv_append"
+    out, lse = pu.device_decode(b, kc, vc, partition_size)
+    assert pkv.get_device_error() == 0
+    ref, ref_lse = pu.oracle_decode(b, hk, hv, rows)
+    if rows is not None:
+        out, lse = out[rows], lse[rows]
+    pu.assert_close(out, ref, f"{b.name} out")
+    pu.assert_close(lse, ref_lse, f"{b.name} lse")
+    return kc, vc
+
+
+def test_tiny_fp32_append_and_decode():
+    b = wl.tiny_batch(device="cuda")
+    _run_batch(b)
+
+
+@pytest.mark.parametrize("partition_size", [16, 32, 48, 64])
+def test_tiny_fp32_split_k(partition_size):
+    b = wl.tiny_batch(device="cuda")
+    _run_batch(b, partition_size=partition_size)
+
+
+EDGE_LENS = [1, 15, 16, 17, 31, 32, 33, 100, 257, 0, 1000, 64, 2]
+
+
+@pytest.mark.parametrize("dtype,d,hq,hkv,p", [
+    ("bf16", 128, 32, 8, 16), ("bf16", 128, 8, 8, 16), ("bf16", 128, 16, 8, 16),
+    ("bf16", 128, 64, 8, 16), ("bf16", 64, 8, 2, 16), ("f32", 128, 8, 2, 16),
+    ("f32", 64, 4, 2, 16), ("bf16", 128, 32, 8, 64), ("bf16", 128, 32, 8, 32),
+    ("bf16", 128, 32, 8, 128), ("bf16", 64, 16, 4, 256),
+])
+@pytest.mark.parametrize("partition_size", [0, "one_block", "three_blocks", "whole"])
+def test_edge_lengths(dtype, d, hq, hkv, p, partition_size):
+    b = wl.custom_batch(EDGE_LENS, dtype=dtype, hq=hq, hkv=hkv, d=d, p=p, seed=31, device="cuda")
+    ps = {0: 0, "one_block": p, "three_blocks": 3 * p,
+          "whole": b.max_blocks * p}[partition_size]
+    _run_batch(b, partition_size=ps)
+
+
+def test_empty_batch_rows_and_all_empty():
+    b = wl.custom_batch([0, 0, 5], dtype="bf16", hq=8, hkv=2, d=128, p=16, seed=5, device="cuda")
+    _run_batch(b)
+    b = wl.custom_batch([0, 0], dtype="bf16", hq=8, hkv=2, d=128, p=16, num_blocks=4, seed=6,
+                        device="cuda")
+    kc, vc = pu.device_pool(b)
+    out, lse = pu.device_decode(b, kc, vc)
+    assert not out.any() and np.isneginf(lse).all()
+
+
+def test_llama_shaped_full_size_sampled():
+    b = wl.llama_batch(device="cuda")
+    rows = np.unique(np.concatenate([np.argsort(b.seq_lens)[[0, 1, -2, -1]], np.arange(0, 64, 9)]))
+    _run_batch(b, rows=rows)
+
+
+@pytest.mark.parametrize("block_size", [16, 64])
+def test_long_context_full_size_sampled(block_size):
+    b = wl.long_batch(device="cuda", block_size=block_size)
+    rows = np.array([int(np.argmax(b.seq_lens)), int(np.argmin(b.seq_lens))])
+    _run_batch(b, rows=rows)
+
+
+def test_block_copy_bit_exact():
+    b = wl.custom_batch([40, 70, 9], dtype="bf16", hq=8, hkv=2, d=128, p=16, seed=41,
+                        device="cuda")
+    kc, vc = pu.device_pool(b)
+    pu.device_fill(b, kc, vc)
+    hk, hv = pu.host_pool(b)
+    pu.oracle_fill(b, hk, hv)
+    used = set(b.block_tables[b.block_tables >= 0].tolist())
+    free = [i for i in range(b.num_blocks) if i not in used]
+    src = sorted(used)[:4]
+    pairs = np.array(list(zip(src, free[:4])), np.int64)
+    pkv.kv_block_copy(kc, vc, torch.from_numpy(pairs).cuda())
+    assert oracle.kv_block_copy(hk, hv, pairs) == oracle.OK
+    assert pkv.get_device_error() == 0
+    assert pu.pools_equal_bytes(kc, hk) and pu.pools_equal_bytes(vc, hv)
+
+
+def test_shared_prefix_cow_then_append_bit_exact():
+    sp = wl.shared_prefix_batch(device="cuda", batch=16, prefix_len=256, shared_tail=8,
+                                suffix_lo=16, suffix_hi=100, seed=51)
+    shape = (sp.num_blocks, sp.block_size, sp.num_kv_heads, sp.head_dim)
+    kc = torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    pkv.kv_append(kc, vc, sp.parent_k, sp.parent_v, torch.from_numpy(sp.parent_slots).cuda())
+    pkv.kv_block_copy(kc, vc, torch.from_numpy(sp.cow_pairs).cuda())
+    pkv.kv_append(kc, vc, sp.child_k, sp.child_v, torch.from_numpy(sp.child_slots).cuda())
+    hk = np.full(shape, 0x7FC0, np.uint16)
+    hv = np.full(shape, 0x7FC0, np.uint16)
+    n_par = sp.prefix_len + sp.shared_tail
+    ps = np.array([oracle.slot_for_position(sp.parent_table, sp.block_size, t)
+                   for t in range(n_par)], np.int64)
+    oracle.kv_append(hk, hv, wl.to_numpy_storage(sp.parent_k), wl.to_numpy_storage(sp.parent_v), ps)
+    oracle.kv_block_copy(hk, hv, sp.cow_pairs)
+    ck, cv = wl.to_numpy_storage(sp.child_k), wl.to_numpy_storage(sp.child_v)
+    for r in range(sp.num_seqs):
+        table = np.concatenate([sp.prefix_block_ids, sp.suffix_tables[r]])
+        lo, hi = sp.child_offsets[r], sp.child_offsets[r + 1]
+        cs = np.array([oracle.slot_for_position(table, sp.block_size, n_par + i)
+                       for i in range(hi - lo)], np.int64)
+        oracle.kv_append(hk, hv, np.ascontiguousarray(ck[lo:hi]), np.ascontiguousarray(cv[lo:hi]), cs)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    assert pu.pools_equal_bytes(kc, hk) and pu.pools_equal_bytes(vc, hv)
+
+
+# ------------------------------------------------------------------ errors
+def test_bad_slot_sets_error_and_writes_nothing():
+    kc = torch.zeros(4, 16, 2, 64, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    k = torch.ones(3, 2, 64, dtype=torch.bfloat16, device="cuda")
+    slots = torch.tensor([-1, 64, 5], dtype=torch.int64, device="cuda")
+    pkv.kv_append(kc, vc, k, k, slots)
+    assert pkv.get_device_error() == pkv.DEVERR_SLOT
+    flat = kc.view(64, 2, 64)
+    assert (flat[5] == 1).all() and (flat.sum() == 2 * 64)
+    assert pkv.get_device_error() == 0  # read-and-clear
+
+
+def test_bad_block_in_table_and_pair_set_error():
+    b = wl.custom_batch([40, 20], dtype="bf16", hq=8, hkv=2, d=128, p=16, seed=61, device="cuda")
+    kc, vc = pu.device_pool(b)
+    pu.device_fill(b, kc, vc)
+    bt = torch.from_numpy(b.block_tables).cuda()
+    bt[0, 1] = b.num_blocks + 3
+    sl = torch.from_numpy(b.seq_lens).cuda()
+    pkv.paged_attention_decode(b.q, kc, vc, bt, sl, b.scale)
+    assert pkv.get_device_error() & pkv.DEVERR_BLOCK
+    pkv.kv_block_copy(kc, vc, torch.tensor([[0, -5]], dtype=torch.int64, device="cuda"))
+    assert pkv.get_device_error() == pkv.DEVERR_BLOCK
+
+
+def test_length_beyond_table_sets_error():
+    b = wl.custom_batch([40, 20], dtype="bf16", hq=8, hkv=2, d=128, p=16, seed=62, device="cuda")
+    kc, vc = pu.device_pool(b)
+    pu.device_fill(b, kc, vc)
+    sl = torch.tensor([40, 10_000], dtype=torch.int32, device="cuda")
+    pkv.paged_attention_decode(b.q, kc, vc, torch.from_numpy(b.block_tables).cuda(), sl, b.scale)
+    assert pkv.get_device_error() & pkv.DEVERR_LENGTH
+
+
+def test_host_validation_rejects_before_launch():
+    kc = torch.zeros(4, 16, 2, 64, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(1, 6, 64, dtype=torch.bfloat16, device="cuda")  # 6 % 2 == 0 but G = 3
+    bt = torch.zeros(1, 1, dtype=torch.int32, device="cuda")
+    sl = torch.ones(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(pkv.PkvError) as ei:
+        pkv.paged_attention_decode(q, kc, kc, bt, sl, 1.0)
+    assert ei.value.status == pkv.PKV_ERR_UNSUPPORTED
+    q = torch.zeros(1, 4, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(pkv.PkvError) as ei:
+        pkv.paged_attention_decode(q, kc, kc, bt, sl, 1.0, partition_size=24)
+    assert ei.value.status == pkv.PKV_ERR_INVALID_ARG
+    kc3 = torch.zeros(4, 8, 2, 64, dtype=torch.bfloat16, device="cuda")  # block size 8
+    with pytest.raises(pkv.PkvError) as ei:
+        pkv.paged_attention_decode(q, kc3, kc3, bt, sl, 1.0)
+    assert ei.value.status == pkv.PKV_ERR_UNSUPPORTED
+    assert pkv.get_device_error() == 0
