@@ -38,11 +38,13 @@ WORKLOADS = ("llama", "long_bs16", "long_bs64", "shared")
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--workload", default="llama", choices=WORKLOADS)
     ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the batch size (small cases for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -150,14 +152,14 @@ def barrier(world):
         dist.barrier()
 
 
-def make_batch(name, device, seed_offset=0):
+def make_batch(name, device, seed_offset=0, batch=0):
     from paged_kv_cache_41_gb300 import workloads as wl
     if name == "llama":
-        return wl.llama_batch(device=device, seed=2 + seed_offset)
+        return wl.llama_batch(device=device, seed=2 + seed_offset, batch=batch or 64)
     if name == "long_bs16":
-        return wl.long_batch(device=device, block_size=16, seed=3 + seed_offset)
+        return wl.long_batch(device=device, block_size=16, seed=3 + seed_offset, batch=batch or 8)
     if name == "long_bs64":
-        return wl.long_batch(device=device, block_size=64, seed=3 + seed_offset)
+        return wl.long_batch(device=device, block_size=64, seed=3 + seed_offset, batch=batch or 8)
     raise ValueError(name)
 
 
@@ -221,7 +223,7 @@ def run_pkv(args, rank, world, local):
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     pkv.load_library()
-    b = make_batch(args.workload, dev, seed_offset=rank)
+    b = make_batch(args.workload, dev, seed_offset=rank, batch=args.batch)
     B = b.num_seqs
     shape = (b.num_blocks, b.block_size, b.num_kv_heads, b.head_dim)
     dt = b.k_hist.dtype
@@ -244,7 +246,6 @@ def run_pkv(args, rank, world, local):
         psize = pkv.decode_auto_partition(kc, B, b.num_q_heads, b.max_blocks)
     ws_bytes = pkv.decode_workspace_bytes(kc, B, b.num_q_heads, b.max_blocks, psize)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
-    del b.k_hist, b.v_hist
     torch.cuda.synchronize()
     assert pkv.get_device_error() == 0
     stream = torch.cuda.current_stream()
@@ -397,7 +398,7 @@ def main():
 
 def run_reference(args):
     """The CPU oracle, as it stands, on bounded samples of the same workload."""
-    b = make_batch(args.workload, "cpu")
+    b = make_batch(args.workload, "cpu", batch=args.batch)
     nthreads = len(os.sched_getaffinity(0))
     per_step = max(1.0, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):

@@ -26,6 +26,12 @@ CUDA_SOURCES = [
     "kernels/decode.cu",
     "kernels/prefix_tc.cu",
 ]
+# Attention kernels take exp2/log2/division from the hardware approximations
+# (softmax in base 2, well inside the attention tolerance).
+PER_SOURCE_FLAGS = {
+    "kernels/decode.cu": ["--use_fast_math"],
+    "kernels/prefix_tc.cu": ["--use_fast_math"],
+}
 
 LIB = os.path.join(HERE, "libpkv.so")
 POOL_LIB = os.path.join(HERE, "libpkv_pool.so")
@@ -72,7 +78,8 @@ def build_cuda(force=False, extra_flags=()) -> str:
     for s in srcs:
         obj = os.path.join(objdir, os.path.basename(s).replace(".cu", ".o"))
         objs.append(obj)
-        procs.append((s, subprocess.Popen(common + ["-c", s, "-o", obj],
+        extra = PER_SOURCE_FLAGS.get(os.path.relpath(s, CSRC), [])
+        procs.append((s, subprocess.Popen(common + extra + ["-c", s, "-o", obj],
                                           stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
     failed = []
     for s, p in procs:

@@ -12,14 +12,18 @@
 // Design (GB300):
 //   * one CTA per (kv head, partition, sequence); the G query heads of a kv
 //     head share every K/V byte the CTA reads;
-//   * warp 4 is the producer: it walks the block table and issues one 4-D TMA
-//     box (a tile of up to 64 token rows x head_dim of one kv head) for K and
-//     one for V into an mbarrier-tracked ring of shared-memory stages;
+//   * warp 4 is the producer: it holds the partition's block ids 32 at a
+//     time (one coalesced load per 32 blocks, the next group in flight) and
+//     issues one 4-D TMA box (up to 64 token rows x head_dim of one kv head)
+//     for K and one for V into an mbarrier-tracked ring of shared-memory
+//     stages, so no table lookup sits between two copies;
 //   * warps 0-3 consume 16-token chunks: each half-warp owns two token rows,
 //     each lane 1/16 of head_dim; q . k partial sums of the 2G (row, head)
 //     pairs are folded across the 16 lanes by a transpose-reduction (each
-//     shuffle level halves the values a lane carries), the softmax update runs
-//     once per (row, head), and P.V accumulates per lane in fp32;
+//     shuffle level halves the values a lane carries), which leaves the row
+//     in lane bit 3, so the softmax max and sum over the warp's four rows are
+//     two shuffles each and never touch shared memory; q . k and P . V use
+//     packed fp32x2 FMAs;
 //   * the exponent base is only moved when the running max grows by more than
 //     2^8 (exact: output and denominator keep the same base), so the
 //     accumulator rescale is rare;
@@ -36,56 +40,9 @@ namespace pkv {
 constexpr int kConsumerWarps = 4;
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
 constexpr int kChunk = 16;             // token rows per softmax update
-constexpr int kMaxTileRows = 64;       // token rows per TMA box
 constexpr float kRescaleLog2 = 8.0f;   // move the exponent base past 2^8 growth
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
-
-__host__ __device__ constexpr int tile_rows_for(int block_size) {
-  return block_size < kMaxTileRows ? block_size : kMaxTileRows;
-}
-
-// Fold N per-lane values across the 16 lanes of a half-warp (xor offsets
-// O, O/2, ..., 1).  While a lane carries more than one value, each level
-// sends half of them to its partner and keeps the other half; afterwards the
-// lane holds the full 16-lane sum of one of the N values (see held_index).
-template <int N, int O>
-struct TransposeReduce {
-  __device__ __forceinline__ static void run(float* v, int l16) {
-    if constexpr (N > 1) {
-      constexpr int H = N / 2;
-      const bool upper = (l16 & O) != 0;
-#pragma unroll
-      for (int i = 0; i < H; ++i) {
-        const float send = upper ? v[i] : v[i + H];
-        const float keep = upper ? v[i + H] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
-      }
-      if constexpr (O > 1) TransposeReduce<H, O / 2>::run(v, l16);
-    } else {
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
-      if constexpr (O > 1) TransposeReduce<1, O / 2>::run(v, l16);
-    }
-  }
-};
-
-template <int N>
-__device__ __forceinline__ int held_index(int l16) {
-  int idx = 0, n = N;
-#pragma unroll
-  for (int o = 8; o >= 1; o >>= 1) {
-    if (n > 1) {
-      n >>= 1;
-      if (l16 & o) idx += n;
-    }
-  }
-  return idx;
-}
-
-template <int N>
-__host__ __device__ constexpr int log2_int() {
-  return N <= 1 ? 0 : 1 + log2_int<N / 2>();
-}
 
 struct DecodeSmem {
   int tile_elems;   // rows * head_dim
@@ -96,7 +53,7 @@ struct DecodeSmem {
 __host__ __device__ inline DecodeSmem decode_smem_layout(int block_size, int head_dim,
                                                          int elem_bytes, int group, int stages) {
   DecodeSmem s;
-  s.tile_elems = tile_rows_for(block_size) * head_dim;
+  s.tile_elems = kStageRows * head_dim;
   s.stages = stages;
   size_t tiles = (size_t)2 * stages * s.tile_elems * elem_bytes;
   const size_t merge = (size_t)(kConsumerWarps * group * head_dim + 2 * kConsumerWarps * group) * 4;
@@ -105,13 +62,14 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int block_size, int hea
   s.bar_off = s.tiles_bytes;
   s.ok_off = s.bar_off + (size_t)2 * stages * 8;
   s.scratch_off = (s.ok_off + (size_t)stages * 4 + 15) & ~(size_t)15;
-  s.total = s.scratch_off + (size_t)kConsumerWarps * 5 * group * 4 + 128;  // +128: base alignment
+  s.total = s.scratch_off + (size_t)kConsumerWarps * 2 * (2 * group * 16) * 4 + 128;  // +128: base alignment
   return s;
 }
 
 int decode_num_stages(int block_size, int head_dim, int elem_bytes) {
-  const int stage_bytes = 2 * tile_rows_for(block_size) * head_dim * elem_bytes;
-  int ns = (64 * 1024) / stage_bytes;
+  (void)block_size;
+  const int stage_bytes = 2 * kStageRows * head_dim * elem_bytes;
+  int ns = (72 * 1024) / stage_bytes;
   if (ns < 2) ns = 2;
   if (ns > 8) ns = 8;
   return ns;
@@ -121,18 +79,108 @@ size_t decode_smem_bytes(int block_size, int head_dim, int elem_bytes, int group
   return decode_smem_layout(block_size, head_dim, elem_bytes, group, stages).total;
 }
 
+// One 16-row chunk of a stage for one consumer warp: rows row0 and row0 + 1
+// of this half-warp.  kTail = false is the full-stage fast path (every row
+// valid, no masking); kTail = true masks rows >= nvalid.
+//
+// Cross-lane sums go through `red`, this half-warp's [2G][16] scratch: lane
+// l16 stores its partial dot product of value i = (row tk, head g) = tk*G + g
+// at red[i][l16]; then each value is summed by 8/G lanes that read 2G
+// consecutive partials each and combine with 8/G - 1 shuffles.  Lane l16 ends
+// up holding value j = l16 / (8/G): row tk = l16 >> 3, head g = j % G.
+template <typename T, int D, int G, bool kTail>
+__device__ __forceinline__ void decode_chunk(const T* __restrict__ kt, const T* __restrict__ vt,
+                                             int row0, int nvalid,
+                                             const float2 (&q2)[G][D / 32],
+                                             float2 (&acc)[G][D / 32], float& m_used,
+                                             float& l_run, float* __restrict__ red, int l16) {
+  constexpr int EPL = D / 16;
+  constexpr int EP2 = EPL / 2;
+  constexpr int NV = 2 * G;    // values per half-warp and chunk
+  constexpr int LPV = 16 / NV; // lanes summing one value
+  // ---- q . k partial sums for rows row0, row0 + 1 and the G heads
+  float v[NV];
+#pragma unroll
+  for (int tk = 0; tk < 2; ++tk) {
+    float kf[EPL];
+    VecLoad<T, EPL>::run(kt + (row0 + tk) * D + l16 * EPL, kf);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float2 d2 = __fmul2_rn(q2[g][0], make_float2(kf[0], kf[1]));
+#pragma unroll
+      for (int j = 1; j < EP2; ++j) d2 = __ffma2_rn(q2[g][j], make_float2(kf[2 * j], kf[2 * j + 1]), d2);
+      v[tk * G + g] = d2.x + d2.y;
+    }
+  }
+  // ---- sum each value over the 16 lanes of the half-warp
+#pragma unroll
+  for (int i = 0; i < NV; ++i) red[i * 16 + l16] = v[i];
+  __syncwarp();
+  const int j = l16 / LPV, sub = l16 % LPV;
+  float part[NV];
+  VecLoad<float, NV>::run(red + j * 16 + sub * NV, part);
+  __syncwarp();  // the next chunk rewrites red
+  float s2 = part[0];
+#pragma unroll
+  for (int k = 1; k < NV; ++k) s2 += part[k];
+#pragma unroll
+  for (int o = LPV / 2; o >= 1; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+  // ---- online softmax over the warp's 4 rows (rows differ in lane bits 3, 4)
+  const float sc = (!kTail || row0 + (l16 >> 3) < nvalid) ? s2 : -INFINITY;
+  float cmax = fmaxf(sc, __shfl_xor_sync(0xffffffffu, sc, 8));
+  cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 16));
+  const float m_new = fmaxf(m_used, cmax);
+  const bool need = m_new > m_used + kRescaleLog2;
+  const bool any = __any_sync(0xffffffffu, need);
+  const float alpha = need ? exp2f(m_used - m_new) : 1.f;
+  m_used = need ? m_new : m_used;
+  l_run *= alpha;
+  const float p = (kTail && sc == -INFINITY) ? 0.f : exp2f(sc - m_used);
+  float psum = p + __shfl_xor_sync(0xffffffffu, p, 8);
+  psum += __shfl_xor_sync(0xffffffffu, psum, 16);
+  l_run += psum;
+  if (any) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float al = __shfl_sync(0xffffffffu, alpha, g * LPV, 16);
+      const float2 al2 = make_float2(al, al);
+#pragma unroll
+      for (int e = 0; e < EP2; ++e) acc[g][e] = __fmul2_rn(acc[g][e], al2);
+    }
+  }
+  // ---- P . V for this half-warp's two rows
+  float pg[2][G];
+#pragma unroll
+  for (int tk = 0; tk < 2; ++tk)
+#pragma unroll
+    for (int g = 0; g < G; ++g) pg[tk][g] = __shfl_sync(0xffffffffu, p, (tk * G + g) * LPV, 16);
+#pragma unroll
+  for (int tk = 0; tk < 2; ++tk) {
+    if (!kTail || row0 + tk < nvalid) {
+      float vf[EPL];
+      VecLoad<T, EPL>::run(vt + (row0 + tk) * D + l16 * EPL, vf);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float2 p2 = make_float2(pg[tk][g], pg[tk][g]);
+#pragma unroll
+        for (int e = 0; e < EP2; ++e)
+          acc[g][e] = __ffma2_rn(p2, make_float2(vf[2 * e], vf[2 * e + 1]), acc[g][e]);
+      }
+    }
+  }
+}
+
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 3))
     decode_partial_kernel(const __grid_constant__ CUtensorMap tmk,
                           const __grid_constant__ CUtensorMap tmv, const DecodeArgs a) {
   constexpr int EPL = D / 16;  // head_dim elements per lane
+  constexpr int EP2 = EPL / 2;
   constexpr int NV = 2 * G;    // (row, head) partial sums per lane per chunk
-  constexpr int LEVELS = log2_int<NV>();
   static_assert(NV <= 16 && (NV & (NV - 1)) == 0, "group must be 1, 2, 4 or 8");
 
   const int kvh = blockIdx.x, part = blockIdx.y, r = blockIdx.z;
   const int P = a.block_size;
-  const int TR = tile_rows_for(P);
   const bool reporter = kvh == 0 && part == 0 && threadIdx.x == 0;
   const int T_r = effective_len(__ldg(a.seq_lens + r), a.max_blocks, P, a.err, reporter);
   const int nblk = (T_r + P - 1) / P;
@@ -149,8 +197,10 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 3))
   }
   const int tok0 = b0 * P;
   const int tok_end = min(T_r, (b0 + a.blocks_per_part) * P);
-  const int ntiles = (tok_end - tok0 + TR - 1) / TR;
-  const int tiles_per_block = P / TR;
+  const int ntiles = (tok_end - tok0 + kStageRows - 1) / kStageRows;  // 64-row stages
+  const int nbp = (tok_end - tok0 + P - 1) / P;  // blocks of this partition
+  const int TB = box_rows_for(P);                // rows per TMA box
+  const int nsub = kStageRows / TB;              // boxes per stage
 
   const DecodeSmem L = decode_smem_layout(P, D, (int)sizeof(T), G, a.num_stages);
   const int NS = a.num_stages;
@@ -176,30 +226,76 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 3))
 
   if (warp == kConsumerWarps) {
     // ---------------------------------------------------------------- producer
+    // The warp holds the partition's block ids 32 at a time (one coalesced
+    // load per 32 blocks, the next group in flight) so no table lookup sits
+    // between two TMA issues.  A stage is 64 token rows: 64 / P boxes of one
+    // block each when P < 64, else one 64-row box of a larger block.  All
+    // positions advance incrementally (no division in the loop).
     if (lane == 0) {
       prefetch_tensormap(&tmk);
       prefetch_tensormap(&tmv);
-      const int32_t* tbl = a.block_tables + (int64_t)r * a.max_blocks + b0;
-      const uint32_t tx = 2u * (uint32_t)(L.tile_elems * sizeof(T));
-      for (int i = 0; i < ntiles; ++i) {
-        const int s = i % NS;
-        if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1)) {
-          atomicOr(a.err, PKV_DEVERR_TIMEOUT);
-          break;
+    }
+    const int32_t* tbl = a.block_tables + (int64_t)r * a.max_blocks + b0;
+    int cur = lane < nbp ? __ldg(tbl + lane) : -1;
+    int nxt = 32 + lane < nbp ? __ldg(tbl + 32 + lane) : -1;
+    int base = 0;
+    const uint32_t box_bytes = (uint32_t)(TB * D * sizeof(T));
+    int jb = 0, brow = 0;        // next box: block within the partition, first row in it
+    int rel = 0;                 // next box: first row relative to tok0
+    int s = 0, round = 0;        // stage and ring round
+    const int avail = tok_end - tok0;
+    for (int i = 0; i < ntiles; ++i) {
+      int ok = 1;
+      if (lane == 0 && round > 0 && !mbar_wait(&empty[s], (round - 1) & 1)) {
+        atomicOr(a.err, PKV_DEVERR_TIMEOUT);
+        ok = 0;
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      int blk[kStageRows / 16], brw[kStageRows / 16];
+      int nbox = 0;
+#pragma unroll
+      for (int j = 0; j < kStageRows / 16; ++j) {
+        blk[j] = -1;
+        brw[j] = 0;
+        if (j < nsub && rel < avail) {
+          if (jb >= base + 32) {
+            cur = nxt;
+            base += 32;
+            nxt = base + 32 + lane < nbp ? __ldg(tbl + base + 32 + lane) : -1;
+          }
+          blk[j] = __shfl_sync(0xffffffffu, cur, jb - base);
+          brw[j] = brow;
+          nbox = j + 1;
+          rel += TB;
+          brow += TB;
+          if (brow == P) {
+            brow = 0;
+            ++jb;
+          }
         }
-        const int jb = i / tiles_per_block;             // block within the partition
-        const int row = (i % tiles_per_block) * TR;     // first row of the tile in the block
-        const int blk = __ldg(tbl + jb);
-        if (blk < 0 || (int64_t)blk >= a.num_blocks) {
+      }
+      if (lane == 0) {
+        bool valid = true;
+        for (int j = 0; j < nbox; ++j)
+          if (blk[j] < 0 || (int64_t)blk[j] >= a.num_blocks) valid = false;
+        if (!valid) {
           atomicOr(a.err, PKV_DEVERR_BLOCK);
           stage_ok[s] = 0;
           mbar_arrive(&full[s]);
         } else {
           stage_ok[s] = 1;
-          mbar_arrive_expect_tx(&full[s], tx);
-          tma_load_4d(ktile + (size_t)s * L.tile_elems, &tmk, 0, kvh, row, blk, &full[s]);
-          tma_load_4d(vtile + (size_t)s * L.tile_elems, &tmv, 0, kvh, row, blk, &full[s]);
+          mbar_arrive_expect_tx(&full[s], 2u * box_bytes * (uint32_t)nbox);
+          T* kd = ktile + (size_t)s * L.tile_elems;
+          T* vd = vtile + (size_t)s * L.tile_elems;
+          for (int j = 0; j < nbox; ++j) {
+            tma_load_4d(kd + j * TB * D, &tmk, 0, kvh, brw[j], blk[j], &full[s]);
+            tma_load_4d(vd + j * TB * D, &tmv, 0, kvh, brw[j], blk[j], &full[s]);
+          }
         }
+      }
+      if (++s == NS) {
+        s = 0;
+        ++round;
       }
     }
     return;
@@ -207,121 +303,67 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 3))
 
   // ------------------------------------------------------------------ consumers
   const int hw = lane >> 4, l16 = lane & 15;
-  float qr[G][EPL];
+  float2 q2[G][EP2];
   {
     const T* qp = static_cast<const T*>(a.q) +
                   ((int64_t)r * a.num_q_heads + (int64_t)kvh * G) * D + l16 * EPL;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      VecLoad<T, EPL>::run(qp + g * D, qr[g]);
+      float f[EPL];
+      VecLoad<T, EPL>::run(qp + g * D, f);
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) qr[g][e] *= a.qscale;
+      for (int j = 0; j < EP2; ++j) q2[g][j] = make_float2(f[2 * j] * a.qscale, f[2 * j + 1] * a.qscale);
     }
   }
-  float acc[G][EPL];
+  float2 acc[G][EP2];
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[g][e] = 0.f;
+    for (int j = 0; j < EP2; ++j) acc[g][j] = make_float2(0.f, 0.f);
 
-  // softmax bookkeeping: lane handles (row stok, head sg) of the warp's 4 x G
-  // scores; the state (m_used, l_run) is that of head sg.
-  float* sw = scratch + warp * 5 * G;  // [4][G] scores / probabilities, then [G] alpha
-  const int sidx = lane & (4 * G - 1);
-  const int stok = sidx / G, sg = sidx % G;
-  const int ridx = held_index<NV>(l16);
-  const int rtk = ridx / G, rg = ridx % G;
-  const bool rep = (l16 & ((1 << (4 - LEVELS)) - 1)) == 0;
+  // (m_used, l_run): softmax state of head (l16 / (8 / G)) % G of this lane.
   float m_used = -INFINITY, l_run = 0.f;
-
+  float* red = scratch + (warp * 2 + hw) * (2 * G * 16);
+  const int rbase = warp * 4 + hw * 2;
+  int s = 0, round = 0;
+  int remain = tok_end - tok0;  // rows of this partition not yet consumed
   for (int i = 0; i < ntiles; ++i) {
-    const int s = i % NS;
-    if (!mbar_wait(&full[s], (i / NS) & 1)) {
+    const int nvalid = min(kStageRows, remain);
+    remain -= kStageRows;
+    if (!mbar_wait(&full[s], round & 1)) {
       if (lane == 0) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
       break;
     }
-    const int nvalid = min(TR, tok_end - (tok0 + i * TR));
     if (stage_ok[s]) {
       const T* kt = ktile + (size_t)s * L.tile_elems;
       const T* vt = vtile + (size_t)s * L.tile_elems;
-      for (int c = 0; c * kChunk < nvalid; ++c) {
-        const int row0 = c * kChunk + warp * 4 + hw * 2;
-        // ---- q . k for rows row0, row0 + 1 and the G heads
-        float v[NV];
-#pragma unroll
-        for (int tk = 0; tk < 2; ++tk) {
-          float kf[EPL];
-          VecLoad<T, EPL>::run(kt + (row0 + tk) * D + l16 * EPL, kf);
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            float d0 = 0.f;
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) d0 = fmaf(qr[g][e], kf[e], d0);
-            v[tk * G + g] = d0;
-          }
-        }
-        TransposeReduce<NV, 8>::run(v, l16);
-        if (rep) sw[(hw * 2 + rtk) * G + rg] = (row0 + rtk < nvalid) ? v[0] : -INFINITY;
-        __syncwarp();
-        // ---- online softmax over the warp's 4 rows, one lane per (row, head)
-        const float sc = sw[stok * G + sg];
-        float cmax = sc;
-#pragma unroll
-        for (int o = G; o < 4 * G; o <<= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
-        const float m_new = fmaxf(m_used, cmax);
-        const bool need = m_new > m_used + kRescaleLog2;
-        const bool any = __any_sync(0xffffffffu, need);
-        float alpha = 1.f;
-        if (need) {
-          alpha = exp2f(m_used - m_new);
-          m_used = m_new;
-          l_run *= alpha;
-        }
-        const float p = (sc == -INFINITY) ? 0.f : exp2f(sc - m_used);
-        float psum = p;
-#pragma unroll
-        for (int o = G; o < 4 * G; o <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
-        l_run += psum;
-        __syncwarp();
-        if (lane < 4 * G) sw[stok * G + sg] = p;
-        if (any && lane < G) sw[4 * G + lane] = alpha;
-        __syncwarp();
-        if (any) {
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float al = sw[4 * G + g];
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) acc[g][e] *= al;
-          }
-        }
-        // ---- P . V for this half-warp's two rows
-#pragma unroll
-        for (int tk = 0; tk < 2; ++tk) {
-          const int row = row0 + tk;
-          if (row < nvalid) {
-            float pg[G];
-#pragma unroll
-            for (int g = 0; g < G; ++g) pg[g] = sw[(hw * 2 + tk) * G + g];
-            float vf[EPL];
-            VecLoad<T, EPL>::run(vt + row * D + l16 * EPL, vf);
-#pragma unroll
-            for (int g = 0; g < G; ++g)
-#pragma unroll
-              for (int e = 0; e < EPL; ++e) acc[g][e] = fmaf(pg[g], vf[e], acc[g][e]);
-          }
-        }
-        __syncwarp();
+      if (nvalid == kStageRows) {
+#pragma unroll 1
+        for (int c = 0; c < kStageRows / kChunk; ++c)
+          decode_chunk<T, D, G, false>(kt, vt, c * kChunk + rbase, kStageRows, q2, acc, m_used,
+                                       l_run, red, l16);
+      } else {
+        for (int c = 0; c * kChunk < nvalid; ++c)
+          decode_chunk<T, D, G, true>(kt, vt, c * kChunk + rbase, nvalid, q2, acc, m_used, l_run,
+                                      red, l16);
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
+    if (++s == NS) {
+      s = 0;
+      ++round;
+    }
   }
 
   // ------------------------------------------------------------------ merge the 4 warps
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], 16);
+    for (int j = 0; j < EP2; ++j) {
+      acc[g][j].x += __shfl_xor_sync(0xffffffffu, acc[g][j].x, 16);
+      acc[g][j].y += __shfl_xor_sync(0xffffffffu, acc[g][j].y, 16);
+    }
 
   named_barrier_sync(1, kConsumerWarps * 32);  // every stage consumed: reuse the tiles
   float* macc = reinterpret_cast<float*>(smem);            // [4][G][D]
@@ -331,11 +373,15 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 3))
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) macc[(warp * G + g) * D + l16 * EPL + e] = acc[g][e];
-  }
-  if (lane < G) {
-    mm[warp * G + lane] = m_used;
-    ml[warp * G + lane] = l_run;
+      for (int j = 0; j < EP2; ++j) {
+        macc[(warp * G + g) * D + l16 * EPL + 2 * j] = acc[g][j].x;
+        macc[(warp * G + g) * D + l16 * EPL + 2 * j + 1] = acc[g][j].y;
+      }
+    constexpr int LPV = 8 / G;  // lanes per (row, head) value
+    if (l16 < 8 && l16 % LPV == 0) {  // row 0 of the half-warp, first lane of each head
+      mm[warp * G + l16 / LPV] = m_used;
+      ml[warp * G + l16 / LPV] = l_run;
+    }
   }
   named_barrier_sync(1, kConsumerWarps * 32);
 

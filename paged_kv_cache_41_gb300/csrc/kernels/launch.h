@@ -15,6 +15,13 @@ cudaError_t launch_kv_block_copy(void* k_cache, void* v_cache, const int64_t* pa
                                  int64_t num_pairs, int64_t num_blocks, int64_t block_bytes,
                                  unsigned int* err, cudaStream_t stream);
 
+// Token rows per shared-memory stage of the decode kernel, and the rows of
+// one TMA box: a box covers one block, or 64 rows of a larger block.
+constexpr int kStageRows = 64;
+__host__ __device__ constexpr int box_rows_for(int block_size) {
+  return block_size < kStageRows ? block_size : kStageRows;
+}
+
 // Arguments of the split-K paged decode kernels.
 struct DecodeArgs {
   const void* q;                // [B, Hq, D]

@@ -62,7 +62,9 @@ pkv_status check_cache(const pkv_cache_desc* c) {
 pkv_status check_attention_shape(const pkv_cache_desc* c, int32_t num_q_heads) {
   if (c->head_dim != 64 && c->head_dim != 128) return PKV_ERR_UNSUPPORTED;
   const int P = c->block_size;
-  if (P % 16 != 0 || P > 256 || (P > 64 && P % 64 != 0)) return PKV_ERR_UNSUPPORTED;
+  // a 64-row stage is whole blocks (P = 16, 32, 64) or a slice of one (P = 64k)
+  if (P < 16 || P > 256 || (P <= 64 && 64 % P != 0) || (P > 64 && P % 64 != 0))
+    return PKV_ERR_UNSUPPORTED;
   if (num_q_heads <= 0 || num_q_heads % c->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   const int G = num_q_heads / c->num_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return PKV_ERR_UNSUPPORTED;
@@ -221,7 +223,7 @@ pkv_status pkv_paged_attention_decode(const pkv_cache_desc* cache, void* out, fl
   if (workspace_bytes < need || (need > 0 && !workspace)) return PKV_ERR_INVALID_ARG;
   if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PKV_ERR_INVALID_ARG;
 
-  const int rows = cache->block_size < 64 ? cache->block_size : 64;
+  const int rows = pkv::box_rows_for(cache->block_size);
   CUtensorMap tmk, tmv;
   if ((st = encode_cache_map(&tmk, cache, k_cache, rows)) != PKV_OK) return st;
   if ((st = encode_cache_map(&tmv, cache, v_cache, rows)) != PKV_OK) return st;
