@@ -131,7 +131,7 @@ int32_t pkv_decode_auto_partition(const pkv_cache_desc* cache, int32_t num_seqs,
  *                  partition are three levels).
  *   workspace:     device scratch of at least pkv_decode_workspace_bytes
  *                  bytes (may be NULL when that is 0), 256-byte aligned.
- * Supported: block_size 16, 32, 64, 128, 192 or 256; head_dim 64 or 128;
+ * Supported: block_size 16 or a multiple of 32 up to 256; head_dim 64 or 128;
  * Hq / Hkv in {1, 2, 4, 8}; num_seqs <= 65535. */
 pkv_status pkv_paged_attention_decode(
     const pkv_cache_desc* cache, void* out, float* lse, const void* q,

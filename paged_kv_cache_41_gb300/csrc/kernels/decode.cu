@@ -10,20 +10,22 @@
 // normalised outputs, with empty partitions as the identity.
 //
 // Design (GB300):
-//   * one CTA per (kv head, partition, sequence); the G query heads of a kv
-//     head share every K/V byte the CTA reads;
-//   * warp 4 is the producer: it holds the partition's block ids 32 at a
+//   * one CTA of four warps per (kv head, partition, sequence); the G query
+//     heads of a kv head share every K/V byte the CTA reads; four CTAs fit on
+//     an SM (registers and a 3 x 16 KiB shared-memory ring each);
+//   * warp 0 also issues the loads: it holds the partition's block ids 32 at a
 //     time (one coalesced load per 32 blocks, the next group in flight) and
-//     issues one 4-D TMA box (up to 64 token rows x head_dim of one kv head)
-//     for K and one for V into an mbarrier-tracked ring of shared-memory
-//     stages, so no table lookup sits between two copies;
-//   * warps 0-3 consume 16-token chunks: each half-warp owns two token rows,
-//     each lane 1/16 of head_dim; q . k partial sums of the 2G (row, head)
-//     pairs are folded across the 16 lanes by a transpose-reduction (each
-//     shuffle level halves the values a lane carries), which leaves the row
-//     in lane bit 3, so the softmax max and sum over the warp's four rows are
-//     two shuffles each and never touch shared memory; q . k and P . V use
-//     packed fp32x2 FMAs;
+//     fills each 32-row stage with 4-D TMA boxes (one block, or a 32-row slice
+//     of a larger block, of one kv head) for K and V, tracked by mbarriers;
+//     a stage is refilled as soon as all four warps have released it, so no
+//     table lookup sits between two copies;
+//   * warps consume 16-row chunks: each half-warp owns two token rows, each
+//     lane 1/16 of head_dim; the 2G (row, head) partial dot products are
+//     summed across the 16 lanes through a small per-warp shared scratch;
+//     the row lands in lane bit 3, so the softmax max and sum over the warp's
+//     four rows are two shuffles each; q . k and P . V use packed fp32x2 FMAs;
+//   * full stages take a straight-line path with no row masking; only a
+//     partition's last stage masks rows;
 //   * the exponent base is only moved when the running max grows by more than
 //     2^8 (exact: output and denominator keep the same base), so the
 //     accumulator rescale is rare;
@@ -38,7 +40,7 @@
 namespace pkv {
 
 constexpr int kConsumerWarps = 4;
-constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+constexpr int kDecodeThreads = kConsumerWarps * 32;
 constexpr int kChunk = 16;             // token rows per softmax update
 constexpr float kRescaleLog2 = 8.0f;   // move the exponent base past 2^8 growth
 constexpr float kLn2 = 0.6931471805599453f;
@@ -69,7 +71,7 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int block_size, int hea
 int decode_num_stages(int block_size, int head_dim, int elem_bytes) {
   (void)block_size;
   const int stage_bytes = 2 * kStageRows * head_dim * elem_bytes;
-  int ns = (72 * 1024) / stage_bytes;
+  int ns = (49 * 1024) / stage_bytes;  // 3 stages of 16 KiB: 4 CTAs per SM
   if (ns < 2) ns = 2;
   if (ns > 8) ns = 8;
   return ns;
@@ -171,7 +173,7 @@ __device__ __forceinline__ void decode_chunk(const T* __restrict__ kt, const T* 
 }
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 3))
+__global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
     decode_partial_kernel(const __grid_constant__ CUtensorMap tmk,
                           const __grid_constant__ CUtensorMap tmv, const DecodeArgs a) {
   constexpr int EPL = D / 16;  // head_dim elements per lane
@@ -224,81 +226,77 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 3))
   }
   __syncthreads();
 
-  if (warp == kConsumerWarps) {
-    // ---------------------------------------------------------------- producer
-    // The warp holds the partition's block ids 32 at a time (one coalesced
-    // load per 32 blocks, the next group in flight) so no table lookup sits
-    // between two TMA issues.  A stage is 64 token rows: 64 / P boxes of one
-    // block each when P < 64, else one 64-row box of a larger block.  All
-    // positions advance incrementally (no division in the loop).
+  // ---------------------------------------------------------------- loads
+  // Warp 0 issues the TMA boxes.  It holds the partition's block ids 32 at a
+  // time (one coalesced load per 32 blocks, the next group in flight) so no
+  // table lookup sits between two copies.  A stage is kStageRows token rows:
+  // kStageRows / P boxes of one block each when P < kStageRows, else one
+  // box of kStageRows rows of a larger block.  Positions advance
+  // incrementally (no division).
+  const int32_t* tbl = a.block_tables + (int64_t)r * a.max_blocks + b0;
+  int cur = 0, nxt = 0, base = 0;
+  int jb = 0, brow = 0, rel = 0;  // next box: block in the partition, row in it, row in partition
+  const int avail = tok_end - tok0;
+  const uint32_t box_bytes = (uint32_t)(TB * D * sizeof(T));
+  if (warp == 0) {
     if (lane == 0) {
       prefetch_tensormap(&tmk);
       prefetch_tensormap(&tmv);
     }
-    const int32_t* tbl = a.block_tables + (int64_t)r * a.max_blocks + b0;
-    int cur = lane < nbp ? __ldg(tbl + lane) : -1;
-    int nxt = 32 + lane < nbp ? __ldg(tbl + 32 + lane) : -1;
-    int base = 0;
-    const uint32_t box_bytes = (uint32_t)(TB * D * sizeof(T));
-    int jb = 0, brow = 0;        // next box: block within the partition, first row in it
-    int rel = 0;                 // next box: first row relative to tok0
-    int s = 0, round = 0;        // stage and ring round
-    const int avail = tok_end - tok0;
-    for (int i = 0; i < ntiles; ++i) {
-      int ok = 1;
-      if (lane == 0 && round > 0 && !mbar_wait(&empty[s], (round - 1) & 1)) {
-        atomicOr(a.err, PKV_DEVERR_TIMEOUT);
-        ok = 0;
-      }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      int blk[kStageRows / 16], brw[kStageRows / 16];
-      int nbox = 0;
+    cur = lane < nbp ? __ldg(tbl + lane) : -1;
+    nxt = 32 + lane < nbp ? __ldg(tbl + 32 + lane) : -1;
+  }
+  // Fill stage `st` with the next kStageRows rows (warp 0, all lanes).
+  auto issue_stage = [&](int st) {
+    int blk[kStageRows / 16], brw[kStageRows / 16];
+    int nbox = 0;
 #pragma unroll
-      for (int j = 0; j < kStageRows / 16; ++j) {
-        blk[j] = -1;
-        brw[j] = 0;
-        if (j < nsub && rel < avail) {
-          if (jb >= base + 32) {
-            cur = nxt;
-            base += 32;
-            nxt = base + 32 + lane < nbp ? __ldg(tbl + base + 32 + lane) : -1;
-          }
-          blk[j] = __shfl_sync(0xffffffffu, cur, jb - base);
-          brw[j] = brow;
-          nbox = j + 1;
-          rel += TB;
-          brow += TB;
-          if (brow == P) {
-            brow = 0;
-            ++jb;
-          }
+    for (int j = 0; j < kStageRows / 16; ++j) {
+      blk[j] = -1;
+      brw[j] = 0;
+      if (j < nsub && rel < avail) {
+        if (jb >= base + 32) {
+          cur = nxt;
+          base += 32;
+          nxt = base + 32 + lane < nbp ? __ldg(tbl + base + 32 + lane) : -1;
         }
-      }
-      if (lane == 0) {
-        bool valid = true;
-        for (int j = 0; j < nbox; ++j)
-          if (blk[j] < 0 || (int64_t)blk[j] >= a.num_blocks) valid = false;
-        if (!valid) {
-          atomicOr(a.err, PKV_DEVERR_BLOCK);
-          stage_ok[s] = 0;
-          mbar_arrive(&full[s]);
-        } else {
-          stage_ok[s] = 1;
-          mbar_arrive_expect_tx(&full[s], 2u * box_bytes * (uint32_t)nbox);
-          T* kd = ktile + (size_t)s * L.tile_elems;
-          T* vd = vtile + (size_t)s * L.tile_elems;
-          for (int j = 0; j < nbox; ++j) {
-            tma_load_4d(kd + j * TB * D, &tmk, 0, kvh, brw[j], blk[j], &full[s]);
-            tma_load_4d(vd + j * TB * D, &tmv, 0, kvh, brw[j], blk[j], &full[s]);
-          }
+        blk[j] = __shfl_sync(0xffffffffu, cur, jb - base);
+        brw[j] = brow;
+        nbox = j + 1;
+        rel += TB;
+        brow += TB;
+        if (brow == P) {
+          brow = 0;
+          ++jb;
         }
-      }
-      if (++s == NS) {
-        s = 0;
-        ++round;
       }
     }
-    return;
+    if (lane == 0) {
+      bool valid = true;
+#pragma unroll
+      for (int j = 0; j < kStageRows / 16; ++j)
+        if (j < nbox && (blk[j] < 0 || (int64_t)blk[j] >= a.num_blocks)) valid = false;
+      if (!valid) {
+        atomicOr(a.err, PKV_DEVERR_BLOCK);
+        stage_ok[st] = 0;
+        mbar_arrive(&full[st]);
+      } else {
+        stage_ok[st] = 1;
+        mbar_arrive_expect_tx(&full[st], 2u * box_bytes * (uint32_t)nbox);
+        T* kd = ktile + (size_t)st * L.tile_elems;
+        T* vd = vtile + (size_t)st * L.tile_elems;
+#pragma unroll
+        for (int j = 0; j < kStageRows / 16; ++j) {
+          if (j < nbox) {
+            tma_load_4d(kd + j * TB * D, &tmk, 0, kvh, brw[j], blk[j], &full[st]);
+            tma_load_4d(vd + j * TB * D, &tmv, 0, kvh, brw[j], blk[j], &full[st]);
+          }
+        }
+      }
+    }
+  };
+  if (warp == 0) {
+    for (int st = 0; st < NS && st < ntiles; ++st) issue_stage(st);
   }
 
   // ------------------------------------------------------------------ consumers
@@ -350,6 +348,16 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 3))
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
+    if (warp == 0 && i + NS < ntiles) {
+      // every warp has released stage s: refill it with stage i + NS
+      int ok = 1;
+      if (lane == 0 && !mbar_wait(&empty[s], round & 1)) {
+        atomicOr(a.err, PKV_DEVERR_TIMEOUT);
+        ok = 0;
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      issue_stage(s);
+    }
     if (++s == NS) {
       s = 0;
       ++round;
@@ -365,7 +373,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 3))
       acc[g][j].y += __shfl_xor_sync(0xffffffffu, acc[g][j].y, 16);
     }
 
-  named_barrier_sync(1, kConsumerWarps * 32);  // every stage consumed: reuse the tiles
+  __syncthreads();  // every stage consumed: reuse the tiles
   float* macc = reinterpret_cast<float*>(smem);            // [4][G][D]
   float* mm = macc + kConsumerWarps * G * D;               // [4][G]
   float* ml = mm + kConsumerWarps * G;                     // [4][G]
@@ -383,7 +391,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 3))
       ml[warp * G + l16 / LPV] = l_run;
     }
   }
-  named_barrier_sync(1, kConsumerWarps * 32);
+  __syncthreads();
 
   for (int j = threadIdx.x; j < G * D; j += kConsumerWarps * 32) {
     const int g = j / D, e = j % D;

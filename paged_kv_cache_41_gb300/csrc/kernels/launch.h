@@ -16,8 +16,9 @@ cudaError_t launch_kv_block_copy(void* k_cache, void* v_cache, const int64_t* pa
                                  unsigned int* err, cudaStream_t stream);
 
 // Token rows per shared-memory stage of the decode kernel, and the rows of
-// one TMA box: a box covers one block, or 64 rows of a larger block.
-constexpr int kStageRows = 64;
+// one TMA box: a box covers one block, or kStageRows rows of a larger block.
+// Block sizes must divide kStageRows or be a multiple of it.
+constexpr int kStageRows = 32;
 __host__ __device__ constexpr int box_rows_for(int block_size) {
   return block_size < kStageRows ? block_size : kStageRows;
 }

@@ -62,8 +62,9 @@ pkv_status check_cache(const pkv_cache_desc* c) {
 pkv_status check_attention_shape(const pkv_cache_desc* c, int32_t num_q_heads) {
   if (c->head_dim != 64 && c->head_dim != 128) return PKV_ERR_UNSUPPORTED;
   const int P = c->block_size;
-  // a 64-row stage is whole blocks (P = 16, 32, 64) or a slice of one (P = 64k)
-  if (P < 16 || P > 256 || (P <= 64 && 64 % P != 0) || (P > 64 && P % 64 != 0))
+  // a stage of pkv::kStageRows rows is whole blocks or a slice of one block
+  const int S = pkv::kStageRows;
+  if (P < 16 || P > 256 || (P <= S && S % P != 0) || (P > S && P % S != 0))
     return PKV_ERR_UNSUPPORTED;
   if (num_q_heads <= 0 || num_q_heads % c->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   const int G = num_q_heads / c->num_kv_heads;
@@ -101,15 +102,19 @@ int sm_count() {
 }
 
 int32_t auto_partition(const pkv_cache_desc* c, int32_t num_seqs, int32_t max_blocks) {
-  // Enough CTAs (kv head x partition x sequence) for several waves of the
-  // ~3 resident CTAs per SM, without splitting rows finer than 16 blocks.
-  const int64_t target = (int64_t)sm_count() * 3 * 4;
+  // 1024-token partitions (measured best on GB300 for block sizes 16-64: long
+  // enough to amortise a CTA's set-up and merge, short enough to balance
+  // ragged lengths); halved while the grid would give fewer than two waves of
+  // the four CTAs an SM holds, down to 256 tokens or one block.
+  const int P = c->block_size;
+  const int64_t max_tokens = (int64_t)max_blocks * P;
   const int64_t rows = (int64_t)num_seqs * c->num_kv_heads;
-  int32_t bpp = max_blocks > 0 ? max_blocks : 1;
-  const int32_t min_bpp = c->block_size >= 64 ? 4 : 16;
-  while (bpp > min_bpp && rows * ((max_blocks + bpp - 1) / bpp) < target) bpp = (bpp + 1) / 2;
-  if (bpp < 1) bpp = 1;
-  return bpp * c->block_size;
+  const int64_t target = (int64_t)sm_count() * 4 * 2;
+  int32_t ps = ((1024 + P - 1) / P) * P;
+  while (ps / 2 >= 256 && ps / 2 >= P && (ps / 2) % P == 0 &&
+         rows * ((max_tokens + ps - 1) / ps) < target)
+    ps /= 2;
+  return ps;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }

@@ -56,6 +56,7 @@ EDGE_LENS = [1, 15, 16, 17, 31, 32, 33, 100, 257, 0, 1000, 64, 2]
     ("bf16", 128, 64, 8, 16), ("bf16", 64, 8, 2, 16), ("f32", 128, 8, 2, 16),
     ("f32", 64, 4, 2, 16), ("bf16", 128, 32, 8, 64), ("bf16", 128, 32, 8, 32),
     ("bf16", 128, 32, 8, 128), ("bf16", 64, 16, 4, 256), ("f32", 128, 16, 2, 192),
+    ("bf16", 128, 16, 4, 96),
 ])
 @pytest.mark.parametrize("partition_size", [0, "one_block", "three_blocks", "whole"])
 def test_edge_lengths(dtype, d, hq, hkv, p, partition_size):
@@ -180,7 +181,7 @@ def test_host_validation_rejects_before_launch():
     with pytest.raises(pkv.PkvError) as ei:
         pkv.paged_attention_decode(q, kc, kc, bt, sl, 1.0, partition_size=24)
     assert ei.value.status == pkv.PKV_ERR_INVALID_ARG
-    for p in (8, 48, 80):  # block sizes the 64-row stages cannot tile
+    for p in (8, 24, 48, 80):  # block sizes the 32-row stages cannot tile
         kc3 = torch.zeros(4, p, 2, 64, dtype=torch.bfloat16, device="cuda")
         with pytest.raises(pkv.PkvError) as ei:
             pkv.paged_attention_decode(q, kc3, kc3, bt, sl, 1.0)
