@@ -50,7 +50,8 @@ typedef enum {
   PKV_ERR_INVALID_ARG = 1,  /* bad pointer, size, shape or workspace        */
   PKV_ERR_UNSUPPORTED = 2,  /* valid but not compiled (head_dim, group ...) */
   PKV_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed          */
-  PKV_ERR_DEVICE = 4        /* pkv_get_device_error found a device-side error */
+  PKV_ERR_DEVICE = 4,       /* pkv_get_device_error found a device-side error */
+  PKV_ERR_CAPACITY = 5      /* needs more than the fixed static scratch array */
 } pkv_status;
 
 typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
@@ -139,6 +140,40 @@ pkv_status pkv_paged_attention_decode(
     int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
     int32_t num_q_heads, float scale, int32_t partition_size, void* workspace,
     size_t workspace_bytes, void* stream);
+
+/* Capacity in bytes of the library-owned scratch array used by
+ * pkv_paged_attention_decode_static (16 MiB on every device that loads the
+ * library, held until the process exits). */
+#define PKV_STATIC_SCRATCH_BYTES (16u << 20)
+
+/* Allocation-free variant of pkv_paged_attention_decode.  (The paper has no
+ * counterpart: this is a deployment convenience of this library.)
+ *
+ * For callers that cannot allocate device memory themselves -- for example a
+ * plugin whose host framework owns every device allocation, or a serving loop
+ * that must never call cudaMalloc/cudaFree in its steady state (both can
+ * synchronise the device or fail under memory pressure).  The split-K partial
+ * states go to a fixed array of PKV_STATIC_SCRATCH_BYTES bytes that the library
+ * declares in device global memory, so the caller passes no workspace and the
+ * call allocates nothing.  Arguments, results and errors are those of
+ * pkv_paged_attention_decode, plus:
+ *   - returns PKV_ERR_CAPACITY, launching nothing, when these sizes need more
+ *     scratch than PKV_STATIC_SCRATCH_BYTES (pkv_decode_workspace_bytes tells
+ *     how much they need); use pkv_paged_attention_decode with a caller-owned
+ *     workspace then;
+ *   - the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture;
+ *   - all calls on a device share the one array.  Calls that may run at the
+ *     same time on the GPU (different streams without ordering between them)
+ *     race on it and give wrong results: order them.  Nothing in the array
+ *     needs to start at zero -- each call writes every partial state it reads
+ *     -- so leftover contents from an earlier call do no harm. */
+pkv_status pkv_paged_attention_decode_static(
+    const pkv_cache_desc* cache, void* out, float* lse, const void* q,
+    const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
+    int32_t num_q_heads, float scale, int32_t partition_size, void* stream);
 
 /* Read and clear the device error word of the current device.  Synchronises
  * `stream` first.  *code_out receives the PKV_DEVERR_* bits seen since the

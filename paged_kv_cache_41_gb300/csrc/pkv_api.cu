@@ -137,6 +137,7 @@ const char* pkv_status_string(pkv_status s) {
     case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
     case PKV_ERR_CUDA: return "CUDA error";
     case PKV_ERR_DEVICE: return "device-side error reported by a kernel";
+    case PKV_ERR_CAPACITY: return "request needs more scratch than the library's fixed device array";
   }
   return "unknown status";
 }
@@ -278,6 +279,64 @@ pkv_status pkv_get_device_error(int32_t* code_out, void* stream) {
     return PKV_ERR_CUDA;
   *code_out = (int32_t)v;
   return v ? PKV_ERR_DEVICE : PKV_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode.  Same computation as pkv_paged_attention_decode, but
+// the split-K partial states live in a fixed array that the library itself
+// owns in device global memory, so the caller passes no workspace and nothing
+// here allocates.
+// ---------------------------------------------------------------------------
+}  // extern "C"
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_static_scratch[PKV_STATIC_SCRATCH_BYTES];
+
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device.  Looked up once
+// per device (with that device current) and cached; NULL if the lookup fails.
+void* static_scratch_address() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return nullptr;
+    g_static_ptr[dev] = p;
+  }
+  return g_static_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_paged_attention_decode_static(
+    const pkv_cache_desc* cache, void* out, float* lse, const void* q, const void* k_cache,
+    const void* v_cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads, float scale,
+    int32_t partition_size, void* stream) {
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || max_blocks_per_seq <= 0 || partition_size < 0 || !isfinite(scale))
+    return PKV_ERR_INVALID_ARG;
+  if ((st = check_attention_shape(cache, num_q_heads)) != PKV_OK) return st;
+  if (num_seqs == 0) return PKV_OK;
+  if (partition_size == 0) partition_size = auto_partition(cache, num_seqs, max_blocks_per_seq);
+  if (partition_size % cache->block_size != 0) return PKV_ERR_INVALID_ARG;
+  const int64_t bpp = partition_size / cache->block_size;
+  const int64_t parts = (max_blocks_per_seq + bpp - 1) / bpp;
+  const size_t need =
+      parts > 1 ? partial_bytes((int64_t)num_seqs * num_q_heads, parts, cache->head_dim) : 0;
+  if (need > (size_t)PKV_STATIC_SCRATCH_BYTES) return PKV_ERR_CAPACITY;
+  void* scratch = need ? static_scratch_address() : nullptr;
+  if (need && !scratch) return PKV_ERR_CUDA;
+  return pkv_paged_attention_decode(cache, out, lse, q, k_cache, v_cache, block_tables,
+                                    max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, scale,
+                                    partition_size, scratch, need, stream);
 }
 
 }  // extern "C"

@@ -15,7 +15,9 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpkv.so")
 
-PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA, PKV_ERR_DEVICE = range(5)
+PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA, PKV_ERR_DEVICE, PKV_ERR_CAPACITY = range(6)
+# PKV_STATIC_SCRATCH_BYTES of include/pkv.h: the library-owned scratch array
+STATIC_SCRATCH_BYTES = 16 << 20
 PKV_F32, PKV_BF16 = 0, 1
 DEVERR_SLOT, DEVERR_BLOCK, DEVERR_LENGTH, DEVERR_TIMEOUT = 1, 2, 4, 8
 
@@ -25,6 +27,7 @@ EXPORTED = [
     "pkv_decode_workspace_bytes",
     "pkv_decode_auto_partition",
     "pkv_paged_attention_decode",
+    "pkv_paged_attention_decode_static",
     "pkv_get_device_error",
     "pkv_status_string",
 ]
@@ -66,6 +69,9 @@ def load_library():
     lib.pkv_paged_attention_decode.restype = ctypes.c_int
     lib.pkv_paged_attention_decode.argtypes = [dp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, f32,
                                                i32, vp, ctypes.c_size_t, vp]
+    lib.pkv_paged_attention_decode_static.restype = ctypes.c_int
+    lib.pkv_paged_attention_decode_static.argtypes = [dp, vp, vp, vp, vp, vp, vp, i32, vp, i32,
+                                                      i32, f32, i32, vp]
     lib.pkv_get_device_error.restype = ctypes.c_int
     lib.pkv_get_device_error.argtypes = [ctypes.POINTER(i32), vp]
     lib.pkv_status_string.restype = ctypes.c_char_p
@@ -160,6 +166,25 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, *
         ctypes.byref(desc), _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache),
         _ptr(block_tables), max_blocks, _ptr(seq_lens), b, hq, float(scale), partition_size,
         _ptr(workspace), ws_bytes, _stream(stream)), "pkv_paged_attention_decode")
+    return out
+
+
+def paged_attention_decode_static(q, k_cache, v_cache, block_tables, seq_lens, scale, *,
+                                  out=None, lse=None, partition_size=0, stream=None):
+    """Allocation-free paged decode: the split-K partial states use the
+    library's own fixed device array (include/pkv.h), so no workspace is
+    passed and nothing is allocated by the call itself.  For callers that may
+    not allocate device memory.  Raises PkvError (status PKV_ERR_CAPACITY) when
+    the sizes need more than STATIC_SCRATCH_BYTES of scratch.  Calls that could
+    overlap on the GPU share that array and must be ordered."""
+    desc = cache_desc(k_cache)
+    b, hq, _ = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check(load_library().pkv_paged_attention_decode_static(
+        ctypes.byref(desc), _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), b, hq, float(scale),
+        partition_size, _stream(stream)), "pkv_paged_attention_decode_static")
     return out
 
 
