@@ -141,6 +141,42 @@ pkv_status pkv_paged_attention_decode(
     int32_t num_q_heads, float scale, int32_t partition_size, void* workspace,
     size_t workspace_bytes, void* stream);
 
+/* Bytes of device workspace pkv_shared_prefix_attention needs for these
+ * sizes.  partition_size as for the suffix decode (0 = library choice). */
+size_t pkv_shared_prefix_workspace_bytes(const pkv_cache_desc* cache,
+                                         int32_t num_seqs, int32_t num_q_heads,
+                                         int32_t prefix_len,
+                                         int32_t max_suffix_blocks,
+                                         int32_t partition_size);
+
+/* Shared-prefix attention (M5.3 0x0BC, Hydragen; merge of 0x0BA).  Request r's
+ * logical history is the shared prefix -- prefix_len tokens in the blocks
+ * prefix_block_ids[0 .. prefix_len / P) -- followed by its own suffix of
+ * suffix_lens[r] tokens in blocks suffix_block_tables[r, 0 ..].  The result is
+ * exactly pkv_paged_attention_decode over that concatenated history:
+ *   - for each kv head, the prefix part is one dense contraction of all
+ *     num_seqs * G query rows against the prefix keys on the tensor cores
+ *     (bf16 in, fp32 accumulate), read once instead of once per request;
+ *   - the suffixes run through the paged decode kernel;
+ *   - the (output, LSE) states of both are merged by log-sum-exp.
+ *   out, lse, q, scale, partition_size: as in pkv_paged_attention_decode.
+ *   prefix_block_ids: int32 [prefix_len / P]; prefix_len a multiple of P (the
+ *                  prefix is whole, shared blocks; a partly filled shared tail
+ *                  is copied on write into each request's suffix first).
+ *   suffix_block_tables: int32 [num_seqs, max_suffix_blocks]; suffix_lens:
+ *                  int32 [num_seqs] (0 allowed).
+ *   workspace:     at least pkv_shared_prefix_workspace_bytes, 256-byte
+ *                  aligned.
+ * Supported: bf16 only; head_dim 64 or 128; Hq / Hkv in {1, 2, 4, 8};
+ * block_size 16, 32, 64, 128 or 256. */
+pkv_status pkv_shared_prefix_attention(
+    const pkv_cache_desc* cache, void* out, float* lse, const void* q,
+    const void* k_cache, const void* v_cache, const int32_t* prefix_block_ids,
+    int32_t prefix_len, const int32_t* suffix_block_tables,
+    int32_t max_suffix_blocks, const int32_t* suffix_lens, int32_t num_seqs,
+    int32_t num_q_heads, float scale, int32_t partition_size, void* workspace,
+    size_t workspace_bytes, void* stream);
+
 /* Capacity in bytes of the library-owned scratch array used by
  * pkv_paged_attention_decode_static (16 MiB on every device that loads the
  * library, held until the process exits). */

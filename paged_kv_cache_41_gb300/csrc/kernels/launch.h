@@ -57,6 +57,38 @@ cudaError_t launch_paged_decode(int dtype, int head_dim, int group, const CUtens
 cudaError_t launch_decode_reduce(int dtype, int head_dim, const DecodeArgs& args,
                                  cudaStream_t stream);
 
+// Arguments of the shared-prefix tensor-core kernel.  Grid: (key split,
+// 128-row query tile, kv head).  Its states go to partial slots
+// [0, num_splits) of the same workspace layout the decode kernels use.
+struct PrefixArgs {
+  const int32_t* prefix_block_ids;  // [ceil(prefix_len / P)]
+  float* part_o;                    // [B, Hq, parts_stride, D]
+  float* part_lse;                  // [B, Hq, parts_stride], base 2
+  unsigned int* err;
+  int64_t num_blocks;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t block_size;
+  int32_t prefix_len;
+  int32_t split_len;     // keys per split, a multiple of 128
+  int32_t parts_stride;
+  float qscale;          // softmax scale * log2(e)
+};
+
+// Query rows per CTA and keys per tile of the prefix kernel.
+constexpr int kPrefixRows = 128;
+constexpr int kPrefixKeys = 128;
+__host__ __device__ constexpr int prefix_box_rows(int block_size) {
+  return block_size < kPrefixKeys ? block_size : kPrefixKeys;
+}
+
+cudaError_t launch_prefix_attention(int head_dim, int group, int num_splits,
+                                    const CUtensorMap& tmq, const CUtensorMap& tmk,
+                                    const CUtensorMap& tmv, const PrefixArgs& args,
+                                    cudaStream_t stream);
+size_t prefix_smem_bytes(int head_dim, int split_len, int block_size);
+
 // Stage count and dynamic shared memory of the partial kernel.
 int decode_num_stages(int block_size, int head_dim, int elem_bytes);
 size_t decode_smem_bytes(int block_size, int head_dim, int elem_bytes, int group, int stages);

@@ -117,6 +117,66 @@ int32_t auto_partition(const pkv_cache_desc* c, int32_t num_seqs, int32_t max_bl
   return ps;
 }
 
+
+// 3-D map over q [B, Hq, D] (bf16) with 128-byte swizzle; box = 64 columns x
+// G heads x rpb requests.
+pkv_status encode_q_map_sw128(CUtensorMap* map, const void* q, int32_t num_seqs, int32_t num_q_heads,
+                              int32_t head_dim, int group, int rpb) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return PKV_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_q_heads, (cuuint64_t)num_seqs};
+  cuuint64_t strides[2] = {dims[0] * 2, dims[0] * dims[1] * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)rpb};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_UNSUPPORTED;
+}
+
+// 4-D map over a bf16 pool with 128-byte swizzle; box = 64 columns x 1 head x
+// `rows` token rows x 1 block.
+pkv_status encode_cache_map_sw128(CUtensorMap* map, const pkv_cache_desc* c, const void* base,
+                                  int rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return PKV_ERR_CUDA;
+  cuuint64_t dims[4] = {(cuuint64_t)c->head_dim, (cuuint64_t)c->num_kv_heads,
+                        (cuuint64_t)c->block_size, (cuuint64_t)c->num_blocks};
+  cuuint64_t strides[3] = {dims[0] * 2, dims[0] * dims[1] * 2, dims[0] * dims[1] * dims[2] * 2};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_UNSUPPORTED;
+}
+
+// Keys per prefix split: whole 128-key tiles, spread so that (split x query
+// tile x kv head) CTAs cover the SMs about once.
+int32_t prefix_split_len(const pkv_cache_desc* c, int32_t num_seqs, int32_t num_q_heads,
+                         int32_t prefix_len) {
+  const int G = num_q_heads / c->num_kv_heads;
+  const int64_t m_tiles = ((int64_t)num_seqs * G + pkv::kPrefixRows - 1) / pkv::kPrefixRows;
+  const int64_t pairs = m_tiles * c->num_kv_heads;
+  const int64_t tiles = (prefix_len + pkv::kPrefixKeys - 1) / pkv::kPrefixKeys;
+  int64_t splits = (sm_count() + pairs / 2) / pairs;
+  if (splits < 1) splits = 1;
+  if (splits > tiles) splits = tiles;
+  const int64_t per = (tiles + splits - 1) / splits;
+  return (int32_t)(per * pkv::kPrefixKeys);
+}
+
+// Shapes the shared-prefix path is compiled for (bf16 tensor cores).
+pkv_status check_prefix_shape(const pkv_cache_desc* c, int32_t num_q_heads, int32_t prefix_len) {
+  pkv_status st = check_attention_shape(c, num_q_heads);
+  if (st != PKV_OK) return st;
+  if (c->dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+  const int P = c->block_size;
+  if (pkv::kPrefixKeys % P != 0 && P % pkv::kPrefixKeys != 0) return PKV_ERR_UNSUPPORTED;
+  if (prefix_len < 0 || prefix_len % P != 0) return PKV_ERR_INVALID_ARG;
+  return PKV_OK;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Partial-state workspace: [B, Hq, parts] x (D floats of output + 1 LSE).
@@ -264,6 +324,124 @@ pkv_status pkv_paged_attention_decode(const pkv_cache_desc* cache, void* out, fl
   cudaError_t e = pkv::launch_paged_decode(cache->dtype, cache->head_dim,
                                            num_q_heads / cache->num_kv_heads, tmk, tmv, a,
                                            as_stream(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+size_t pkv_shared_prefix_workspace_bytes(const pkv_cache_desc* cache, int32_t num_seqs,
+                                         int32_t num_q_heads, int32_t prefix_len,
+                                         int32_t max_suffix_blocks, int32_t partition_size) {
+  if (check_cache(cache) != PKV_OK || num_seqs <= 0 || num_q_heads <= 0 || max_suffix_blocks <= 0 ||
+      partition_size < 0 || check_prefix_shape(cache, num_q_heads, prefix_len) != PKV_OK)
+    return 0;
+  if (partition_size == 0) partition_size = auto_partition(cache, num_seqs, max_suffix_blocks);
+  if (partition_size % cache->block_size != 0) return 0;
+  const int64_t bpp = partition_size / cache->block_size;
+  const int64_t suffix_parts = (max_suffix_blocks + bpp - 1) / bpp;
+  int64_t prefix_parts = 0;
+  if (prefix_len > 0) {
+    const int32_t sl = prefix_split_len(cache, num_seqs, num_q_heads, prefix_len);
+    prefix_parts = (prefix_len + sl - 1) / sl;
+  }
+  return partial_bytes((int64_t)num_seqs * num_q_heads, prefix_parts + suffix_parts,
+                       cache->head_dim);
+}
+
+pkv_status pkv_shared_prefix_attention(
+    const pkv_cache_desc* cache, void* out, float* lse, const void* q, const void* k_cache,
+    const void* v_cache, const int32_t* prefix_block_ids, int32_t prefix_len,
+    const int32_t* suffix_block_tables, int32_t max_suffix_blocks, const int32_t* suffix_lens,
+    int32_t num_seqs, int32_t num_q_heads, float scale, int32_t partition_size, void* workspace,
+    size_t workspace_bytes, void* stream) {
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || max_suffix_blocks <= 0 || partition_size < 0 || !isfinite(scale))
+    return PKV_ERR_INVALID_ARG;
+  if ((st = check_prefix_shape(cache, num_q_heads, prefix_len)) != PKV_OK) return st;
+  if (num_seqs == 0) return PKV_OK;
+  if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
+  if (!out || !q || !k_cache || !v_cache || !suffix_block_tables || !suffix_lens ||
+      (prefix_len > 0 && !prefix_block_ids))
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_INVALID_ARG;
+  if (partition_size == 0) partition_size = auto_partition(cache, num_seqs, max_suffix_blocks);
+  if (partition_size % cache->block_size != 0) return PKV_ERR_INVALID_ARG;
+  const int32_t bpp = partition_size / cache->block_size;
+  const int64_t suffix_parts = (max_suffix_blocks + (int64_t)bpp - 1) / bpp;
+  int32_t split_len = 0, prefix_parts = 0;
+  if (prefix_len > 0) {
+    split_len = prefix_split_len(cache, num_seqs, num_q_heads, prefix_len);
+    prefix_parts = (prefix_len + split_len - 1) / split_len;
+  }
+  const int64_t parts = prefix_parts + suffix_parts;
+  if (suffix_parts > 65535 || parts > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  const size_t need = partial_bytes((int64_t)num_seqs * num_q_heads, parts, cache->head_dim);
+  if (workspace_bytes < need || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return PKV_ERR_INVALID_ARG;
+  const int G = num_q_heads / cache->num_kv_heads;
+  unsigned int* err = device_error_word();
+  if (!err) return PKV_ERR_CUDA;
+  const size_t rows_parts = (size_t)num_seqs * num_q_heads * (size_t)parts;
+  float* part_o = static_cast<float*>(workspace);
+  float* part_lse = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) +
+                                             align256(rows_parts * cache->head_dim * 4));
+  const float qscale = scale * 1.4426950408889634f;
+  cudaStream_t s = as_stream(stream);
+
+  if (prefix_parts > 0) {
+    CUtensorMap tmq, tmk, tmv;
+    if ((st = encode_q_map_sw128(&tmq, q, num_seqs, num_q_heads, cache->head_dim, G,
+                                 pkv::kPrefixRows / G)) != PKV_OK)
+      return st;
+    const int rows = pkv::prefix_box_rows(cache->block_size);
+    if ((st = encode_cache_map_sw128(&tmk, cache, k_cache, rows)) != PKV_OK) return st;
+    if ((st = encode_cache_map_sw128(&tmv, cache, v_cache, rows)) != PKV_OK) return st;
+    pkv::PrefixArgs pa{};
+    pa.prefix_block_ids = prefix_block_ids;
+    pa.part_o = part_o;
+    pa.part_lse = part_lse;
+    pa.err = err;
+    pa.num_blocks = cache->num_blocks;
+    pa.num_seqs = num_seqs;
+    pa.num_q_heads = num_q_heads;
+    pa.num_kv_heads = cache->num_kv_heads;
+    pa.block_size = cache->block_size;
+    pa.prefix_len = prefix_len;
+    pa.split_len = split_len;
+    pa.parts_stride = (int32_t)parts;
+    pa.qscale = qscale;
+    if (pkv::launch_prefix_attention(cache->head_dim, G, prefix_parts, tmq, tmk, tmv, pa, s) !=
+        cudaSuccess)
+      return PKV_ERR_CUDA;
+  }
+
+  const int rows = pkv::box_rows_for(cache->block_size);
+  CUtensorMap tmk, tmv;
+  if ((st = encode_cache_map(&tmk, cache, k_cache, rows)) != PKV_OK) return st;
+  if ((st = encode_cache_map(&tmv, cache, v_cache, rows)) != PKV_OK) return st;
+  pkv::DecodeArgs a{};
+  a.q = q;
+  a.block_tables = suffix_block_tables;
+  a.seq_lens = suffix_lens;
+  a.part_o = part_o;
+  a.part_lse = part_lse;
+  a.out = out;
+  a.lse_out = lse;
+  a.err = err;
+  a.num_blocks = cache->num_blocks;
+  a.max_blocks = max_suffix_blocks;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.block_size = cache->block_size;
+  a.blocks_per_part = bpp;
+  a.max_parts = (int32_t)suffix_parts;
+  a.part_offset = prefix_parts;
+  a.parts_stride = (int32_t)parts;
+  a.num_stages = pkv::decode_num_stages(cache->block_size, cache->head_dim, elem_bytes(cache->dtype));
+  a.qscale = qscale;
+  a.direct = 0;
+  cudaError_t e = pkv::launch_paged_decode(cache->dtype, cache->head_dim, G, tmk, tmv, a, s);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -28,6 +28,8 @@ EXPORTED = [
     "pkv_decode_auto_partition",
     "pkv_paged_attention_decode",
     "pkv_paged_attention_decode_static",
+    "pkv_shared_prefix_workspace_bytes",
+    "pkv_shared_prefix_attention",
     "pkv_get_device_error",
     "pkv_status_string",
 ]
@@ -72,6 +74,11 @@ def load_library():
     lib.pkv_paged_attention_decode_static.restype = ctypes.c_int
     lib.pkv_paged_attention_decode_static.argtypes = [dp, vp, vp, vp, vp, vp, vp, i32, vp, i32,
                                                       i32, f32, i32, vp]
+    lib.pkv_shared_prefix_workspace_bytes.restype = ctypes.c_size_t
+    lib.pkv_shared_prefix_workspace_bytes.argtypes = [dp, i32, i32, i32, i32, i32]
+    lib.pkv_shared_prefix_attention.restype = ctypes.c_int
+    lib.pkv_shared_prefix_attention.argtypes = [dp, vp, vp, vp, vp, vp, vp, i32, vp, i32, vp, i32,
+                                                i32, f32, i32, vp, ctypes.c_size_t, vp]
     lib.pkv_get_device_error.restype = ctypes.c_int
     lib.pkv_get_device_error.argtypes = [ctypes.POINTER(i32), vp]
     lib.pkv_status_string.restype = ctypes.c_char_p
@@ -185,6 +192,36 @@ def paged_attention_decode_static(q, k_cache, v_cache, block_tables, seq_lens, s
         ctypes.byref(desc), _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache),
         _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), b, hq, float(scale),
         partition_size, _stream(stream)), "pkv_paged_attention_decode_static")
+    return out
+
+
+def shared_prefix_workspace_bytes(k_cache, num_seqs, num_q_heads, prefix_len,
+                                  max_suffix_blocks, partition_size=0) -> int:
+    desc = cache_desc(k_cache)
+    return load_library().pkv_shared_prefix_workspace_bytes(
+        ctypes.byref(desc), num_seqs, num_q_heads, prefix_len, max_suffix_blocks, partition_size)
+
+
+def shared_prefix_attention(q, k_cache, v_cache, prefix_block_ids, prefix_len,
+                            suffix_block_tables, suffix_lens, scale, *, out=None, lse=None,
+                            partition_size=0, workspace=None, stream=None):
+    """Attention over prefix ++ suffix for every request, with the shared
+    prefix as one tensor-core contraction per kv head (include/pkv.h)."""
+    desc = cache_desc(k_cache)
+    b, hq, _ = q.shape
+    max_suffix = suffix_block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    need = shared_prefix_workspace_bytes(k_cache, b, hq, prefix_len, max_suffix,
+                                         partition_size) if b else 0
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load_library().pkv_shared_prefix_attention(
+        ctypes.byref(desc), _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+        _ptr(prefix_block_ids), int(prefix_len), _ptr(suffix_block_tables), max_suffix,
+        _ptr(suffix_lens), b, hq, float(scale), partition_size, _ptr(workspace), ws_bytes,
+        _stream(stream)), "pkv_shared_prefix_attention")
     return out
 
 

@@ -187,3 +187,72 @@ def test_host_validation_rejects_before_launch():
             pkv.paged_attention_decode(q, kc3, kc3, bt, sl, 1.0)
         assert ei.value.status == pkv.PKV_ERR_UNSUPPORTED
     assert pkv.get_device_error() == 0
+
+
+# ------------------------------------------------------------------ shared prefix
+def _shared_prefix_run(sp, rows=None, suffix_lens=None, partition_size=0):
+    """Device: append parent rows, CoW copies, child rows, then the shared-prefix
+    call.  Oracle: its own pool (own slots) and the concatenated-table decode."""
+    shape = (sp.num_blocks, sp.block_size, sp.num_kv_heads, sp.head_dim)
+    kc = torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    pkv.kv_append(kc, vc, sp.parent_k, sp.parent_v, torch.from_numpy(sp.parent_slots).cuda())
+    pkv.kv_block_copy(kc, vc, torch.from_numpy(sp.cow_pairs).cuda())
+    pkv.kv_append(kc, vc, sp.child_k, sp.child_v, torch.from_numpy(sp.child_slots).cuda())
+    lens = sp.suffix_lens if suffix_lens is None else np.asarray(suffix_lens, np.int32)
+    lse = torch.empty(sp.num_seqs, sp.num_q_heads, dtype=torch.float32, device="cuda")
+    out = pkv.shared_prefix_attention(
+        sp.q, kc, vc, torch.from_numpy(sp.prefix_block_ids).cuda(), sp.prefix_len,
+        torch.from_numpy(sp.suffix_tables).cuda(), torch.from_numpy(lens).cuda(), sp.scale,
+        lse=lse, partition_size=partition_size)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    hk = np.full(shape, 0x7FC0, np.uint16)
+    hv = np.full(shape, 0x7FC0, np.uint16)
+    n_par = sp.prefix_len + sp.shared_tail
+    ps = np.array([oracle.slot_for_position(sp.parent_table, sp.block_size, t)
+                   for t in range(n_par)], np.int64)
+    oracle.kv_append(hk, hv, wl.to_numpy_storage(sp.parent_k), wl.to_numpy_storage(sp.parent_v), ps)
+    oracle.kv_block_copy(hk, hv, sp.cow_pairs)
+    ck, cv = wl.to_numpy_storage(sp.child_k), wl.to_numpy_storage(sp.child_v)
+    for r in range(sp.num_seqs):
+        table = np.concatenate([sp.prefix_block_ids, sp.suffix_tables[r]])
+        lo, hi = sp.child_offsets[r], sp.child_offsets[r + 1]
+        cs = np.array([oracle.slot_for_position(table, sp.block_size, n_par + i)
+                       for i in range(hi - lo)], np.int64)
+        oracle.kv_append(hk, hv, np.ascontiguousarray(ck[lo:hi]), np.ascontiguousarray(cv[lo:hi]), cs)
+    q = wl.to_numpy_storage(sp.q)
+    st, sl = sp.suffix_tables, lens
+    if rows is not None:
+        q, st, sl = q[rows], st[rows], sl[rows]
+    ref, ref_lse = oracle.shared_prefix(np.ascontiguousarray(q), hk, hv, sp.prefix_block_ids,
+                                        sp.prefix_len, np.ascontiguousarray(st),
+                                        np.ascontiguousarray(sl), sp.scale, nthreads=pu.NTHREADS)
+    got, got_lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    if rows is not None:
+        got, got_lse = got[rows], got_lse[rows]
+    pu.assert_close(got, ref, "shared prefix out")
+    pu.assert_close(got_lse, ref_lse, "shared prefix lse")
+
+
+@pytest.mark.parametrize("batch,prefix,hq,hkv,d", [
+    (16, 256, 32, 8, 128), (5, 384, 8, 2, 128), (40, 128, 16, 16, 64), (3, 512, 16, 2, 128),
+])
+def test_shared_prefix_small(batch, prefix, hq, hkv, d):
+    sp = wl.shared_prefix_batch(device="cuda", batch=batch, prefix_len=prefix, shared_tail=8,
+                                suffix_lo=8, suffix_hi=200, hq=hq, hkv=hkv, d=d, seed=81 + batch)
+    _shared_prefix_run(sp)
+
+
+def test_shared_prefix_with_empty_suffixes():
+    sp = wl.shared_prefix_batch(device="cuda", batch=9, prefix_len=256, shared_tail=0,
+                                suffix_lo=0, suffix_hi=40, seed=91)
+    lens = sp.suffix_lens.copy()
+    lens[::3] = 0
+    _shared_prefix_run(sp, suffix_lens=lens)
+
+
+def test_shared_prefix_full_size_sampled():
+    sp = wl.shared_prefix_batch(device="cuda")  # 128 requests, 2048-token prefix
+    rows = np.array([0, 1, 31, 32, 63, 64, 100, 127])
+    _shared_prefix_run(sp, rows=rows)
