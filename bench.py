@@ -374,6 +374,176 @@ def run_pkv(args, rank, world, local):
     return res, b
 
 
+# ------------------------------------------------------------------ shared prefix
+def run_shared(args, rank, world, local):
+    """Shared-prefix batch: 128 requests on one 2048-token prefix (128 full
+    blocks) plus private suffixes U{16..512} whose first 8 rows were copied on
+    write from the parent's shared tail block."""
+    import torch
+    from paged_kv_cache_41_gb300 import pkv
+    from paged_kv_cache_41_gb300 import workloads as wl
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    pkv.load_library()
+    sp = wl.shared_prefix_batch(device=dev, seed=5 + rank, batch=args.batch or 128)
+    shape = (sp.num_blocks, sp.block_size, sp.num_kv_heads, sp.head_dim)
+    kc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    pkv.kv_append(kc, vc, sp.parent_k, sp.parent_v, torch.from_numpy(sp.parent_slots).to(dev))
+    pairs = torch.from_numpy(sp.cow_pairs).to(dev)
+    pkv.kv_block_copy(kc, vc, pairs)
+    pkv.kv_append(kc, vc, sp.child_k, sp.child_v, torch.from_numpy(sp.child_slots).to(dev))
+    pre = torch.from_numpy(sp.prefix_block_ids).to(dev)
+    st = torch.from_numpy(sp.suffix_tables).to(dev)
+    sl = torch.from_numpy(sp.suffix_lens).to(dev)
+    B, Hq, D = sp.num_seqs, sp.num_q_heads, sp.head_dim
+    out = torch.empty_like(sp.q)
+    ws = torch.empty(pkv.shared_prefix_workspace_bytes(kc, B, Hq, sp.prefix_len, st.shape[1]),
+                     dtype=torch.uint8, device=dev)
+    split = pkv.prefix_split_len(kc, B, Hq, sp.prefix_len)
+    nsplit = -(-sp.prefix_len // split)
+    so = torch.empty(B, Hq, nsplit, D, dtype=torch.float32, device=dev)
+    sls = torch.empty(B, Hq, nsplit, dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > L2 (129 MB)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    stream = torch.cuda.current_stream()
+
+    def prefix_call():
+        pkv.prefix_attention_states(sp.q, kc, vc, pre, sp.prefix_len, sp.scale, split_len=split,
+                                    states_o=so, states_lse=sls)
+
+    def full_call():
+        pkv.shared_prefix_attention(sp.q, kc, vc, pre, sp.prefix_len, st, sl, sp.scale, out=out,
+                                    workspace=ws)
+
+    def timed(fn, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for a, b in evs:
+            flush.fill_(1)  # evict the prefix K/V and q from L2 before each call
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b) for a, b in evs]))
+
+    for _ in range(args.warmup):
+        prefix_call()
+        full_call()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = ClockSampler(local)
+    clocks.start()
+    n = max(args.steps, 20)
+    prefix_ms = all_max(timed(prefix_call, n), world)
+    full_ms = all_max(timed(full_call, n), world)
+    clk = clocks.stop()
+    assert pkv.get_device_error() == 0
+
+    # end to end: q, tables and lengths from pinned host memory, output back
+    h_q, h_st, h_sl = sp.q.cpu().pin_memory(), st.cpu().pin_memory(), sl.cpu().pin_memory()
+    h_pre = pre.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    d_q, d_st, d_sl, d_pre = (torch.empty_like(x) for x in (sp.q, st, sl, pre))
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_st, h_sl, h_pre))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e():
+        d_q.copy_(h_q, non_blocking=True)
+        d_st.copy_(h_st, non_blocking=True)
+        d_sl.copy_(h_sl, non_blocking=True)
+        d_pre.copy_(h_pre, non_blocking=True)
+        pkv.shared_prefix_attention(d_q, kc, vc, d_pre, sp.prefix_len, d_st, d_sl, sp.scale,
+                                    out=out, workspace=ws)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e()
+    e2e_ms = timed(e2e, n)
+    assert pkv.get_device_error() == 0
+
+    flops = 4.0 * B * Hq * sp.prefix_len * D
+    tflops = flops / (prefix_ms * 1e-3) / 1e12
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    row = kv_row_bytes_dims(sp.num_kv_heads, D, 2)
+    logical = B * (sp.prefix_len + float(sp.suffix_lens.mean())) * row
+    unique = (sp.prefix_len + float(sp.suffix_lens.sum())) * row
+    res = {
+        "metric": "shared-prefix TFLOP/s (prefix contraction on tensor cores, % of dense bf16 peak)",
+        "value": world * tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": n,
+        "warmup": args.warmup, "ms_per_step": full_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v, seeded suffix lengths and block placement)",
+        "config": {"workload": "shared-prefix batch", "batch": B, "prefix_len": sp.prefix_len,
+                   "suffix_len_mean": float(sp.suffix_lens.mean()), "num_q_heads": Hq,
+                   "num_kv_heads": sp.num_kv_heads, "head_dim": D, "block_size": sp.block_size,
+                   "prefix_split_len": split, "prefix_splits": nsplit,
+                   "cow_pairs": int(sp.cow_pairs.shape[0]),
+                   "l2": "flushed (256 MB write) before every timed call"},
+        "prefix_ms": prefix_ms,
+        "shared_prefix_call_ms": full_ms,
+        "logical_kv_bytes": logical, "unique_kv_bytes": unique,
+        "effective_kv_gbps": logical / (full_ms * 1e-3) / 1e9,
+        "roofline": {"bound": "tensor", "kernel": "prefix_attention_kernel",
+                     "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                     "peak_kind": "measured bf16_tflops (burst, kernel timed alone)",
+                     "traffic": None, "algorithmic_flops_per_launch": flops},
+        "e2e": {"value": world * logical / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s (logical K/V)",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": n * 4,
+        "clocks": clk,
+    }
+    return res, sp
+
+
+def kv_row_bytes_dims(hkv, d, elem):
+    return 2 * hkv * d * elem
+
+
+def shared_cpu_baseline(sp, seconds):
+    """The oracle on whole requests of the shared-prefix batch (its own pool)."""
+    import oracle
+    from paged_kv_cache_41_gb300 import workloads as wl
+    nthreads = len(os.sched_getaffinity(0))
+    shape = (sp.num_blocks, sp.block_size, sp.num_kv_heads, sp.head_dim)
+    hk = np.zeros(shape, np.uint16)
+    hv = np.zeros(shape, np.uint16)
+    n_par = sp.prefix_len + sp.shared_tail
+    ps = np.array([oracle.slot_for_position(sp.parent_table, sp.block_size, t)
+                   for t in range(n_par)], np.int64)
+    oracle.kv_append(hk, hv, wl.to_numpy_storage(sp.parent_k), wl.to_numpy_storage(sp.parent_v), ps)
+    oracle.kv_block_copy(hk, hv, sp.cow_pairs)
+    ck, cv = wl.to_numpy_storage(sp.child_k), wl.to_numpy_storage(sp.child_v)
+    for r in range(sp.num_seqs):
+        table = np.concatenate([sp.prefix_block_ids, sp.suffix_tables[r]])
+        lo, hi = sp.child_offsets[r], sp.child_offsets[r + 1]
+        cs = np.array([oracle.slot_for_position(table, sp.block_size, n_par + i)
+                       for i in range(hi - lo)], np.int64)
+        oracle.kv_append(hk, hv, np.ascontiguousarray(ck[lo:hi]), np.ascontiguousarray(cv[lo:hi]), cs)
+    q = wl.to_numpy_storage(sp.q)
+    done = 0
+    el = 0.0
+    flops = 0.0
+    while el < seconds and done < sp.num_seqs:
+        r = done
+        t0 = time.perf_counter()
+        oracle.shared_prefix(np.ascontiguousarray(q[r:r + 1]), hk, hv, sp.prefix_block_ids,
+                             sp.prefix_len, np.ascontiguousarray(sp.suffix_tables[r:r + 1]),
+                             np.ascontiguousarray(sp.suffix_lens[r:r + 1]), sp.scale,
+                             nthreads=nthreads)
+        el += time.perf_counter() - t0
+        flops += 4.0 * sp.num_q_heads * sp.prefix_len * sp.head_dim
+        done += 1
+    return {"value": flops / el / 1e12, "unit": "TFLOP/s (prefix part)", "cores": nthreads,
+            "kind": "oracle",
+            "sample": f"{done} of {sp.num_seqs} requests, all heads, prefix + suffix, fp64 oracle"}
+
+
+
 def main():
     args = parse()
     if args.warmup < 3:
@@ -385,11 +555,15 @@ def main():
         res = run_reference(args)
         print(json.dumps(res), flush=True)
         return
-    res, b = run_pkv(args, rank, world, local)
+    if args.workload == "shared":
+        res, sp = run_shared(args, rank, world, local)
+        if rank == 0 and not args.no_cpu_baseline and world == 1:
+            res["cpu_baseline"] = shared_cpu_baseline(sp, args.cpu_sample_seconds)
+    else:
+        res, b = run_pkv(args, rank, world, local)
+        if rank == 0 and not args.no_cpu_baseline and world == 1:
+            res["cpu_baseline"] = cpu_baseline(b, args.cpu_sample_seconds)
     if rank == 0:
-        if not args.no_cpu_baseline and world == 1:
-            cb = cpu_baseline(b, args.cpu_sample_seconds)
-            res["cpu_baseline"] = cb
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist

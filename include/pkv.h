@@ -177,6 +177,33 @@ pkv_status pkv_shared_prefix_attention(
     int32_t num_q_heads, float scale, int32_t partition_size, void* workspace,
     size_t workspace_bytes, void* stream);
 
+/* Keys per split the library uses for the prefix of these sizes (a multiple
+ * of 128, chosen so that splits x query tiles x kv heads covers the SMs about
+ * once); 0 for unsupported sizes. */
+int32_t pkv_prefix_split_len(const pkv_cache_desc* cache, int32_t num_seqs,
+                             int32_t num_q_heads, int32_t prefix_len);
+
+/* Chunk-first phase of shared-prefix attention (M5.3 0x0BD, ChunkAttention:
+ * batch the queries of every sequence against a shared chunk and materialise
+ * partial softmax states; Hydragen's attention_with_lse over the shared part,
+ * 0x0BC).  The prefix keys are cut into splits of split_len keys; for every
+ * request r, query head h and split s it writes the state of attention of
+ * q[r, h] over that split's keys alone:
+ *   states_o[((r * Hq + h) * n + s) * D + c]  normalised output (fp32),
+ *   states_lse[(r * Hq + h) * n + s]          natural-log LSE (fp32),
+ * with n = ceil(prefix_len / split_len).  Merging a request's n states (and
+ * any suffix state) by log-sum-exp gives attention over prefix ++ suffix.
+ *   split_len: a positive multiple of 128 (pkv_prefix_split_len suggests one).
+ * Other arguments and support as in pkv_shared_prefix_attention. */
+pkv_status pkv_prefix_attention_states(const pkv_cache_desc* cache,
+                                       float* states_o, float* states_lse,
+                                       const void* q, const void* k_cache,
+                                       const void* v_cache,
+                                       const int32_t* prefix_block_ids,
+                                       int32_t prefix_len, int32_t split_len,
+                                       int32_t num_seqs, int32_t num_q_heads,
+                                       float scale, void* stream);
+
 /* Capacity in bytes of the library-owned scratch array used by
  * pkv_paged_attention_decode_static (16 MiB on every device that loads the
  * library, held until the process exits). */

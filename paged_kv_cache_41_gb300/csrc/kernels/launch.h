@@ -74,14 +74,12 @@ struct PrefixArgs {
   int32_t split_len;     // keys per split, a multiple of 128
   int32_t parts_stride;
   float qscale;          // softmax scale * log2(e)
+  float lse_scale;       // 1: LSE in base 2 (partial states); ln 2: natural log
 };
 
 // Query rows per CTA and keys per tile of the prefix kernel.
 constexpr int kPrefixRows = 128;
 constexpr int kPrefixKeys = 128;
-__host__ __device__ constexpr int prefix_box_rows(int block_size) {
-  return block_size < kPrefixKeys ? block_size : kPrefixKeys;
-}
 
 cudaError_t launch_prefix_attention(int head_dim, int group, int num_splits,
                                     const CUtensorMap& tmq, const CUtensorMap& tmk,

@@ -15,8 +15,13 @@
 //     i.e. TMEM lane t, so the softmax needs no cross-thread reduction;
 //   * Q (128 rows x D), K and V tiles (128 keys x D) arrive by TMA with
 //     128-byte swizzle, directly in the canonical K-major layout the UMMA
-//     descriptors expect; K/V blocks are gathered through the prefix's block
-//     ids, keys past the prefix read a zero-filled out-of-range box;
+//     descriptors expect; K/V boxes are gathered through the prefix's block
+//     ids, one box per producer lane so a tile's boxes are in flight
+//     together; keys past the prefix read a zero-filled out-of-range box;
+//   * warp roles: warps 0-3 softmax (one TMEM lane, i.e. query row, per
+//     thread), warp 4 issues the MMAs, warps 5 and 6 gather K and V; stages
+//     are handed over by mbarriers and tcgen05.commit, never by a CTA-wide
+//     barrier;
 //   * S = Q K^T and O += P V are tcgen05.mma (bf16 in, fp32 accumulate in
 //     TMEM); S is double-buffered in TMEM so QK^T of tile j+1 runs while the
 //     softmax of tile j does; K and V are double-buffered in shared memory;
@@ -49,7 +54,7 @@ size_t prefix_smem_bytes(int head_dim, int split_len, int block_size) {
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(224, 1)
     prefix_attention_kernel(const __grid_constant__ CUtensorMap tmq,
                             const __grid_constant__ CUtensorMap tmk,
                             const __grid_constant__ CUtensorMap tmv, const PrefixArgs a) {
@@ -61,7 +66,6 @@ __global__ void __launch_bounds__(128, 1)
 
   const int split = blockIdx.x, mt = blockIdx.y, kvh = blockIdx.z;
   const int P = a.block_size;
-  const int PB = prefix_box_rows(P);
   const int key0 = split * a.split_len;
   const int nkeys = min(a.split_len, a.prefix_len - key0);
   if (nkeys <= 0) return;
@@ -77,31 +81,32 @@ __global__ void __launch_bounds__(128, 1)
   unsigned char* vs = ks + 2 * kTile;      // two stages
   unsigned char* ps = vs + 2 * kTile;      // 128 rows x 128 keys bf16 (two halves)
   int* ids = reinterpret_cast<int*>(ps + 2 * kHalfBytes);
-  __shared__ uint64_t qbar, kfull[2], vfull[2], sbar, obar;
+  // qbar: Q by TMA; kfull/vfull: a producer warp filled a stage; kfree/vfree:
+  // the MMA that read a stage completed; sfull[b]: QK^T into S buffer b done;
+  // pfull: the four softmax warps wrote P; ofull: PV done.
+  __shared__ uint64_t qbar, kfull[2], vfull[2], kfree[2], vfree[2], sfull[2], pfull, ofull;
   __shared__ uint32_t tmem_base;
-  __shared__ int abort_flag;
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   if (t == 0) {
     mbar_init(&qbar, 1);
-    mbar_init(&kfull[0], 1);
-    mbar_init(&kfull[1], 1);
-    mbar_init(&vfull[0], 1);
-    mbar_init(&vfull[1], 1);
-    mbar_init(&sbar, 1);
-    mbar_init(&obar, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kfull[i], 1);
+      mbar_init(&vfull[i], 1);
+      mbar_init(&kfree[i], 1);
+      mbar_init(&vfree[i], 1);
+      mbar_init(&sfull[i], 1);
+    }
+    mbar_init(&pfull, 4);
+    mbar_init(&ofull, 1);
     fence_barrier_init();
-    prefetch_tensormap(&tmq);
-    prefetch_tensormap(&tmk);
-    prefetch_tensormap(&tmv);
-    abort_flag = 0;
   }
   if (warp == 0) tc::tmem_alloc(&tmem_base, 512);
   for (int i = t; i < nid; i += blockDim.x) {
     int b = __ldg(a.prefix_block_ids + id0 + i);
     if (b < 0 || (int64_t)b >= a.num_blocks) {
       atomicOr(a.err, PKV_DEVERR_BLOCK);
-      b = (int)a.num_blocks;  // an out-of-range box reads zeros
+      b = -1;  // rows of a bad block are zero-filled
     }
     ids[i] = b;
   }
@@ -109,172 +114,196 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
   const uint32_t tO = tmem + 256;
 
-  // ---- loads and MMA issue (thread 0 only)
-  auto load_kv = [&](const CUtensorMap* map, unsigned char* dst, uint64_t* bar, int jt) {
-    mbar_arrive_expect_tx(bar, kTile);
-    for (int b = 0; b < kPrefixKeys / PB; ++b) {
-      const int key = key0 + jt * kPrefixKeys + b * PB;
-      int blk = (int)a.num_blocks, row = 0;
-      if (key < a.prefix_len) {
-        blk = ids[key / P - id0];
-        row = key % P;
+  if (warp == 5 || warp == 6) {
+    // ============================================================ producers
+    // warp 5 streams Q and K, warp 6 streams V.  A tile is kPrefixKeys / PB
+    // blocks x H column halves of TMA boxes (PB rows x 128 B each, 128-byte
+    // swizzle); each lane issues its own boxes, so the boxes of a tile are
+    // requested in parallel.  A stage is refilled as soon as the MMA that read
+    // it has completed; keys past the split read a zero-filled out-of-range
+    // box.
+    const bool is_k = warp == 5;
+    const CUtensorMap* map = is_k ? &tmk : &tmv;
+    unsigned char* base = is_k ? ks : vs;
+    uint64_t* fullb = is_k ? kfull : vfull;
+    uint64_t* freeb = is_k ? kfree : vfree;
+    const int PB = P < kPrefixKeys ? P : kPrefixKeys;
+    const int nbox = (kPrefixKeys / PB) * H;
+    if (lane == 0) {
+      prefetch_tensormap(map);
+      if (is_k) {
+        prefetch_tensormap(&tmq);
+        mbar_arrive_expect_tx(&qbar, kTile);
+#pragma unroll
+        for (int h = 0; h < H; ++h)
+          tma_load_3d(qs + h * kHalfBytes, &tmq, h * 64, kvh * G, mt * RPB, &qbar);
       }
-#pragma unroll
-      for (int h = 0; h < H; ++h)
-        tma_load_4d(dst + h * kHalfBytes + b * PB * 128, map, h * 64, kvh, row, blk, bar);
     }
-  };
-  auto issue_qk = [&](int jt) -> bool {
-    if (!mbar_wait(&kfull[jt & 1], (jt >> 1) & 1)) return false;
-    const uint32_t kb = smem_u32(ks + (jt & 1) * kTile), qb = smem_u32(qs);
-#pragma unroll
-    for (int k = 0; k < D / 16; ++k) {
-      const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-      tc::mma_bf16(tmem + (jt & 1) * 128, tc::smem_desc_sw128(qb + off, 16, 1024),
-                   tc::smem_desc_sw128(kb + off, 16, 1024), kIdQK, k > 0 ? 1u : 0u);
-    }
-    tc::commit(&sbar);
-    return true;
-  };
-  auto issue_pv = [&](int jt) -> bool {
-    if (!mbar_wait(&vfull[jt & 1], (jt >> 1) & 1)) return false;
-    const uint32_t vb = smem_u32(vs + (jt & 1) * kTile), pb = smem_u32(ps);
-#pragma unroll
-    for (int k = 0; k < kPrefixKeys / 16; ++k) {
-      const uint64_t ad = tc::smem_desc_sw128(pb + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
-      // V is MN-major: 64-column d chunks kHalfBytes apart, 8-key groups 1 KiB apart
-      const uint64_t bd = tc::smem_desc_sw128(vb + k * 2048, kHalfBytes, 1024);
-      tc::mma_bf16(tO, ad, bd, kIdPV, (jt > 0 || k > 0) ? 1u : 0u);
-    }
-    tc::commit(&obar);
-    return true;
-  };
-
-  if (t == 0) {
-    mbar_arrive_expect_tx(&qbar, kTile);
-#pragma unroll
-    for (int h = 0; h < H; ++h) tma_load_3d(qs + h * kHalfBytes, &tmq, h * 64, kvh * G, mt * RPB, &qbar);
-    load_kv(&tmk, ks, &kfull[0], 0);
-    load_kv(&tmv, vs, &vfull[0], 0);
-    if (J > 1) {
-      load_kv(&tmk, ks + kTile, &kfull[1], 1);
-      load_kv(&tmv, vs + kTile, &vfull[1], 1);
-    }
-    if (!mbar_wait(&qbar, 0) || !issue_qk(0)) {
-      atomicOr(a.err, PKV_DEVERR_TIMEOUT);
-      abort_flag = 1;
-    }
-  }
-  __syncthreads();
-
-  const float c = a.qscale;
-  float m_run = -INFINITY, l_run = 0.f;
-  bool alive = abort_flag == 0;
-  for (int j = 0; j < J && alive; ++j) {
-    bool ok = mbar_wait(&sbar, j & 1);
-    tc::fence_after_sync();
-    if (t == 0 && ok) {
-      if (j + 2 < J) load_kv(&tmk, ks + (j & 1) * kTile, &kfull[j & 1], j + 2);
-      if (j + 1 < J && !issue_qk(j + 1)) ok = false;
-    }
-    // ---- scores of this row: S_j * scale * log2 e, keys past the split masked
-    float s[kPrefixKeys];
-#pragma unroll
-    for (int c0 = 0; c0 < kPrefixKeys; c0 += 32) {
-      uint32_t r[32];
-      tc::tmem_ld32(tmem + (j & 1) * 128 + lane_base + c0, r);
-      tc::wait_ld();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) s[c0 + i] = __uint_as_float(r[i]) * c;
-    }
-    const int kvalid = nkeys - j * kPrefixKeys;
-    float mx = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kPrefixKeys; ++i) {
-      if (i >= kvalid) s[i] = -INFINITY;
-      mx = fmaxf(mx, s[i]);
-    }
-    const float m_new = fmaxf(m_run, mx);
-    const bool need = m_new > m_run + 8.0f;
-    const float alpha = need ? exp2f(m_run - m_new) : 1.f;
-    if (j > 0) {
-      // PV_{j-1} done: O is current, P and V stage (j+1)&1 are free
-      if (!mbar_wait(&obar, (j - 1) & 1)) ok = false;
-      tc::fence_after_sync();
-      if (t == 0 && ok && j + 1 < J) load_kv(&tmv, vs + ((j + 1) & 1) * kTile, &vfull[(j + 1) & 1], j + 1);
-      if (__any_sync(0xffffffffu, need)) {
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t r[32];
-          tc::tmem_ld32(tO + lane_base + c0, r);
-          tc::wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-          tc::tmem_st32(tO + lane_base + c0, r);
+    for (int jt = 0; jt < J; ++jt) {
+      const int st = jt & 1;
+      int ok = 1;
+      if (lane == 0 && jt >= 2 && !mbar_wait(&freeb[st], ((jt - 2) >> 1) & 1)) {
+        atomicOr(a.err, PKV_DEVERR_TIMEOUT);
+        ok = 0;
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      if (lane == 0) mbar_arrive_expect_tx(&fullb[st], kTile);
+      __syncwarp();
+      for (int bi = lane; bi < nbox; bi += 32) {
+        const int b = bi / H, h = bi % H;
+        const int key = key0 + jt * kPrefixKeys + b * PB;
+        int blk = (int)a.num_blocks, row = 0;  // out of range: zero fill
+        if (key < key0 + nkeys && ids[key / P - id0] >= 0) {
+          blk = ids[key / P - id0];
+          row = key % P;
         }
-        tc::wait_st();
+        tma_load_4d(base + st * kTile + h * kHalfBytes + b * PB * 128, map, h * 64, kvh, row,
+                    blk, &fullb[st]);
       }
     }
-    if (need) m_run = m_new;
-    l_run *= alpha;
-    // ---- P = exp2(s - m) in bf16, swizzled K-major rows for the PV MMA
-    float lsum = 0.f;
+  } else if (warp == 4) {
+    // ============================================================ MMA issue
+    if (lane == 0) {
+      auto issue_qk = [&](int jt) -> bool {
+        if (!mbar_wait(&kfull[jt & 1], (jt >> 1) & 1)) return false;
+        tc::fence_after_sync();
+        const uint32_t kb = smem_u32(ks + (jt & 1) * kTile), qb = smem_u32(qs);
 #pragma unroll
-    for (int ch = 0; ch < kPrefixKeys / 8; ++ch) {
-      uint32_t w[4];
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
+          tc::mma_bf16(tmem + (jt & 1) * 128, tc::smem_desc_sw128(qb + off, 16, 1024),
+                       tc::smem_desc_sw128(kb + off, 16, 1024), kIdQK, k > 0 ? 1u : 0u);
+        }
+        tc::commit(&sfull[jt & 1]);
+        tc::commit(&kfree[jt & 1]);
+        return true;
+      };
+      auto issue_pv = [&](int jt) -> bool {
+        if (!mbar_wait(&vfull[jt & 1], (jt >> 1) & 1)) return false;
+        tc::fence_after_sync();
+        const uint32_t vb = smem_u32(vs + (jt & 1) * kTile), pb = smem_u32(ps);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float p0 = exp2f(s[ch * 8 + 2 * i] - m_run);
-        const float p1 = exp2f(s[ch * 8 + 2 * i + 1] - m_run);
-        lsum += p0 + p1;
-        __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-        w[i] = *reinterpret_cast<uint32_t*>(&b2);
+        for (int k = 0; k < kPrefixKeys / 16; ++k) {
+          const uint64_t ad =
+              tc::smem_desc_sw128(pb + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
+          // V is MN-major: 64-column d chunks kHalfBytes apart, 8-key groups 1 KiB apart
+          const uint64_t bd = tc::smem_desc_sw128(vb + k * 2048, kHalfBytes, 1024);
+          tc::mma_bf16(tO, ad, bd, kIdPV, (jt > 0 || k > 0) ? 1u : 0u);
+        }
+        tc::commit(&ofull);
+        tc::commit(&vfree[jt & 1]);
+        return true;
+      };
+      bool ok = mbar_wait(&qbar, 0) && issue_qk(0) && (J < 2 || issue_qk(1));
+      for (int j = 0; j < J && ok; ++j) {
+        // softmax j has read S_j and written P_j
+        if (!mbar_wait(&pfull, j & 1)) { ok = false; break; }
+        tc::fence_after_sync();
+        if (!issue_pv(j)) { ok = false; break; }
+        if (j + 2 < J && !issue_qk(j + 2)) { ok = false; break; }
       }
-      const int half = ch >> 3, cc = ch & 7;
-      uint4* dst = reinterpret_cast<uint4*>(ps + half * kHalfBytes + t * 128 + ((cc ^ (t & 7)) << 4));
-      *dst = make_uint4(w[0], w[1], w[2], w[3]);
+      if (!ok) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
     }
-    l_run += lsum;
-    tc::fence_proxy_async_smem();
-    tc::fence_before_sync();
-    alive = __syncthreads_and(ok ? 1 : 0) != 0;
-    if (t == 0 && alive) {
+  } else {
+    // ============================================================ softmax rows
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float c = a.qscale;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < J && ok; ++j) {
+      if (!mbar_wait(&sfull[j & 1], (j >> 1) & 1)) { ok = false; break; }
       tc::fence_after_sync();
-      if (!issue_pv(j)) alive = false;
-    }
-    if (!alive && t == 0) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
-    alive = __syncthreads_and(alive ? 1 : 0) != 0;
-  }
-
-  // ---- epilogue: O / l and the base-2 LSE of this row
-  const bool done = __syncthreads_and((alive && mbar_wait(&obar, (J - 1) & 1)) ? 1 : 0) != 0;
-  tc::fence_after_sync();
-  const int r = mt * RPB + t / G;
-  const int g = t % G;
-  const bool row_ok = done && r < a.num_seqs;
-  if (!done && t == 0) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
-  const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-  const int64_t slot = ((int64_t)r * a.num_q_heads + (int64_t)kvh * G + g) * a.parts_stride + split;
-  if (done) {
-#pragma unroll 1
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t v[32];
-      tc::tmem_ld32(tO + lane_base + c0, v);
-      tc::wait_ld();
-      if (row_ok) {
-        float4* dst = reinterpret_cast<float4*>(a.part_o + slot * D + c0);
+      uint32_t r[kPrefixKeys];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          dst[i] = make_float4(__uint_as_float(v[4 * i]) * inv, __uint_as_float(v[4 * i + 1]) * inv,
-                               __uint_as_float(v[4 * i + 2]) * inv,
-                               __uint_as_float(v[4 * i + 3]) * inv);
+      for (int c0 = 0; c0 < kPrefixKeys; c0 += 32)
+        tc::tmem_ld32(tmem + (j & 1) * 128 + lane_base + c0,
+                      *reinterpret_cast<uint32_t(*)[32]>(r + c0));
+      tc::wait_ld();
+      const int kvalid = nkeys - j * kPrefixKeys;
+      float s[kPrefixKeys];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kPrefixKeys; ++i) {
+        s[i] = i < kvalid ? __uint_as_float(r[i]) * c : -INFINITY;
+        mx = fmaxf(mx, s[i]);
+      }
+      const float m_new = fmaxf(m_run, mx);
+      const bool need = m_new > m_run + 8.0f;
+      const float alpha = need ? exp2f(m_run - m_new) : 1.f;
+      if (j > 0) {
+        // PV_{j-1} has completed: O is current and the P buffer is free
+        if (!mbar_wait(&ofull, (j - 1) & 1)) { ok = false; break; }
+        tc::fence_after_sync();
+        if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tc::tmem_ld32(tO + lane_base + c0, o);
+            tc::wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tc::tmem_st32(tO + lane_base + c0, o);
+          }
+          tc::wait_st();
+        }
+      }
+      if (need) m_run = m_new;
+      l_run *= alpha;
+      // ---- P = exp2(s - m) in bf16, swizzled K-major rows for the PV MMA
+      float lsum = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < kPrefixKeys / 8; ++ch) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float p0 = exp2f(s[ch * 8 + 2 * i] - m_run);
+          const float p1 = exp2f(s[ch * 8 + 2 * i + 1] - m_run);
+          lsum += p0 + p1;
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+          w[i] = *reinterpret_cast<uint32_t*>(&b2);
+        }
+        const int hf = ch >> 3, cc = ch & 7;
+        uint4* dst =
+            reinterpret_cast<uint4*>(ps + hf * kHalfBytes + t * 128 + ((cc ^ (t & 7)) << 4));
+        *dst = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      l_run += lsum;
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pfull);
+    }
+    // ---- epilogue: O / l and the LSE of this row
+    const bool done = ok && mbar_wait(&ofull, (J - 1) & 1);
+    tc::fence_after_sync();
+    if (!done && lane == 0) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
+    const int r = mt * RPB + t / G;
+    const int g = t % G;
+    const bool row_ok = done && r < a.num_seqs;
+    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+    const int64_t slot =
+        ((int64_t)r * a.num_q_heads + (int64_t)kvh * G + g) * a.parts_stride + split;
+    if (__all_sync(0xffffffffu, done)) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t v[32];
+        tc::tmem_ld32(tO + lane_base + c0, v);
+        tc::wait_ld();
+        if (row_ok) {
+          float4* dst = reinterpret_cast<float4*>(a.part_o + slot * D + c0);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(v[4 * i]) * inv,
+                                 __uint_as_float(v[4 * i + 1]) * inv,
+                                 __uint_as_float(v[4 * i + 2]) * inv,
+                                 __uint_as_float(v[4 * i + 3]) * inv);
+        }
       }
     }
+    if (row_ok) a.part_lse[slot] = l_run > 0.f ? (m_run + log2f(l_run)) * a.lse_scale : -INFINITY;
   }
-  if (row_ok) a.part_lse[slot] = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, 512);
@@ -290,7 +319,7 @@ static cudaError_t launch_prefix_t(int num_splits, const CUtensorMap& tmq, const
   if (e != cudaSuccess) return e;
   const int m_tiles = (a.num_seqs * G + kPrefixRows - 1) / kPrefixRows;
   dim3 grid((unsigned)num_splits, (unsigned)m_tiles, (unsigned)a.num_kv_heads);
-  kern<<<grid, 128, smem, stream>>>(tmq, tmk, tmv, a);
+  kern<<<grid, 224, smem, stream>>>(tmq, tmk, tmv, a);
   return cudaGetLastError();
 }
 

@@ -151,6 +151,14 @@ pkv_status encode_cache_map_sw128(CUtensorMap* map, const pkv_cache_desc* c, con
   return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_UNSUPPORTED;
 }
 
+// Prefix K/V maps: one box is one block (or 128 rows of a larger one).
+pkv_status encode_prefix_maps(CUtensorMap* tmk, CUtensorMap* tmv, const pkv_cache_desc* c,
+                              const void* k_cache, const void* v_cache) {
+  const int rows = c->block_size < pkv::kPrefixKeys ? c->block_size : pkv::kPrefixKeys;
+  pkv_status st = encode_cache_map_sw128(tmk, c, k_cache, rows);
+  return st != PKV_OK ? st : encode_cache_map_sw128(tmv, c, v_cache, rows);
+}
+
 // Keys per prefix split: whole 128-key tiles, spread so that (split x query
 // tile x kv head) CTAs cover the SMs about once.
 int32_t prefix_split_len(const pkv_cache_desc* c, int32_t num_seqs, int32_t num_q_heads,
@@ -389,13 +397,10 @@ pkv_status pkv_shared_prefix_attention(
   cudaStream_t s = as_stream(stream);
 
   if (prefix_parts > 0) {
-    CUtensorMap tmq, tmk, tmv;
+    CUtensorMap tmq;
     if ((st = encode_q_map_sw128(&tmq, q, num_seqs, num_q_heads, cache->head_dim, G,
                                  pkv::kPrefixRows / G)) != PKV_OK)
       return st;
-    const int rows = pkv::prefix_box_rows(cache->block_size);
-    if ((st = encode_cache_map_sw128(&tmk, cache, k_cache, rows)) != PKV_OK) return st;
-    if ((st = encode_cache_map_sw128(&tmv, cache, v_cache, rows)) != PKV_OK) return st;
     pkv::PrefixArgs pa{};
     pa.prefix_block_ids = prefix_block_ids;
     pa.part_o = part_o;
@@ -410,7 +415,10 @@ pkv_status pkv_shared_prefix_attention(
     pa.split_len = split_len;
     pa.parts_stride = (int32_t)parts;
     pa.qscale = qscale;
-    if (pkv::launch_prefix_attention(cache->head_dim, G, prefix_parts, tmq, tmk, tmv, pa, s) !=
+    pa.lse_scale = 1.f;
+    CUtensorMap ptk, ptv;
+    if ((st = encode_prefix_maps(&ptk, &ptv, cache, k_cache, v_cache)) != PKV_OK) return st;
+    if (pkv::launch_prefix_attention(cache->head_dim, G, prefix_parts, tmq, ptk, ptv, pa, s) !=
         cudaSuccess)
       return PKV_ERR_CUDA;
   }
@@ -442,6 +450,64 @@ pkv_status pkv_shared_prefix_attention(
   a.qscale = qscale;
   a.direct = 0;
   cudaError_t e = pkv::launch_paged_decode(cache->dtype, cache->head_dim, G, tmk, tmv, a, s);
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int32_t pkv_prefix_split_len(const pkv_cache_desc* cache, int32_t num_seqs, int32_t num_q_heads,
+                             int32_t prefix_len) {
+  if (check_cache(cache) != PKV_OK || num_seqs <= 0 || prefix_len <= 0 ||
+      check_prefix_shape(cache, num_q_heads, prefix_len) != PKV_OK)
+    return 0;
+  return prefix_split_len(cache, num_seqs, num_q_heads, prefix_len);
+}
+
+pkv_status pkv_prefix_attention_states(const pkv_cache_desc* cache, float* states_o,
+                                       float* states_lse, const void* q, const void* k_cache,
+                                       const void* v_cache, const int32_t* prefix_block_ids,
+                                       int32_t prefix_len, int32_t split_len, int32_t num_seqs,
+                                       int32_t num_q_heads, float scale, void* stream) {
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || prefix_len <= 0 || split_len <= 0 || split_len % pkv::kPrefixKeys != 0 ||
+      !isfinite(scale))
+    return PKV_ERR_INVALID_ARG;
+  if ((st = check_prefix_shape(cache, num_q_heads, prefix_len)) != PKV_OK) return st;
+  if (num_seqs == 0) return PKV_OK;
+  if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
+  if (!states_o || !states_lse || !q || !k_cache || !v_cache || !prefix_block_ids)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned16(states_o) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_INVALID_ARG;
+  const int64_t splits = ((int64_t)prefix_len + split_len - 1) / split_len;
+  if (splits > 65535) return PKV_ERR_UNSUPPORTED;
+  if (pkv::prefix_smem_bytes(cache->head_dim, split_len, cache->block_size) > 227 * 1024)
+    return PKV_ERR_UNSUPPORTED;
+  const int G = num_q_heads / cache->num_kv_heads;
+  unsigned int* err = device_error_word();
+  if (!err) return PKV_ERR_CUDA;
+  CUtensorMap tmq;
+  if ((st = encode_q_map_sw128(&tmq, q, num_seqs, num_q_heads, cache->head_dim, G,
+                               pkv::kPrefixRows / G)) != PKV_OK)
+    return st;
+  pkv::PrefixArgs pa{};
+  pa.prefix_block_ids = prefix_block_ids;
+  pa.part_o = states_o;
+  pa.part_lse = states_lse;
+  pa.err = err;
+  pa.num_blocks = cache->num_blocks;
+  pa.num_seqs = num_seqs;
+  pa.num_q_heads = num_q_heads;
+  pa.num_kv_heads = cache->num_kv_heads;
+  pa.block_size = cache->block_size;
+  pa.prefix_len = prefix_len;
+  pa.split_len = split_len;
+  pa.parts_stride = (int32_t)splits;
+  pa.qscale = scale * 1.4426950408889634f;
+  pa.lse_scale = 0.6931471805599453f;
+  CUtensorMap ptk, ptv;
+  if ((st = encode_prefix_maps(&ptk, &ptv, cache, k_cache, v_cache)) != PKV_OK) return st;
+  cudaError_t e = pkv::launch_prefix_attention(cache->head_dim, G, (int)splits, tmq, ptk, ptv, pa,
+                                               as_stream(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

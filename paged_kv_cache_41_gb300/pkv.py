@@ -30,6 +30,8 @@ EXPORTED = [
     "pkv_paged_attention_decode_static",
     "pkv_shared_prefix_workspace_bytes",
     "pkv_shared_prefix_attention",
+    "pkv_prefix_split_len",
+    "pkv_prefix_attention_states",
     "pkv_get_device_error",
     "pkv_status_string",
 ]
@@ -79,6 +81,11 @@ def load_library():
     lib.pkv_shared_prefix_attention.restype = ctypes.c_int
     lib.pkv_shared_prefix_attention.argtypes = [dp, vp, vp, vp, vp, vp, vp, i32, vp, i32, vp, i32,
                                                 i32, f32, i32, vp, ctypes.c_size_t, vp]
+    lib.pkv_prefix_split_len.restype = i32
+    lib.pkv_prefix_split_len.argtypes = [dp, i32, i32, i32]
+    lib.pkv_prefix_attention_states.restype = ctypes.c_int
+    lib.pkv_prefix_attention_states.argtypes = [dp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32,
+                                                vp]
     lib.pkv_get_device_error.restype = ctypes.c_int
     lib.pkv_get_device_error.argtypes = [ctypes.POINTER(i32), vp]
     lib.pkv_status_string.restype = ctypes.c_char_p
@@ -223,6 +230,33 @@ def shared_prefix_attention(q, k_cache, v_cache, prefix_block_ids, prefix_len,
         _ptr(suffix_lens), b, hq, float(scale), partition_size, _ptr(workspace), ws_bytes,
         _stream(stream)), "pkv_shared_prefix_attention")
     return out
+
+
+def prefix_split_len(k_cache, num_seqs, num_q_heads, prefix_len) -> int:
+    desc = cache_desc(k_cache)
+    return load_library().pkv_prefix_split_len(ctypes.byref(desc), num_seqs, num_q_heads,
+                                               prefix_len)
+
+
+def prefix_attention_states(q, k_cache, v_cache, prefix_block_ids, prefix_len, scale, *,
+                            split_len=0, states_o=None, states_lse=None, stream=None):
+    """Per-split (O, LSE) states of every query row against the shared prefix
+    (include/pkv.h).  Returns (states_o [B, Hq, n, D] fp32, states_lse
+    [B, Hq, n] fp32 natural log, split_len)."""
+    desc = cache_desc(k_cache)
+    b, hq, d = q.shape
+    if split_len == 0:
+        split_len = prefix_split_len(k_cache, b, hq, prefix_len)
+    n = (prefix_len + split_len - 1) // split_len if split_len else 0
+    if states_o is None:
+        states_o = torch.empty(b, hq, n, d, dtype=torch.float32, device=q.device)
+    if states_lse is None:
+        states_lse = torch.empty(b, hq, n, dtype=torch.float32, device=q.device)
+    _check(load_library().pkv_prefix_attention_states(
+        ctypes.byref(desc), _ptr(states_o), _ptr(states_lse), _ptr(q), _ptr(k_cache),
+        _ptr(v_cache), _ptr(prefix_block_ids), int(prefix_len), int(split_len), b, hq, float(scale),
+        _stream(stream)), "pkv_prefix_attention_states")
+    return states_o, states_lse, split_len
 
 
 def get_device_error(stream=None) -> int:

@@ -237,6 +237,8 @@ def _shared_prefix_run(sp, rows=None, suffix_lens=None, partition_size=0):
 
 @pytest.mark.parametrize("batch,prefix,hq,hkv,d", [
     (16, 256, 32, 8, 128), (5, 384, 8, 2, 128), (40, 128, 16, 16, 64), (3, 512, 16, 2, 128),
+    # 2, 3 (padded to 4) and 5 (padded to 8) query tiles: clusters of 2 and 4 CTAs
+    (50, 256, 32, 8, 128), (80, 384, 32, 8, 128), (150, 256, 32, 8, 64),
 ])
 def test_shared_prefix_small(batch, prefix, hq, hkv, d):
     sp = wl.shared_prefix_batch(device="cuda", batch=batch, prefix_len=prefix, shared_tail=8,
@@ -256,3 +258,35 @@ def test_shared_prefix_full_size_sampled():
     sp = wl.shared_prefix_batch(device="cuda")  # 128 requests, 2048-token prefix
     rows = np.array([0, 1, 31, 32, 63, 64, 100, 127])
     _shared_prefix_run(sp, rows=rows)
+
+
+@pytest.mark.parametrize("split_len", [0, 128, 384])
+def test_prefix_states_per_split(split_len):
+    """Each split's state equals the oracle's attention over that split's keys."""
+    sp = wl.shared_prefix_batch(device="cuda", batch=20, prefix_len=768, shared_tail=0,
+                                suffix_lo=1, suffix_hi=20, seed=95)
+    shape = (sp.num_blocks, sp.block_size, sp.num_kv_heads, sp.head_dim)
+    kc = torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    pkv.kv_append(kc, vc, sp.parent_k, sp.parent_v, torch.from_numpy(sp.parent_slots).cuda())
+    so, sl, split = pkv.prefix_attention_states(
+        sp.q, kc, vc, torch.from_numpy(sp.prefix_block_ids).cuda(), sp.prefix_len, sp.scale,
+        split_len=split_len)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0 and split % 128 == 0
+    hk = np.full(shape, 0x7FC0, np.uint16)
+    hv = np.full(shape, 0x7FC0, np.uint16)
+    ps = np.array([oracle.slot_for_position(sp.parent_table, sp.block_size, t)
+                   for t in range(sp.prefix_len)], np.int64)
+    oracle.kv_append(hk, hv, wl.to_numpy_storage(sp.parent_k)[:sp.prefix_len].copy(),
+                     wl.to_numpy_storage(sp.parent_v)[:sp.prefix_len].copy(), ps)
+    q = wl.to_numpy_storage(sp.q)
+    n = -(-sp.prefix_len // split)
+    for s in range(n):
+        lo, hi = s * split, min((s + 1) * split, sp.prefix_len)
+        ids = sp.prefix_block_ids[lo // sp.block_size: hi // sp.block_size]
+        tables = np.tile(ids, (sp.num_seqs, 1)).astype(np.int32)
+        lens = np.full(sp.num_seqs, hi - lo, np.int32)
+        ref, ref_lse = oracle.paged_decode(q, hk, hv, tables, lens, sp.scale, nthreads=pu.NTHREADS)
+        pu.assert_close(so[:, :, s].cpu().numpy(), ref, f"split {s} O")
+        pu.assert_close(sl[:, :, s].cpu().numpy(), ref_lse, f"split {s} LSE")
