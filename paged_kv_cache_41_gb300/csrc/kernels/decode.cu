@@ -466,7 +466,8 @@ static cudaError_t launch_partial(const CUtensorMap& tmk, const CUtensorMap& tmv
                                   const DecodeArgs& a, cudaStream_t stream) {
   const size_t smem = decode_smem_bytes(a.block_size, D, (int)sizeof(T), G, a.num_stages);
   auto kern = decode_partial_kernel<T, D, G>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static SmemAttrCache attr_cache;
+  cudaError_t e = ensure_smem_limit(kern, (int)smem, attr_cache);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)a.num_kv_heads, (unsigned)a.max_parts, (unsigned)a.num_seqs);
   kern<<<grid, kDecodeThreads, smem, stream>>>(tmk, tmv, a);

@@ -5,7 +5,28 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace pkv {
+
+// Raise a kernel's dynamic shared-memory limit once per device: the attribute
+// persists, so later launches that need no more skip the driver call.
+struct SmemAttrCache {
+  std::mutex mu;
+  int set[64] = {};
+};
+
+template <typename Kernel>
+cudaError_t ensure_smem_limit(Kernel kern, int smem, SmemAttrCache& cache) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(cache.mu);
+  if (dev >= 0 && dev < 64 && cache.set[dev] >= smem) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) cache.set[dev] = smem;
+  return e;
+}
 
 cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k, const void* v,
                              const int64_t* slots, int64_t num_tokens, int64_t num_slots,

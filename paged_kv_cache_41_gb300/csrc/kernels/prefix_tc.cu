@@ -49,7 +49,7 @@ __host__ __device__ constexpr int prefix_tile_bytes(int head_dim) {
 
 size_t prefix_smem_bytes(int head_dim, int split_len, int block_size) {
   const size_t tiles = (size_t)5 * prefix_tile_bytes(head_dim) + 2 * kHalfBytes;  // Q, K[2], V[2], P
-  const size_t ids = ((size_t)split_len / block_size + 2) * sizeof(int);
+  const size_t ids = 2 * ((size_t)split_len / block_size + 2) * sizeof(int);
   return tiles + ((ids + 15) & ~(size_t)15) + 1024;  // +1024: base alignment
 }
 
@@ -80,7 +80,8 @@ __global__ void __launch_bounds__(224, 1)
   unsigned char* ks = qs + kTile;          // two stages
   unsigned char* vs = ks + 2 * kTile;      // two stages
   unsigned char* ps = vs + 2 * kTile;      // 128 rows x 128 keys bf16 (two halves)
-  int* ids = reinterpret_cast<int*>(ps + 2 * kHalfBytes);
+  const int nid_cap = a.split_len / P + 2;  // block ids of a split, per producer copy
+  int* ids_all = reinterpret_cast<int*>(ps + 2 * kHalfBytes);
   // qbar: Q by TMA; kfull/vfull: a producer warp filled a stage; kfree/vfree:
   // the MMA that read a stage completed; sfull[b]: QK^T into S buffer b done;
   // pfull: the four softmax warps wrote P; ofull: PV done.
@@ -100,16 +101,14 @@ __global__ void __launch_bounds__(224, 1)
     mbar_init(&pfull, 4);
     mbar_init(&ofull, 1);
     fence_barrier_init();
+    // Q needs no block ids: start it before anything else
+    prefetch_tensormap(&tmq);
+    mbar_arrive_expect_tx(&qbar, kTile);
+#pragma unroll
+    for (int h = 0; h < H; ++h)
+      tma_load_3d(qs + h * kHalfBytes, &tmq, h * 64, kvh * G, mt * RPB, &qbar);
   }
   if (warp == 0) tc::tmem_alloc(&tmem_base, 512);
-  for (int i = t; i < nid; i += blockDim.x) {
-    int b = __ldg(a.prefix_block_ids + id0 + i);
-    if (b < 0 || (int64_t)b >= a.num_blocks) {
-      atomicOr(a.err, PKV_DEVERR_BLOCK);
-      b = -1;  // rows of a bad block are zero-filled
-    }
-    ids[i] = b;
-  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -125,22 +124,23 @@ __global__ void __launch_bounds__(224, 1)
     // it has completed; keys past the split read a zero-filled out-of-range
     // box.
     const bool is_k = warp == 5;
+    int* ids = ids_all + (is_k ? 0 : nid_cap);  // each producer gathers its own copy
+    for (int i = lane; i < nid; i += 32) {
+      int b = __ldg(a.prefix_block_ids + id0 + i);
+      if (b < 0 || (int64_t)b >= a.num_blocks) {
+        if (is_k) atomicOr(a.err, PKV_DEVERR_BLOCK);
+        b = -1;  // rows of a bad block are zero-filled
+      }
+      ids[i] = b;
+    }
+    __syncwarp();
     const CUtensorMap* map = is_k ? &tmk : &tmv;
     unsigned char* base = is_k ? ks : vs;
     uint64_t* fullb = is_k ? kfull : vfull;
     uint64_t* freeb = is_k ? kfree : vfree;
     const int PB = P < kPrefixKeys ? P : kPrefixKeys;
     const int nbox = (kPrefixKeys / PB) * H;
-    if (lane == 0) {
-      prefetch_tensormap(map);
-      if (is_k) {
-        prefetch_tensormap(&tmq);
-        mbar_arrive_expect_tx(&qbar, kTile);
-#pragma unroll
-        for (int h = 0; h < H; ++h)
-          tma_load_3d(qs + h * kHalfBytes, &tmq, h * 64, kvh * G, mt * RPB, &qbar);
-      }
-    }
+    if (lane == 0) prefetch_tensormap(map);
     for (int jt = 0; jt < J; ++jt) {
       const int st = jt & 1;
       int ok = 1;
@@ -286,19 +286,31 @@ __global__ void __launch_bounds__(224, 1)
     const int64_t slot =
         ((int64_t)r * a.num_q_heads + (int64_t)kvh * G + g) * a.parts_stride + split;
     if (__all_sync(0xffffffffu, done)) {
-#pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t v[32];
-        tc::tmem_ld32(tO + lane_base + c0, v);
-        tc::wait_ld();
-        if (row_ok) {
-          float4* dst = reinterpret_cast<float4*>(a.part_o + slot * D + c0);
+      // O row -> registers (one wait), scaled; then through the free K stages
+      // (128 rows x D floats, 16-byte chunk i of row t at chunk i ^ (t % 32))
+      // so each warp stores whole 4*D-byte rows, one per instruction.
+      uint32_t v[D];
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(__uint_as_float(v[4 * i]) * inv,
-                                 __uint_as_float(v[4 * i + 1]) * inv,
-                                 __uint_as_float(v[4 * i + 2]) * inv,
-                                 __uint_as_float(v[4 * i + 3]) * inv);
+      for (int c0 = 0; c0 < D; c0 += 32)
+        tc::tmem_ld32(tO + lane_base + c0, *reinterpret_cast<uint32_t(*)[32]>(v + c0));
+      tc::wait_ld();
+      float4* stage = reinterpret_cast<float4*>(ks);  // K stages are idle: every QK^T completed
+      constexpr int kChunks = D / 4;
+#pragma unroll
+      for (int i = 0; i < kChunks; ++i)
+        stage[t * kChunks + (i ^ (t & (kChunks - 1)))] =
+            make_float4(__uint_as_float(v[4 * i]) * inv, __uint_as_float(v[4 * i + 1]) * inv,
+                        __uint_as_float(v[4 * i + 2]) * inv, __uint_as_float(v[4 * i + 3]) * inv);
+      __syncwarp();
+      for (int rr = 0; rr < 32; ++rr) {
+        const int row = warp * 32 + rr;
+        const int r2 = mt * RPB + row / G;
+        if (r2 < a.num_seqs) {
+          const int64_t slot2 =
+              ((int64_t)r2 * a.num_q_heads + (int64_t)kvh * G + row % G) * a.parts_stride + split;
+          for (int i = lane; i < kChunks; i += 32)
+            reinterpret_cast<float4*>(a.part_o + slot2 * D)[i] =
+                stage[row * kChunks + (i ^ (row & (kChunks - 1)))];
         }
       }
     }
@@ -315,7 +327,8 @@ static cudaError_t launch_prefix_t(int num_splits, const CUtensorMap& tmq, const
                                    cudaStream_t stream) {
   const size_t smem = prefix_smem_bytes(D, a.split_len, a.block_size);
   auto kern = prefix_attention_kernel<D, G>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static SmemAttrCache attr_cache;
+  cudaError_t e = ensure_smem_limit(kern, (int)smem, attr_cache);
   if (e != cudaSuccess) return e;
   const int m_tiles = (a.num_seqs * G + kPrefixRows - 1) / kPrefixRows;
   dim3 grid((unsigned)num_splits, (unsigned)m_tiles, (unsigned)a.num_kv_heads);

@@ -5,6 +5,8 @@
 #include <cudaTypedefs.h>
 
 #include <math.h>
+#include <string.h>
+
 #include <mutex>
 
 #include "kernels/launch.h"
@@ -46,6 +48,64 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return g_encode;
 }
 
+// Encoded tensor maps are pure functions of their arguments, so recently used
+// ones are kept (a few hundred bytes each) and reused without re-encoding.
+struct MapKey {
+  CUtensorMapDataType dtype;
+  cuuint32_t rank;
+  void* base;
+  cuuint64_t dims[5], strides[4];
+  cuuint32_t box[5];
+  CUtensorMapSwizzle swizzle;
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+  bool used;
+};
+constexpr int kMapCacheSize = 64;
+MapEntry g_maps[kMapCacheSize];
+int g_map_next = 0;
+std::mutex g_map_mu;
+
+CUresult encode_tiled_cached(CUtensorMap* map, CUtensorMapDataType dtype, cuuint32_t rank,
+                             void* base, const cuuint64_t* dims, const cuuint64_t* strides,
+                             const cuuint32_t* box, CUtensorMapSwizzle swizzle) {
+  MapKey k;
+  memset(&k, 0, sizeof(k));
+  k.dtype = dtype;
+  k.rank = rank;
+  k.base = base;
+  for (cuuint32_t i = 0; i < rank; ++i) {
+    k.dims[i] = dims[i];
+    k.box[i] = box[i];
+    if (i + 1 < rank) k.strides[i] = strides[i];
+  }
+  k.swizzle = swizzle;
+  {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (int i = 0; i < kMapCacheSize; ++i)
+      if (g_maps[i].used && memcmp(&g_maps[i].key, &k, sizeof(k)) == 0) {
+        *map = g_maps[i].map;
+        return CUDA_SUCCESS;
+      }
+  }
+  auto enc = tensor_map_encoder();
+  if (!enc) return CUDA_ERROR_NOT_INITIALIZED;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = enc(map, dtype, rank, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r == CUDA_SUCCESS) {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    MapEntry& e = g_maps[g_map_next];
+    g_map_next = (g_map_next + 1) % kMapCacheSize;
+    e.key = k;
+    e.map = *map;
+    e.used = true;
+  }
+  return r;
+}
+
 int elem_bytes(int dtype) { return dtype == PKV_BF16 ? 2 : 4; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -77,19 +137,16 @@ pkv_status check_attention_shape(const pkv_cache_desc* c, int32_t num_q_heads) {
 // token rows x head_dim.
 pkv_status encode_cache_map(CUtensorMap* map, const pkv_cache_desc* c, const void* base,
                             int rows) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return PKV_ERR_CUDA;
   const cuuint64_t es = (cuuint64_t)elem_bytes(c->dtype);
   cuuint64_t dims[4] = {(cuuint64_t)c->head_dim, (cuuint64_t)c->num_kv_heads,
                         (cuuint64_t)c->block_size, (cuuint64_t)c->num_blocks};
   cuuint64_t strides[3] = {dims[0] * es, dims[0] * dims[1] * es, dims[0] * dims[1] * dims[2] * es};
   cuuint32_t box[4] = {(cuuint32_t)c->head_dim, 1, (cuuint32_t)rows, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = enc(map, c->dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                   4, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = encode_tiled_cached(map, c->dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                                   4, const_cast<void*>(base), dims, strides, box,
+                                   CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (r == CUDA_ERROR_NOT_INITIALIZED) return PKV_ERR_CUDA;
   return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_UNSUPPORTED;
 }
 
@@ -122,15 +179,12 @@ int32_t auto_partition(const pkv_cache_desc* c, int32_t num_seqs, int32_t max_bl
 // G heads x rpb requests.
 pkv_status encode_q_map_sw128(CUtensorMap* map, const void* q, int32_t num_seqs, int32_t num_q_heads,
                               int32_t head_dim, int group, int rpb) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return PKV_ERR_CUDA;
   cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_q_heads, (cuuint64_t)num_seqs};
   cuuint64_t strides[2] = {dims[0] * 2, dims[0] * dims[1] * 2};
   cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)rpb};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = encode_tiled_cached(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q),
+                                   dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (r == CUDA_ERROR_NOT_INITIALIZED) return PKV_ERR_CUDA;
   return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_UNSUPPORTED;
 }
 
@@ -138,16 +192,13 @@ pkv_status encode_q_map_sw128(CUtensorMap* map, const void* q, int32_t num_seqs,
 // `rows` token rows x 1 block.
 pkv_status encode_cache_map_sw128(CUtensorMap* map, const pkv_cache_desc* c, const void* base,
                                   int rows) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return PKV_ERR_CUDA;
   cuuint64_t dims[4] = {(cuuint64_t)c->head_dim, (cuuint64_t)c->num_kv_heads,
                         (cuuint64_t)c->block_size, (cuuint64_t)c->num_blocks};
   cuuint64_t strides[3] = {dims[0] * 2, dims[0] * dims[1] * 2, dims[0] * dims[1] * dims[2] * 2};
   cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
-                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = encode_tiled_cached(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base),
+                                   dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (r == CUDA_ERROR_NOT_INITIALIZED) return PKV_ERR_CUDA;
   return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_UNSUPPORTED;
 }
 
