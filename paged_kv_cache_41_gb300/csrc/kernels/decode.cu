@@ -207,8 +207,9 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
   const DecodeSmem L = decode_smem_layout(P, D, (int)sizeof(T), G, a.num_stages);
   const int NS = a.num_stages;
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem =
-      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  // Align by offsetting the array itself (not through an integer), so the
+  // compiler keeps every tile and scratch access in the shared state space.
+  unsigned char* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
   T* ktile = reinterpret_cast<T*>(smem);
   T* vtile = ktile + (size_t)NS * L.tile_elems;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
@@ -271,27 +272,36 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
         }
       }
     }
-    if (lane == 0) {
-      bool valid = true;
+    bool valid = true;
 #pragma unroll
-      for (int j = 0; j < kStageRows / 16; ++j)
-        if (j < nbox && (blk[j] < 0 || (int64_t)blk[j] >= a.num_blocks)) valid = false;
-      if (!valid) {
+    for (int j = 0; j < kStageRows / 16; ++j)
+      if (j < nbox && (blk[j] < 0 || (int64_t)blk[j] >= a.num_blocks)) valid = false;
+    if (!valid) {
+      if (lane == 0) {
         atomicOr(a.err, PKV_DEVERR_BLOCK);
         stage_ok[st] = 0;
         mbar_arrive(&full[st]);
-      } else {
+      }
+    } else {
+      if (lane == 0) {
         stage_ok[st] = 1;
         mbar_arrive_expect_tx(&full[st], 2u * box_bytes * (uint32_t)nbox);
-        T* kd = ktile + (size_t)st * L.tile_elems;
-        T* vd = vtile + (size_t)st * L.tile_elems;
+      }
+      __syncwarp();
+      // one box per lane: lanes 0..nbox-1 load K, lanes 16..16+nbox-1 load V
+      const int j = lane & 15;
+      if (j < nbox) {
+        int bj = blk[0], rj = brw[0];
 #pragma unroll
-        for (int j = 0; j < kStageRows / 16; ++j) {
-          if (j < nbox) {
-            tma_load_4d(kd + j * TB * D, &tmk, 0, kvh, brw[j], blk[j], &full[st]);
-            tma_load_4d(vd + j * TB * D, &tmv, 0, kvh, brw[j], blk[j], &full[st]);
+        for (int jj = 1; jj < kStageRows / 16; ++jj)
+          if (j == jj) {
+            bj = blk[jj];
+            rj = brw[jj];
           }
-        }
+        if (lane < 16)
+          tma_load_4d(ktile + (size_t)st * L.tile_elems + j * TB * D, &tmk, 0, kvh, rj, bj, &full[st]);
+        else
+          tma_load_4d(vtile + (size_t)st * L.tile_elems + j * TB * D, &tmv, 0, kvh, rj, bj, &full[st]);
       }
     }
   };

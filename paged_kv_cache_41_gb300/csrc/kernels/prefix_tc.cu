@@ -74,8 +74,9 @@ __global__ void __launch_bounds__(224, 1)
   const int nid = (key0 + nkeys - 1) / P - id0 + 1;
 
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* sm = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // Align by offsetting the array itself (not through an integer), so the
+  // compiler keeps every access in the shared state space.
+  unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   unsigned char* qs = sm;
   unsigned char* ks = qs + kTile;          // two stages
   unsigned char* vs = ks + 2 * kTile;      // two stages
