@@ -242,8 +242,7 @@ def run_pkv(args, rank, world, local):
     q = b.q.contiguous()
     out = torch.empty_like(q)
     psize = args.partition_size
-    if psize == 0:
-        psize = pkv.decode_auto_partition(kc, B, b.num_q_heads, b.max_blocks)
+    ctas = pkv.decode_num_ctas(kc, B, b.num_q_heads, b.max_blocks, psize)
     ws_bytes = pkv.decode_workspace_bytes(kc, B, b.num_q_heads, b.max_blocks, psize)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
@@ -330,7 +329,6 @@ def run_pkv(args, rank, world, local):
     peak, peak_kind = load_peaks()
     achieved = kv_bytes / (decode_ms * 1e-3) / 1e9
     traffic = kernel_traffic("decode.cu", "decode_partial_llama.md") if args.workload == "llama" else None
-    parts = math.ceil(b.max_blocks * b.block_size / psize)
     res = {
         "metric": "paged-decode KV GB/s (% of HBM peak) and decode rows/s at 1 GB300",
         "value": world * kv_bytes / (ms_step * 1e-3) / 1e9,
@@ -352,7 +350,7 @@ def run_pkv(args, rank, world, local):
             "head_dim": b.head_dim, "block_size": b.block_size,
             "seq_len_min": int(b.seq_lens.min()), "seq_len_max": int(b.seq_lens.max()),
             "total_tokens": int(b.seq_lens.sum()), "pool_blocks": b.num_blocks,
-            "partition_size": psize, "max_partitions": parts,
+            "partition_size": psize, "decode_ctas": ctas,
             "kv_bytes_per_step": kv_bytes,
             "l2": "inputs larger than L2 (K/V read per step >> 129 MB)",
             "parallelism": f"replicas x{world} (sequences shard, no collective)",
@@ -361,14 +359,15 @@ def run_pkv(args, rank, world, local):
         "pct_of_hbm_peak": 100.0 * (kv_bytes / (ms_step * 1e-3) / 1e9) / peak,
         "decode_ms": decode_ms,
         "append_ms": append_ms,
-        "roofline": {"bound": "hbm", "kernel": "decode_partial_kernel + decode_reduce_kernel",
+        "roofline": {"bound": "hbm",
+                     "kernel": "decode_plan_kernel + decode_partial_kernel + decode_reduce_kernel",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs (copy)",
                      "traffic": traffic,
                      "algorithmic_bytes_per_launch": kv_bytes},
         "e2e": {"value": world * kv_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * (2 if parts <= 1 else 3),
+        "gpu_launches": args.steps * 4,  # append, plan, partial, reduce
         "clocks": clk,
     }
     return res, b
@@ -495,7 +494,7 @@ def run_shared(args, rank, world, local):
                      "traffic": None, "algorithmic_flops_per_launch": flops},
         "e2e": {"value": world * logical / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s (logical K/V)",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": n * 4,
+        "gpu_launches": n * 5,  # prefix states; prefix, plan, partial, reduce
         "clocks": clk,
     }
     return res, sp

@@ -99,16 +99,19 @@ pkv_status pkv_kv_block_copy(const pkv_cache_desc* cache, void* k_cache,
                              int64_t num_pairs, void* stream);
 
 /* Bytes of device workspace pkv_paged_attention_decode needs for these sizes
- * (0 when one partition covers every sequence).  partition_size as below. */
+ * and partition_size (see below); 0 for unsupported or invalid sizes.  It
+ * depends on the device (its SM count), so query it with the device current. */
 size_t pkv_decode_workspace_bytes(const pkv_cache_desc* cache, int32_t num_seqs,
                                   int32_t num_q_heads,
                                   int32_t max_blocks_per_seq,
                                   int32_t partition_size);
 
-/* Partition size (tokens) the library picks when partition_size == 0. */
-int32_t pkv_decode_auto_partition(const pkv_cache_desc* cache, int32_t num_seqs,
-                                  int32_t num_q_heads,
-                                  int32_t max_blocks_per_seq);
+/* CTAs the decode's main kernel launches for these sizes and partition_size
+ * (one wave of resident CTAs for partition_size 0); 0 for unsupported or
+ * invalid sizes. */
+int32_t pkv_decode_num_ctas(const pkv_cache_desc* cache, int32_t num_seqs,
+                            int32_t num_q_heads, int32_t max_blocks_per_seq,
+                            int32_t partition_size);
 
 /* Paged attention decode (M5.3 0x0A, 0x0BA): one query row per sequence and
  * query head against the sequence's full logical history,
@@ -124,14 +127,18 @@ int32_t pkv_decode_auto_partition(const pkv_cache_desc* cache, int32_t num_seqs,
  *   block_tables:  int32 [num_seqs, max_blocks_per_seq]; entries past
  *                  ceil(seq_lens[r] / P) are never read.
  *   seq_lens:      int32 [num_seqs].
- *   partition_size: tokens per split-K partition (a multiple of block_size),
- *                  or 0 for the library's choice.  A sequence is split into
- *                  ceil(T / partition_size) partitions whose (output, LSE)
- *                  states are merged by log-sum-exp in a second kernel
- *                  (M5.3 0x0A: allocator block, kernel block and reduction
- *                  partition are three levels).
+ *   partition_size: 0, or a multiple of block_size.  The work is split into
+ *                  pieces (M5.3 0x0A: allocator block, kernel block and
+ *                  reduction partition are three levels): the token rows of
+ *                  every (sequence, kv head), in 32-row stages, are dealt out
+ *                  in equal contiguous shares to persistent CTAs -- one wave of
+ *                  them for 0 -- and a (sequence, kv head) cut between CTAs is
+ *                  merged from its pieces' (output, LSE) states by log-sum-exp
+ *                  in a second kernel.  A positive partition_size adds CTAs
+ *                  until none streams more than max(32, partition_size) rows.
  *   workspace:     device scratch of at least pkv_decode_workspace_bytes
- *                  bytes (may be NULL when that is 0), 256-byte aligned.
+ *                  bytes, 256-byte aligned.  Nothing in it needs to be
+ *                  initialised.
  * Supported: block_size 16 or a multiple of 32 up to 256; head_dim 64 or 128;
  * Hq / Hkv in {1, 2, 4, 8}; num_seqs <= 65535. */
 pkv_status pkv_paged_attention_decode(
@@ -142,7 +149,7 @@ pkv_status pkv_paged_attention_decode(
     size_t workspace_bytes, void* stream);
 
 /* Bytes of device workspace pkv_shared_prefix_attention needs for these
- * sizes.  partition_size as for the suffix decode (0 = library choice). */
+ * sizes.  partition_size as for the suffix decode. */
 size_t pkv_shared_prefix_workspace_bytes(const pkv_cache_desc* cache,
                                          int32_t num_seqs, int32_t num_q_heads,
                                          int32_t prefix_len,
@@ -215,8 +222,9 @@ pkv_status pkv_prefix_attention_states(const pkv_cache_desc* cache,
  * For callers that cannot allocate device memory themselves -- for example a
  * plugin whose host framework owns every device allocation, or a serving loop
  * that must never call cudaMalloc/cudaFree in its steady state (both can
- * synchronise the device or fail under memory pressure).  The split-K partial
- * states go to a fixed array of PKV_STATIC_SCRATCH_BYTES bytes that the library
+ * synchronise the device or fail under memory pressure).  The decode's
+ * workspace (its plan and piece states) is a fixed array of
+ * PKV_STATIC_SCRATCH_BYTES bytes that the library
  * declares in device global memory, so the caller passes no workspace and the
  * call allocates nothing.  Arguments, results and errors are those of
  * pkv_paged_attention_decode, plus:
@@ -230,8 +238,8 @@ pkv_status pkv_prefix_attention_states(const pkv_cache_desc* cache,
  *   - all calls on a device share the one array.  Calls that may run at the
  *     same time on the GPU (different streams without ordering between them)
  *     race on it and give wrong results: order them.  Nothing in the array
- *     needs to start at zero -- each call writes every partial state it reads
- *     -- so leftover contents from an earlier call do no harm. */
+ *     needs to start at zero -- each call writes every value it reads -- so
+ *     leftover contents from an earlier call do no harm. */
 pkv_status pkv_paged_attention_decode_static(
     const pkv_cache_desc* cache, void* out, float* lse, const void* q,
     const void* k_cache, const void* v_cache, const int32_t* block_tables,

@@ -3,29 +3,39 @@
 // What it computes ("M5.3 - KV Memory Layout and Exact Reuse", 0x0A and
 // 0x0BA): for sequence r and query head h, attention of q[r, h] over the
 // request-visible rows t < T_r of kv head h / G, where row t lives in physical
-// block block_tables[r, t / P] at offset t % P.  A sequence's blocks are cut
-// into partitions of `blocks_per_part` blocks; each partition keeps an online
-// softmax state (m, l, u) and emits (O_p = u / l, LSE_p = m + log l); a second
-// kernel merges the partitions of a row by log-sum-exp, never by averaging
-// normalised outputs, with empty partitions as the identity.
+// block block_tables[r, t / P] at offset t % P.  The rows of one (sequence,
+// kv head) are cut into pieces; each piece keeps an online softmax state
+// (m, l, u) and emits (O_p = u / l, LSE_p = m + log l); pieces are merged by
+// log-sum-exp, never by averaging normalised outputs, with empty pieces as
+// the identity.
 //
 // Design (GB300):
-//   * one CTA of four warps per (kv head, partition, sequence); the G query
-//     heads of a kv head share every K/V byte the CTA reads; four CTAs fit on
-//     an SM (registers and a 3 x 16 KiB shared-memory ring each);
-//   * warp 0 also issues the loads: it holds the partition's block ids 32 at a
-//     time (one coalesced load per 32 blocks, the next group in flight) and
-//     fills each 32-row stage with 4-D TMA boxes (one block, or a 32-row slice
-//     of a larger block, of one kv head) for K and V, tracked by mbarriers;
-//     a stage is refilled as soon as all four warps have released it, so no
-//     table lookup sits between two copies;
+//   * persistent, balanced CTAs: the work is the list of 32-row stages of
+//     every (sequence, kv head) segment, sequence-major; a one-CTA planning
+//     kernel scans the lengths, and CTA c of C (one wave: four per SM) streams
+//     stages [c S / C, (c + 1) S / C) of the S in the list.  Every CTA moves
+//     the same bytes whatever the length mix, there is no tail wave, and a
+//     CTA crosses segment boundaries without draining its pipeline;
+//   * a segment a CTA covers whole is finished there (output written
+//     directly); a segment cut by CTA boundaries leaves one (O, LSE) record
+//     per piece -- at most two per CTA, for its first and last segments --
+//     and a reduction kernel merges them;
+//   * the G query heads of a kv head share every K/V byte the CTA reads;
+//   * warp 0 also issues the loads: it walks the CTA's stages, holds the
+//     current sequence's block ids 32 at a time (one coalesced load per 32
+//     blocks, the next group in flight), and fills each 32-row stage with 4-D
+//     TMA boxes (one block, or a 32-row slice of a larger block, of one kv
+//     head) for K and V, tracked by mbarriers, plus a small descriptor of the
+//     stage (sequence, head, valid rows, piece start / end) for the
+//     consumers; a stage is refilled as soon as all four warps released it;
 //   * warps consume 16-row chunks: each half-warp owns two token rows, each
 //     lane 1/16 of head_dim; the 2G (row, head) partial dot products are
 //     summed across the 16 lanes through a small per-warp shared scratch;
 //     the row lands in lane bit 3, so the softmax max and sum over the warp's
 //     four rows are two shuffles each; q . k and P . V use packed fp32x2 FMAs;
-//   * full stages take a straight-line path with no row masking; only a
-//     partition's last stage masks rows;
+//   * full stages take a straight-line path with no row masking;
+//   * at a piece's end the four warps merge through the stage's own tile
+//     (released only afterwards), so the ring keeps streaming the next piece;
 //   * the exponent base is only moved when the running max grows by more than
 //     2^8 (exact: output and denominator keep the same base), so the
 //     accumulator rescale is rare;
@@ -44,32 +54,40 @@ constexpr int kDecodeThreads = kConsumerWarps * 32;
 constexpr int kChunk = 16;             // token rows per softmax update
 constexpr float kRescaleLog2 = 8.0f;   // move the exponent base past 2^8 growth
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kPlanPer = 8;           // sequences per thread per pass of the length scan
+constexpr int kPlanChunk = kDecodeThreads * kPlanPer;
+
+// Stage descriptor flags.
+constexpr int kPieceStart = 1;   // first stage of a piece: reset the state, load q
+constexpr int kPieceEnd = 2;     // last stage of a piece: merge the warps and write
+constexpr int kWhole = 4;        // the piece is its whole segment: write the result
+constexpr int kSlot1 = 8;        // a cut piece that is not the CTA's first: record slot 1
 
 struct DecodeSmem {
-  int tile_elems;   // rows * head_dim
+  int tile_elems;   // rows * head_dim of one K (or V) tile
   int stages;
-  size_t tiles_bytes, bar_off, ok_off, scratch_off, total;
+  size_t tiles_bytes, bar_off, ok_off, desc_off, ring_off, scratch_off, total;
 };
 
-__host__ __device__ inline DecodeSmem decode_smem_layout(int block_size, int head_dim,
-                                                         int elem_bytes, int group, int stages) {
+// Stage s holds its K tile then its V tile; both together also hold the
+// [4][G][D] fp32 merge of a piece's end (16 G D bytes <= 2 * 32 * D * b for
+// G <= 8).
+__host__ __device__ inline DecodeSmem decode_smem_layout(int head_dim, int elem_bytes, int group,
+                                                         int stages) {
   DecodeSmem s;
   s.tile_elems = kStageRows * head_dim;
   s.stages = stages;
-  size_t tiles = (size_t)2 * stages * s.tile_elems * elem_bytes;
-  const size_t merge = (size_t)(kConsumerWarps * group * head_dim + 2 * kConsumerWarps * group) * 4;
-  if (merge > tiles) tiles = merge;
-  s.tiles_bytes = (tiles + 127) & ~(size_t)127;
-  s.bar_off = s.tiles_bytes;
-  s.ok_off = s.bar_off + (size_t)2 * stages * 8;
-  s.scratch_off = (s.ok_off + (size_t)stages * 4 + 15) & ~(size_t)15;
+  s.tiles_bytes = ((size_t)2 * stages * s.tile_elems * elem_bytes + 127) & ~(size_t)127;
+  s.bar_off = s.tiles_bytes;                        // full[stages], empty[stages], merge
+  s.ok_off = s.bar_off + (size_t)(2 * stages + 1) * 8;
+  s.desc_off = (s.ok_off + (size_t)stages * 4 + 15) & ~(size_t)15;
+  s.ring_off = s.desc_off + (size_t)stages * 16;
+  s.scratch_off = s.ring_off + (size_t)2 * 64 * 16;  // two 64-entry stage descriptor rings
   s.total = s.scratch_off + (size_t)kConsumerWarps * 2 * (2 * group * 16) * 4 + 128;  // +128: base alignment
   return s;
 }
 
-int decode_num_stages(int block_size, int head_dim, int elem_bytes) {
-  (void)block_size;
+int decode_num_stages(int head_dim, int elem_bytes) {
   const int stage_bytes = 2 * kStageRows * head_dim * elem_bytes;
   int ns = (49 * 1024) / stage_bytes;  // 3 stages of 16 KiB: 4 CTAs per SM
   if (ns < 2) ns = 2;
@@ -77,8 +95,11 @@ int decode_num_stages(int block_size, int head_dim, int elem_bytes) {
   return ns;
 }
 
-size_t decode_smem_bytes(int block_size, int head_dim, int elem_bytes, int group, int stages) {
-  return decode_smem_layout(block_size, head_dim, elem_bytes, group, stages).total;
+// Stages per CTA: CTA c streams stages [c w, min((c + 1) w, S)) with
+// w = ceil(S / C), so only trailing CTAs can be empty and stage p belongs to
+// CTA p / w.
+__host__ __device__ __forceinline__ long long stages_per_cta(long long S, int C) {
+  return (S + C - 1) / C;
 }
 
 // One 16-row chunk of a stage for one consumer warp: rows row0 and row0 + 1
@@ -181,101 +202,176 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
   constexpr int NV = 2 * G;    // (row, head) partial sums per lane per chunk
   static_assert(NV <= 16 && (NV & (NV - 1)) == 0, "group must be 1, 2, 4 or 8");
 
-  const int kvh = blockIdx.x, part = blockIdx.y, r = blockIdx.z;
-  const int P = a.block_size;
-  const bool reporter = kvh == 0 && part == 0 && threadIdx.x == 0;
-  const int T_r = effective_len(__ldg(a.seq_lens + r), a.max_blocks, P, a.err, reporter);
-  const int nblk = (T_r + P - 1) / P;
-  const int b0 = part * a.blocks_per_part;
-  if (b0 >= nblk) {  // empty partition: the whole CTA leaves before any barrier
-    if (a.direct && part == 0) {  // an empty sequence still gets out = 0, lse = -inf
-      const int64_t rh0 = (int64_t)r * a.num_q_heads + (int64_t)kvh * G;
-      for (int j = threadIdx.x; j < G * D; j += blockDim.x) {
-        store_out(static_cast<T*>(a.out) + rh0 * D + j, 0.f);
-        if (j % D == 0 && a.lse_out) a.lse_out[rh0 + j / D] = -INFINITY;
-      }
-    }
-    return;
-  }
-  const int tok0 = b0 * P;
-  const int tok_end = min(T_r, (b0 + a.blocks_per_part) * P);
-  const int ntiles = (tok_end - tok0 + kStageRows - 1) / kStageRows;  // 64-row stages
-  const int nbp = (tok_end - tok0 + P - 1) / P;  // blocks of this partition
-  const int TB = box_rows_for(P);                // rows per TMA box
-  const int nsub = kStageRows / TB;              // boxes per stage
-
-  const DecodeSmem L = decode_smem_layout(P, D, (int)sizeof(T), G, a.num_stages);
+  const int c = blockIdx.x, C = a.num_ctas;
+  const int Hkv = a.num_kv_heads, B = a.num_seqs, P = a.block_size;
+  const int TB = box_rows_for(P);  // rows per TMA box
+  const DecodeSmem L = decode_smem_layout(D, (int)sizeof(T), G, a.num_stages);
   const int NS = a.num_stages;
   extern __shared__ unsigned char smem_raw[];
   // Align by offsetting the array itself (not through an integer), so the
   // compiler keeps every tile and scratch access in the shared state space.
   unsigned char* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
-  T* ktile = reinterpret_cast<T*>(smem);
-  T* vtile = ktile + (size_t)NS * L.tile_elems;
+  T* tiles = reinterpret_cast<T*>(smem);  // [NS][K tile, V tile]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* empty = full + NS;
+  uint64_t* mrg = empty + NS;  // all 128 threads arrive: the merge's CTA barrier
   volatile int* stage_ok = reinterpret_cast<volatile int*>(smem + L.ok_off);
+  int4* sdesc = reinterpret_cast<int4*>(smem + L.desc_off);  // per ring slot: (seq, head, rows, flags)
+  int4* dA = reinterpret_cast<int4*>(smem + L.ring_off);      // per stage: (id0, id1, row, boxes)
+  int4* dB = dA + 64;                                          // per stage: (seq, head, rows, flags)
   float* scratch = reinterpret_cast<float*>(smem + L.scratch_off);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---------------------------------------------------------------- plan
+  // Every CTA scans the lengths: stages per sequence ceil(T / 32), their
+  // total S (times Hkv), its own range, and the (sequence, kv head, stage)
+  // of its first stage.  CTA 0 also stores the exclusive prefix of stages per
+  // sequence for the reduction and reports bad lengths.  The scan runs in
+  // passes of kPlanChunk sequences, kPlanPer consecutive ones per thread.
+  long long* wsum = reinterpret_cast<long long*>(scratch);  // [4] warp totals, then the start
+  auto scan_chunk = [&](int base, int (&nt)[kPlanPer], long long& excl, long long& total,
+                        bool report) {
+    long long mine = 0;
+#pragma unroll
+    for (int j = 0; j < kPlanPer; ++j) {
+      const int r = base + threadIdx.x * kPlanPer + j;
+      nt[j] = r < B ? (effective_len(__ldg(a.seq_lens + r), a.max_blocks, P, a.err, report) +
+                       kStageRows - 1) / kStageRows
+                    : 0;
+      mine += nt[j];
+    }
+    long long x = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    long long before = 0;
+    total = 0;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const long long t = wsum[w];
+      if (w < warp) before += t;
+      total += t;
+    }
+    excl = before + x - mine;
+    __syncthreads();  // wsum is rewritten by the next pass
+  };
+  long long carry = 0;
+  for (int base = 0; base < B; base += kPlanChunk) {
+    int nt[kPlanPer];
+    long long excl, total;
+    scan_chunk(base, nt, excl, total, c == 0);
+    if (c == 0) {
+      long long p = carry + excl;
+#pragma unroll
+      for (int j = 0; j < kPlanPer; ++j) {
+        const int r = base + threadIdx.x * kPlanPer + j;
+        if (r < B) a.plan_pre[r] = p;
+        p += nt[j];
+      }
+    }
+    carry += total;
+  }
+  if (c == 0 && threadIdx.x == 0) a.plan_pre[B] = carry;
+  const long long S = carry * Hkv;
+  const long long wct = stages_per_cta(S, C);
+  const long long p0 = min((long long)c * wct, S);
+  const int n = (int)(min(p0 + wct, S) - p0);
+  if (n <= 0) return;  // no stages: the whole CTA leaves before any barrier
+  // the sequence holding stage p0, found in a second pass
+  int* start = reinterpret_cast<int*>(wsum + kConsumerWarps);
+  carry = 0;
+  for (int base = 0; base < B; base += kPlanChunk) {
+    int nt[kPlanPer];
+    long long excl, total;
+    scan_chunk(base, nt, excl, total, false);
+    if (p0 < (carry + total) * Hkv) {
+      long long p = carry + excl;
+#pragma unroll
+      for (int j = 0; j < kPlanPer; ++j) {
+        if (nt[j] > 0 && p * Hkv <= p0 && p0 < (p + nt[j]) * Hkv) {
+          const long long off = p0 - p * Hkv;
+          start[0] = base + threadIdx.x * kPlanPer + j;
+          start[1] = (int)(off / nt[j]);
+          start[2] = (int)(off % nt[j]);
+        }
+        p += nt[j];
+      }
+      __syncthreads();
+      break;
+    }
+    carry += total;
+  }
+  const int4 d0 = make_int4(start[0], start[1], start[2], 0);
+  __syncthreads();  // the scratch is the consumers' from here on
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
+    mbar_init(mrg, kDecodeThreads);
     fence_barrier_init();
   }
   __syncthreads();
 
   // ---------------------------------------------------------------- loads
-  // Warp 0 issues the TMA boxes.  It holds the partition's block ids 32 at a
-  // time (one coalesced load per 32 blocks, the next group in flight) so no
-  // table lookup sits between two copies.  A stage is kStageRows token rows:
-  // kStageRows / P boxes of one block each when P < kStageRows, else one
-  // box of kStageRows rows of a larger block.  Positions advance
-  // incrementally (no division).
-  const int32_t* tbl = a.block_tables + (int64_t)r * a.max_blocks + b0;
-  int cur = 0, nxt = 0, base = 0;
-  int jb = 0, brow = 0, rel = 0;  // next box: block in the partition, row in it, row in partition
-  const int avail = tok_end - tok0;
+  // Warp 0 issues the loads.  Once per 32 stages it works out the next 32
+  // stages of the CTA's range lane-parallel (lane l: stage kb + l) into a
+  // two-batch descriptor ring in shared memory: block ids of the stage's
+  // boxes, first row in the block, box count, and (sequence, kv head, valid
+  // rows, flags).  The cursor (cr, ch, ci) is the position of the next
+  // batch's first stage, cpnt / cT the stages and length of sequence cr.
+  int cr = d0.x, ch = d0.y, ci = d0.z, cpnt = 0, cT = 0;
   const uint32_t box_bytes = (uint32_t)(TB * D * sizeof(T));
-  if (warp == 0) {
-    if (lane == 0) {
-      prefetch_tensormap(&tmk);
-      prefetch_tensormap(&tmv);
-    }
-    cur = lane < nbp ? __ldg(tbl + lane) : -1;
-    nxt = 32 + lane < nbp ? __ldg(tbl + 32 + lane) : -1;
-  }
-  // Fill stage `st` with the next kStageRows rows (warp 0, all lanes).
-  auto issue_stage = [&](int st) {
-    int blk[kStageRows / 16], brw[kStageRows / 16];
-    int nbox = 0;
-#pragma unroll
-    for (int j = 0; j < kStageRows / 16; ++j) {
-      blk[j] = -1;
-      brw[j] = 0;
-      if (j < nsub && rel < avail) {
-        if (jb >= base + 32) {
-          cur = nxt;
-          base += 32;
-          nxt = base + 32 + lane < nbp ? __ldg(tbl + base + 32 + lane) : -1;
-        }
-        blk[j] = __shfl_sync(0xffffffffu, cur, jb - base);
-        brw[j] = brow;
-        nbox = j + 1;
-        rel += TB;
-        brow += TB;
-        if (brow == P) {
-          brow = 0;
-          ++jb;
+  auto compute_batch = [&](int kb) {
+    int r = cr, h = ch, i = ci + lane, pnt = cpnt, len = cT;
+    const bool act = kb + lane < n;
+    if (act) {
+      while (i >= pnt) {  // crossed into a later segment (rare)
+        i -= pnt;
+        if (++h == Hkv) {
+          h = 0;
+          do {
+            ++r;
+            len = effective_len(__ldg(a.seq_lens + r), a.max_blocks, P, a.err, false);
+            pnt = (len + kStageRows - 1) / kStageRows;
+          } while (pnt == 0);
         }
       }
+      const int k = kb + lane, row0 = i * kStageRows;
+      const int nvalid = min(kStageRows, len - row0);
+      const int b0 = row0 / P;
+      const int nbox = (nvalid + TB - 1) / TB;  // 1 or 2 (two only when P < 32)
+      const int32_t* tbl = a.block_tables + (int64_t)r * a.max_blocks + b0;
+      const int id0 = __ldg(tbl), id1 = nbox > 1 ? __ldg(tbl + 1) : -1;
+      const int dseg = k - i;  // CTA stage index of the segment's first stage
+      const bool end = k == n - 1 || i == pnt - 1;
+      const int flags = (k == 0 || i == 0 ? kPieceStart : 0) | (end ? kPieceEnd : 0) |
+                        (end && i == pnt - 1 && dseg >= 0 ? kWhole : 0) | (dseg > 0 ? kSlot1 : 0);
+      dA[k & 63] = make_int4(id0, id1, row0 - b0 * P, nbox);
+      dB[k & 63] = make_int4(r, h, nvalid, flags);
     }
-    bool valid = true;
-#pragma unroll
-    for (int j = 0; j < kStageRows / 16; ++j)
-      if (j < nbox && (blk[j] < 0 || (int64_t)blk[j] >= a.num_blocks)) valid = false;
+    // the cursor moves to the stage after lane 31's
+    cr = __shfl_sync(0xffffffffu, r, 31);
+    ch = __shfl_sync(0xffffffffu, h, 31);
+    ci = __shfl_sync(0xffffffffu, i, 31) + 1;
+    cpnt = __shfl_sync(0xffffffffu, pnt, 31);
+    cT = __shfl_sync(0xffffffffu, len, 31);
+    __syncwarp();
+  };
+  // Fill ring slot `st` with the CTA's k-th stage (warp 0, all lanes).
+  auto issue_stage = [&](int st, int k) {
+    const int4 da = dA[k & 63];
+    const int4 db = dB[k & 63];
+    const int nbox = da.w;
+    const bool valid = da.x >= 0 && (int64_t)da.x < a.num_blocks &&
+                       (nbox < 2 || (da.y >= 0 && (int64_t)da.y < a.num_blocks));
+    if (lane == 0) sdesc[st] = db;
     if (!valid) {
       if (lane == 0) {
         atomicOr(a.err, PKV_DEVERR_BLOCK);
@@ -291,163 +387,207 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
       // one box per lane: lanes 0..nbox-1 load K, lanes 16..16+nbox-1 load V
       const int j = lane & 15;
       if (j < nbox) {
-        int bj = blk[0], rj = brw[0];
-#pragma unroll
-        for (int jj = 1; jj < kStageRows / 16; ++jj)
-          if (j == jj) {
-            bj = blk[jj];
-            rj = brw[jj];
-          }
-        if (lane < 16)
-          tma_load_4d(ktile + (size_t)st * L.tile_elems + j * TB * D, &tmk, 0, kvh, rj, bj, &full[st]);
-        else
-          tma_load_4d(vtile + (size_t)st * L.tile_elems + j * TB * D, &tmv, 0, kvh, rj, bj, &full[st]);
+        T* dst = tiles + (size_t)st * 2 * L.tile_elems + (lane < 16 ? 0 : L.tile_elems) + j * TB * D;
+        tma_load_4d(dst, lane < 16 ? &tmk : &tmv, 0, db.y, j == 0 ? da.z : 0, j == 0 ? da.x : da.y,
+                    &full[st]);
       }
     }
+    if ((k & 31) == 0 && k + 32 < n) compute_batch(k + 32);
   };
   if (warp == 0) {
-    for (int st = 0; st < NS && st < ntiles; ++st) issue_stage(st);
+    if (lane == 0) {
+      prefetch_tensormap(&tmk);
+      prefetch_tensormap(&tmv);
+    }
+    cT = effective_len(__ldg(a.seq_lens + cr), a.max_blocks, P, a.err, false);
+    cpnt = (cT + kStageRows - 1) / kStageRows;
+    compute_batch(0);
+    for (int st = 0; st < NS && st < n; ++st) issue_stage(st, st);
   }
 
   // ------------------------------------------------------------------ consumers
   const int hw = lane >> 4, l16 = lane & 15;
   float2 q2[G][EP2];
-  {
-    const T* qp = static_cast<const T*>(a.q) +
-                  ((int64_t)r * a.num_q_heads + (int64_t)kvh * G) * D + l16 * EPL;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float f[EPL];
-      VecLoad<T, EPL>::run(qp + g * D, f);
-#pragma unroll
-      for (int j = 0; j < EP2; ++j) q2[g][j] = make_float2(f[2 * j] * a.qscale, f[2 * j + 1] * a.qscale);
-    }
-  }
   float2 acc[G][EP2];
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int j = 0; j < EP2; ++j) acc[g][j] = make_float2(0.f, 0.f);
-
   // (m_used, l_run): softmax state of head (l16 / (8 / G)) % G of this lane.
   float m_used = -INFINITY, l_run = 0.f;
   float* red = scratch + (warp * 2 + hw) * (2 * G * 16);
   const int rbase = warp * 4 + hw * 2;
   int s = 0, round = 0;
-  int remain = tok_end - tok0;  // rows of this partition not yet consumed
-  for (int i = 0; i < ntiles; ++i) {
-    const int nvalid = min(kStageRows, remain);
-    remain -= kStageRows;
-    if (!mbar_wait(&full[s], round & 1)) {
+  uint32_t mrg_phase = 0;
+  // CTA barrier of the merge, bounded like every wait here; warp-uniform.
+  auto merge_sync = [&]() -> bool {
+    mbar_arrive(mrg);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(mrg, mrg_phase));
+    mrg_phase ^= 1u;
+    if (!ok && lane == 0) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
+    return ok;
+  };
+  int k = 0;
+  for (; k < n; ++k) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], round & 1))) {
       if (lane == 0) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
       break;
     }
+    const int4 dsc = sdesc[s];  // (sequence, kv head, valid rows, flags)
+    const int nvalid = dsc.z, flags = dsc.w;
+    const T* kt = tiles + (size_t)s * 2 * L.tile_elems;
+    const T* vt = kt + L.tile_elems;
+    if (flags & kPieceStart) {
+      const T* qp = static_cast<const T*>(a.q) +
+                    ((int64_t)dsc.x * a.num_q_heads + (int64_t)dsc.y * G) * D + l16 * EPL;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float f[EPL];
+        VecLoad<T, EPL>::run(qp + g * D, f);
+#pragma unroll
+        for (int j = 0; j < EP2; ++j) {
+          q2[g][j] = make_float2(f[2 * j] * a.qscale, f[2 * j + 1] * a.qscale);
+          acc[g][j] = make_float2(0.f, 0.f);
+        }
+      }
+      m_used = -INFINITY;
+      l_run = 0.f;
+    }
     if (stage_ok[s]) {
-      const T* kt = ktile + (size_t)s * L.tile_elems;
-      const T* vt = vtile + (size_t)s * L.tile_elems;
       if (nvalid == kStageRows) {
 #pragma unroll 1
-        for (int c = 0; c < kStageRows / kChunk; ++c)
-          decode_chunk<T, D, G, false>(kt, vt, c * kChunk + rbase, kStageRows, q2, acc, m_used,
+        for (int cc = 0; cc < kStageRows / kChunk; ++cc)
+          decode_chunk<T, D, G, false>(kt, vt, cc * kChunk + rbase, kStageRows, q2, acc, m_used,
                                        l_run, red, l16);
       } else {
-        for (int c = 0; c * kChunk < nvalid; ++c)
-          decode_chunk<T, D, G, true>(kt, vt, c * kChunk + rbase, nvalid, q2, acc, m_used, l_run,
+        for (int cc = 0; cc * kChunk < nvalid; ++cc)
+          decode_chunk<T, D, G, true>(kt, vt, cc * kChunk + rbase, nvalid, q2, acc, m_used, l_run,
                                       red, l16);
       }
     }
+    if (flags & kPieceEnd) {
+      // ---- merge the four warps through this stage's tile, then write
+      if (!merge_sync()) break;  // every warp is done with the tile
+      float* macc = reinterpret_cast<float*>(const_cast<T*>(kt));  // [4][G][D]
+      float* mm = scratch;                                          // [4][G]
+      float* ml = mm + kConsumerWarps * G;                          // [4][G]
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int j = 0; j < EP2; ++j) {
+          float2 v = acc[g][j];
+          v.x += __shfl_xor_sync(0xffffffffu, v.x, 16);
+          v.y += __shfl_xor_sync(0xffffffffu, v.y, 16);
+          if (hw == 0) {
+            macc[(warp * G + g) * D + l16 * EPL + 2 * j] = v.x;
+            macc[(warp * G + g) * D + l16 * EPL + 2 * j + 1] = v.y;
+          }
+        }
+      constexpr int LPV = 8 / G;  // lanes per (row, head) value
+      if (lane < 8 && lane % LPV == 0) {  // row 0 of half-warp 0, first lane of each head
+        mm[warp * G + lane / LPV] = m_used;
+        ml[warp * G + lane / LPV] = l_run;
+      }
+      if (!merge_sync()) break;
+      const int64_t rh0 = (int64_t)dsc.x * a.num_q_heads + (int64_t)dsc.y * G;
+      const int64_t rec = (int64_t)2 * c + ((flags & kSlot1) ? 1 : 0);
+      for (int j = threadIdx.x; j < G * D; j += kDecodeThreads) {
+        const int g = j / D, e = j % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mm[w * G + g]);
+        float Lsum = 0.f, o = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            const float wt = exp2f(mm[w * G + g] - M);
+            Lsum = fmaf(wt, ml[w * G + g], Lsum);
+            o = fmaf(wt, macc[(w * G + g) * D + e], o);
+          }
+        }
+        const bool nonempty = Lsum > 0.f;
+        o = nonempty ? o / Lsum : 0.f;
+        const float lse2 = nonempty ? M + log2f(Lsum) : -INFINITY;
+        const int64_t rh = rh0 + g;
+        if (!(flags & kWhole)) {
+          a.rec_o[(rec * G + g) * D + e] = o;
+          if (e == 0) a.rec_lse[rec * G + g] = lse2;
+        } else if (a.st_o) {
+          const int64_t slot = rh * a.st_stride + a.st_slot;
+          a.st_o[slot * D + e] = o;
+          if (e == 0) a.st_lse[slot] = lse2;
+        } else {
+          store_out(static_cast<T*>(a.out) + rh * D + e, o);
+          if (e == 0 && a.lse_out) a.lse_out[rh] = lse2 * kLn2;
+        }
+      }
+      if (!merge_sync()) break;  // merge reads done before the tile is refilled
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
-    if (warp == 0 && i + NS < ntiles) {
-      // every warp has released stage s: refill it with stage i + NS
+    if (warp == 0 && k + NS < n) {
+      // every warp has released ring slot s: refill it with stage k + NS
       int ok = 1;
       if (lane == 0 && !mbar_wait(&empty[s], round & 1)) {
         atomicOr(a.err, PKV_DEVERR_TIMEOUT);
         ok = 0;
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      issue_stage(s);
+      issue_stage(s, k + NS);
     }
     if (++s == NS) {
       s = 0;
       ++round;
     }
   }
-
-  // ------------------------------------------------------------------ merge the 4 warps
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int j = 0; j < EP2; ++j) {
-      acc[g][j].x += __shfl_xor_sync(0xffffffffu, acc[g][j].x, 16);
-      acc[g][j].y += __shfl_xor_sync(0xffffffffu, acc[g][j].y, 16);
-    }
-
-  __syncthreads();  // every stage consumed: reuse the tiles
-  float* macc = reinterpret_cast<float*>(smem);            // [4][G][D]
-  float* mm = macc + kConsumerWarps * G * D;               // [4][G]
-  float* ml = mm + kConsumerWarps * G;                     // [4][G]
-  if (hw == 0) {
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int j = 0; j < EP2; ++j) {
-        macc[(warp * G + g) * D + l16 * EPL + 2 * j] = acc[g][j].x;
-        macc[(warp * G + g) * D + l16 * EPL + 2 * j + 1] = acc[g][j].y;
-      }
-    constexpr int LPV = 8 / G;  // lanes per (row, head) value
-    if (l16 < 8 && l16 % LPV == 0) {  // row 0 of the half-warp, first lane of each head
-      mm[warp * G + l16 / LPV] = m_used;
-      ml[warp * G + l16 / LPV] = l_run;
-    }
-  }
-  __syncthreads();
-
-  for (int j = threadIdx.x; j < G * D; j += kConsumerWarps * 32) {
-    const int g = j / D, e = j % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mm[w * G + g]);
-    float Lsum = 0.f, o = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float wt = exp2f(mm[w * G + g] - M);
-        Lsum = fmaf(wt, ml[w * G + g], Lsum);
-        o = fmaf(wt, macc[(w * G + g) * D + e], o);
-      }
-    }
-    const bool nonempty = Lsum > 0.f;
-    o = nonempty ? o / Lsum : 0.f;
-    const float lse2 = nonempty ? M + log2f(Lsum) : -INFINITY;
-    const int64_t rh = (int64_t)r * a.num_q_heads + (int64_t)kvh * G + g;
-    if (a.direct) {
-      store_out(static_cast<T*>(a.out) + rh * D + e, o);
-      if (e == 0 && a.lse_out) a.lse_out[rh] = lse2 * kLn2;
-    } else {
-      const int64_t slot = rh * a.parts_stride + a.part_offset + part;
-      a.part_o[slot * D + e] = o;
-      if (e == 0) a.part_lse[slot] = lse2;
-    }
+  if (k < n && warp == 0 && lane == 0) {
+    // left early after a timeout: wait (bounded) for copies still in flight
+    // into the ring before the CTA's shared memory is released
+    for (int kk = k; kk < min(n, k + NS); ++kk) mbar_wait(&full[kk % NS], (kk / NS) & 1);
   }
 }
 
-// One warp per (sequence, query head): merge its partitions by log-sum-exp.
+// One warp per (sequence, query head): merge the pieces of its segment (and,
+// in states mode, the extra states before them) by log-sum-exp.  A segment
+// one CTA covered whole was written by that CTA (plain mode: nothing to do).
 template <typename T, int D>
 __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) {
   constexpr int EPL = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t rh = (int64_t)blockIdx.x * 4 + warp;
   if (rh >= (int64_t)a.num_seqs * a.num_q_heads) return;
-  const int r = (int)(rh / a.num_q_heads);
-  const int P = a.block_size;
-  const int T_r = effective_len(__ldg(a.seq_lens + r), a.max_blocks, P, a.err, false);
-  const int nblk = (T_r + P - 1) / P;
-  const int nparts = a.part_offset + (nblk + a.blocks_per_part - 1) / a.blocks_per_part;
-  const float* plse = a.part_lse + rh * a.parts_stride;
-  const float* po = a.part_o + rh * a.parts_stride * D;
+  const int r = (int)(rh / a.num_q_heads), qh = (int)(rh % a.num_q_heads);
+  const int G = a.num_q_heads / a.num_kv_heads, h = qh / G, g = qh % G;
+  const int Hkv = a.num_kv_heads, C = a.num_ctas;
+  const long long S = a.plan_pre[a.num_seqs] * Hkv;
+  const long long s0 = a.plan_pre[r], nt = a.plan_pre[r + 1] - s0;
+  const int n_ext = a.st_o ? a.st_slot : 0;
+  // Sources: extra states [0, n_ext), then either the whole-segment state
+  // (states mode) or pieces c_first..c_last.
+  const long long wct = stages_per_cta(S, C);
+  int c_first = 0, n_pc = 0;  // pieces: CTAs c_first .. c_first + n_pc - 1
+  bool whole_state = false;
+  long long seg0 = 0;
+  if (nt > 0) {
+    seg0 = s0 * Hkv + (long long)h * nt;
+    c_first = (int)(seg0 / wct);
+    const int c_last = (int)((seg0 + nt - 1) / wct);
+    if (c_first == c_last) {
+      if (!a.st_o) return;  // written whole by its CTA
+      whole_state = true;
+    } else {
+      n_pc = c_last - c_first + 1;
+    }
+  }
+  const float* ext_lse = a.st_o ? a.st_lse + rh * a.st_stride : nullptr;
+  const float* ext_o = a.st_o ? a.st_o + rh * a.st_stride * D : nullptr;
+  const int n_st = n_ext + (whole_state ? 1 : 0);
+  // a cut segment's first piece is in slot 1 of its CTA unless the segment
+  // starts that CTA's range
+  const bool first_is_slot1 = n_pc > 0 && seg0 != (long long)c_first * wct;
+  auto piece_rec = [&](int i) -> int64_t {  // record of piece i (CTA c_first + i)
+    const int64_t cc = c_first + i;
+    return (2 * cc + (i == 0 && first_is_slot1 ? 1 : 0)) * G + g;
+  };
   float M = -INFINITY;
-  for (int p = lane; p < nparts; p += 32) M = fmaxf(M, plse[p]);
+  for (int i = lane; i < n_st + n_pc; i += 32)
+    M = fmaxf(M, i < n_st ? ext_lse[i] : a.rec_lse[piece_rec(i - n_st)]);
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float acc[EPL];
@@ -455,11 +595,14 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) 
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
   float Lsum = 0.f;
   if (M != -INFINITY) {
-    for (int p = 0; p < nparts; ++p) {
-      const float w = exp2f(plse[p] - M);
+    for (int i = 0; i < n_st + n_pc; ++i) {
+      const float l = i < n_st ? ext_lse[i] : a.rec_lse[piece_rec(i - n_st)];
+      if (l == -INFINITY) continue;  // empty state: the merge's identity
+      const float w = exp2f(l - M);
       Lsum += w;
+      const float* po = i < n_st ? ext_o + (int64_t)i * D : a.rec_o + piece_rec(i - n_st) * D;
       float x[EPL];
-      VecLoad<float, EPL>::run(po + (int64_t)p * D + lane * EPL, x);
+      VecLoad<float, EPL>::run(po + lane * EPL, x);
 #pragma unroll
       for (int e = 0; e < EPL; ++e) acc[e] = fmaf(w, x[e], acc[e]);
     }
@@ -472,32 +615,63 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) 
 }
 
 template <typename T, int D, int G>
+static size_t partial_smem_bytes() {
+  return decode_smem_layout(D, (int)sizeof(T), G, decode_num_stages(D, (int)sizeof(T))).total;
+}
+
+template <typename T, int D, int G>
 static cudaError_t launch_partial(const CUtensorMap& tmk, const CUtensorMap& tmv,
                                   const DecodeArgs& a, cudaStream_t stream) {
-  const size_t smem = decode_smem_bytes(a.block_size, D, (int)sizeof(T), G, a.num_stages);
+  const size_t smem = decode_smem_layout(D, (int)sizeof(T), G, a.num_stages).total;
   auto kern = decode_partial_kernel<T, D, G>;
   static SmemAttrCache attr_cache;
   cudaError_t e = ensure_smem_limit(kern, (int)smem, attr_cache);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)a.num_kv_heads, (unsigned)a.max_parts, (unsigned)a.num_seqs);
-  kern<<<grid, kDecodeThreads, smem, stream>>>(tmk, tmv, a);
+  kern<<<(unsigned)a.num_ctas, kDecodeThreads, smem, stream>>>(tmk, tmv, a);
   return cudaGetLastError();
+}
+
+// Resident CTAs per SM of one partial-kernel instance, looked up once per
+// device.
+template <typename T, int D, int G>
+static int resident_ctas() {
+  static std::mutex mu;
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    const size_t smem = partial_smem_bytes<T, D, G>();
+    auto kern = decode_partial_kernel<T, D, G>;
+    int per_sm = 0, sms = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecodeThreads, smem) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return 0;
+    cached[dev] = per_sm * sms;
+  }
+  return cached[dev];
 }
 
 template <typename T, int D>
-static cudaError_t launch_reduce_t(const DecodeArgs& a, cudaStream_t stream) {
-  const int64_t rows = (int64_t)a.num_seqs * a.num_q_heads;
-  decode_reduce_kernel<T, D><<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(a);
-  return cudaGetLastError();
+static int resident_for_group(int group) {
+  switch (group) {
+    case 1: return resident_ctas<T, D, 1>();
+    case 2: return resident_ctas<T, D, 2>();
+    case 4: return resident_ctas<T, D, 4>();
+    case 8: return resident_ctas<T, D, 8>();
+    default: return 0;
+  }
 }
 
-cudaError_t launch_decode_reduce(int dtype, int head_dim, const DecodeArgs& a,
-                                 cudaStream_t stream) {
+int decode_resident_ctas(int dtype, int head_dim, int group) {
   if (dtype == PKV_BF16)
-    return head_dim == 128 ? launch_reduce_t<__nv_bfloat16, 128>(a, stream)
-                           : launch_reduce_t<__nv_bfloat16, 64>(a, stream);
-  return head_dim == 128 ? launch_reduce_t<float, 128>(a, stream)
-                         : launch_reduce_t<float, 64>(a, stream);
+    return head_dim == 128 ? resident_for_group<__nv_bfloat16, 128>(group)
+                           : resident_for_group<__nv_bfloat16, 64>(group);
+  return head_dim == 128 ? resident_for_group<float, 128>(group)
+                         : resident_for_group<float, 64>(group);
 }
 
 template <typename T, int D>
@@ -512,6 +686,13 @@ static cudaError_t dispatch_group(int group, const CUtensorMap& tmk, const CUten
   }
 }
 
+template <typename T, int D>
+static cudaError_t launch_reduce_t(const DecodeArgs& a, cudaStream_t stream) {
+  const int64_t rows = (int64_t)a.num_seqs * a.num_q_heads;
+  decode_reduce_kernel<T, D><<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_paged_decode(int dtype, int head_dim, int group, const CUtensorMap& tmk,
                                 const CUtensorMap& tmv, const DecodeArgs& a,
                                 cudaStream_t stream) {
@@ -522,8 +703,12 @@ cudaError_t launch_paged_decode(int dtype, int head_dim, int group, const CUtens
   else
     e = head_dim == 128 ? dispatch_group<float, 128>(group, tmk, tmv, a, stream)
                         : dispatch_group<float, 64>(group, tmk, tmv, a, stream);
-  if (e != cudaSuccess || a.direct) return e;
-  return launch_decode_reduce(dtype, head_dim, a, stream);
+  if (e != cudaSuccess) return e;
+  if (dtype == PKV_BF16)
+    return head_dim == 128 ? launch_reduce_t<__nv_bfloat16, 128>(a, stream)
+                           : launch_reduce_t<__nv_bfloat16, 64>(a, stream);
+  return head_dim == 128 ? launch_reduce_t<float, 128>(a, stream)
+                         : launch_reduce_t<float, 64>(a, stream);
 }
 
 }  // namespace pkv

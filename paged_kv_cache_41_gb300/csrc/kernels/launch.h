@@ -44,43 +44,54 @@ __host__ __device__ constexpr int box_rows_for(int block_size) {
   return block_size < kStageRows ? block_size : kStageRows;
 }
 
-// Arguments of the split-K paged decode kernels.
+// Arguments of the paged decode kernels.
+//
+// Work list: every (sequence, kv head) segment of ceil(T / kStageRows)
+// stages, sequence-major then kv head; S stages in all.  CTA c of C streams
+// stages [c w, min((c + 1) w, S)), w = ceil(S / C).  A segment a CTA covers
+// whole is written out directly; a segment cut by a CTA boundary leaves one
+// record per piece, slot 0 of its CTA for the piece holding the CTA's first
+// stage and slot 1 for a last piece that is not also the first.
 struct DecodeArgs {
   const void* q;                // [B, Hq, D]
   const int32_t* block_tables;  // [B, max_blocks]
   const int32_t* seq_lens;      // [B]
-  float* part_o;                // [B, Hq, parts_stride, D] normalised partial outputs
-  float* part_lse;              // [B, Hq, parts_stride] partial LSE, base 2
   void* out;                    // [B, Hq, D]
   float* lse_out;               // [B, Hq] natural log, or null
   unsigned int* err;
+  int64_t* plan_pre;            // [B + 1] exclusive prefix of stages per sequence (CTA 0 writes)
+  float* rec_o;                 // [2C, G, D] normalised piece outputs
+  float* rec_lse;               // [2C, G] piece LSEs, base 2
+  // States mode (shared prefix): a whole segment writes (O, LSE base 2) to
+  // slot st_slot of st_o / st_lse instead of out, and the reduction also
+  // merges the st_slot extra states held in slots [0, st_slot).  Plain
+  // decode: st_o == nullptr.
+  float* st_o;                  // [B, Hq, st_stride, D]
+  float* st_lse;                // [B, Hq, st_stride]
+  int32_t st_stride;
+  int32_t st_slot;
   int64_t num_blocks;
   int32_t max_blocks;
   int32_t num_seqs;
   int32_t num_q_heads;
   int32_t num_kv_heads;
   int32_t block_size;
-  int32_t blocks_per_part;
-  int32_t max_parts;     // partitions per sequence at most (grid.y)
-  int32_t part_offset;   // partial slots before the first decode partition
-  int32_t parts_stride;  // partial slots per (sequence, head)
-  int32_t num_stages;
+  int32_t num_ctas;      // C
+  int32_t num_stages;    // shared-memory ring depth
   float qscale;          // softmax scale * log2(e)
-  int32_t direct;        // 1: a single partition per sequence writes out/lse itself
 };
 
-// Launch the partial kernel (and the LSE reduction unless args.direct).
+// Partial kernel, then the LSE reduction of cut segments, on one stream.
 cudaError_t launch_paged_decode(int dtype, int head_dim, int group, const CUtensorMap& tmk,
                                 const CUtensorMap& tmv, const DecodeArgs& args,
                                 cudaStream_t stream);
 
-// LSE reduction over the partial states (also used after the shared prefix).
-cudaError_t launch_decode_reduce(int dtype, int head_dim, const DecodeArgs& args,
-                                 cudaStream_t stream);
+// CTAs of one wave of the partial kernel (resident CTAs per SM x SMs).
+int decode_resident_ctas(int dtype, int head_dim, int group);
 
 // Arguments of the shared-prefix tensor-core kernel.  Grid: (key split,
-// 128-row query tile, kv head).  Its states go to partial slots
-// [0, num_splits) of the same workspace layout the decode kernels use.
+// 128-row query tile, kv head).  Its states go to slots [0, num_splits) of
+// [B, Hq, parts_stride] state arrays.
 struct PrefixArgs {
   const int32_t* prefix_block_ids;  // [ceil(prefix_len / P)]
   float* part_o;                    // [B, Hq, parts_stride, D]
@@ -108,8 +119,7 @@ cudaError_t launch_prefix_attention(int head_dim, int group, int num_splits,
                                     cudaStream_t stream);
 size_t prefix_smem_bytes(int head_dim, int split_len, int block_size);
 
-// Stage count and dynamic shared memory of the partial kernel.
-int decode_num_stages(int block_size, int head_dim, int elem_bytes);
-size_t decode_smem_bytes(int block_size, int head_dim, int elem_bytes, int group, int stages);
+// Stage count of the partial kernel's shared-memory ring.
+int decode_num_stages(int head_dim, int elem_bytes);
 
 }  // namespace pkv

@@ -158,20 +158,57 @@ int sm_count() {
   return n;
 }
 
-int32_t auto_partition(const pkv_cache_desc* c, int32_t num_seqs, int32_t max_blocks) {
-  // 1024-token partitions (measured best on GB300 for block sizes 16-64: long
-  // enough to amortise a CTA's set-up and merge, short enough to balance
-  // ragged lengths); halved while the grid would give fewer than two waves of
-  // the four CTAs an SM holds, down to 256 tokens or one block.
-  const int P = c->block_size;
-  const int64_t max_tokens = (int64_t)max_blocks * P;
-  const int64_t rows = (int64_t)num_seqs * c->num_kv_heads;
-  const int64_t target = (int64_t)sm_count() * 4 * 2;
-  int32_t ps = ((1024 + P - 1) / P) * P;
-  while (ps / 2 >= 256 && ps / 2 >= P && (ps / 2) % P == 0 &&
-         rows * ((max_tokens + ps - 1) / ps) < target)
-    ps /= 2;
-  return ps;
+// Stages (kStageRows rows of one kv head) in the decode work list at most:
+// every (sequence, kv head) at max_blocks * P rows.
+int64_t max_decode_stages(const pkv_cache_desc* c, int32_t num_seqs, int32_t max_blocks) {
+  const int64_t rows = (int64_t)max_blocks * c->block_size;
+  return (int64_t)num_seqs * c->num_kv_heads * ((rows + pkv::kStageRows - 1) / pkv::kStageRows);
+}
+
+// CTAs of the persistent decode kernel: one wave of resident CTAs (fewer
+// when there are fewer stages); partition_size > 0 adds CTAs until none
+// streams more than partition_size rows (at least one stage each).
+int64_t decode_ctas(const pkv_cache_desc* c, int32_t num_seqs, int32_t num_q_heads,
+                    int32_t max_blocks, int32_t partition_size) {
+  const int G = num_q_heads / c->num_kv_heads;
+  int64_t resident = pkv::decode_resident_ctas(c->dtype, c->head_dim, G);
+  if (resident <= 0) resident = 4LL * sm_count();
+  const int64_t smax = max_decode_stages(c, num_seqs, max_blocks);
+  int64_t C = resident < smax ? resident : smax;
+  if (partition_size > 0) {
+    int64_t cap = partition_size / pkv::kStageRows;
+    if (cap < 1) cap = 1;
+    const int64_t need = (smax + cap - 1) / cap;
+    if (need > C) C = need;
+  }
+  const int64_t fit = (smax + (1LL << 30) - 1) >> 30;  // stages per CTA fit an int
+  if (fit > C) C = fit;
+  return C < 1 ? 1 : C;
+}
+
+// Decode workspace: stage prefix [B + 1] int64, piece LSEs [2C, G] and piece
+// outputs [2C, G, D] fp32, each 256-byte aligned.
+struct DecodeWorkspace {
+  size_t pre_off, lse_off, o_off, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+DecodeWorkspace decode_workspace(int64_t num_seqs, int64_t ctas, int64_t group, int64_t head_dim) {
+  DecodeWorkspace w;
+  w.pre_off = 0;
+  w.lse_off = align256((size_t)(num_seqs + 1) * 8);
+  w.o_off = w.lse_off + align256((size_t)(2 * ctas * group) * 4);
+  w.total = w.o_off + align256((size_t)(2 * ctas * group * head_dim) * 4);
+  return w;
+}
+
+// Point the decode arguments' plan and piece records into a workspace.
+void bind_decode_workspace(pkv::DecodeArgs* a, void* base, const DecodeWorkspace& w) {
+  unsigned char* b = static_cast<unsigned char*>(base);
+  a->plan_pre = reinterpret_cast<int64_t*>(b + w.pre_off);
+  a->rec_lse = reinterpret_cast<float*>(b + w.lse_off);
+  a->rec_o = reinterpret_cast<float*>(b + w.o_off);
 }
 
 
@@ -236,11 +273,9 @@ pkv_status check_prefix_shape(const pkv_cache_desc* c, int32_t num_q_heads, int3
   return PKV_OK;
 }
 
-size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
-
-// Partial-state workspace: [B, Hq, parts] x (D floats of output + 1 LSE).
-size_t partial_bytes(int64_t rows, int64_t parts, int64_t head_dim) {
-  return align256((size_t)(rows * parts * head_dim) * 4) + align256((size_t)(rows * parts) * 4);
+// Shared-prefix states: [B, Hq, stride] x (D floats of output + 1 LSE).
+size_t states_bytes(int64_t rows, int64_t stride, int64_t head_dim) {
+  return align256((size_t)(rows * stride * head_dim) * 4) + align256((size_t)(rows * stride) * 4);
 }
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
@@ -301,25 +336,26 @@ pkv_status pkv_kv_block_copy(const pkv_cache_desc* cache, void* k_cache, void* v
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-int32_t pkv_decode_auto_partition(const pkv_cache_desc* cache, int32_t num_seqs,
-                                  int32_t num_q_heads, int32_t max_blocks_per_seq) {
-  (void)num_q_heads;
-  if (check_cache(cache) != PKV_OK || max_blocks_per_seq <= 0 || num_seqs <= 0) return 0;
-  return auto_partition(cache, num_seqs, max_blocks_per_seq);
+int32_t pkv_decode_num_ctas(const pkv_cache_desc* cache, int32_t num_seqs, int32_t num_q_heads,
+                            int32_t max_blocks_per_seq, int32_t partition_size) {
+  if (check_cache(cache) != PKV_OK || max_blocks_per_seq <= 0 || num_seqs <= 0 ||
+      partition_size < 0 || check_attention_shape(cache, num_q_heads) != PKV_OK ||
+      partition_size % cache->block_size != 0)
+    return 0;
+  const int64_t C = decode_ctas(cache, num_seqs, num_q_heads, max_blocks_per_seq, partition_size);
+  return C > INT32_MAX ? 0 : (int32_t)C;
 }
 
 size_t pkv_decode_workspace_bytes(const pkv_cache_desc* cache, int32_t num_seqs,
                                   int32_t num_q_heads, int32_t max_blocks_per_seq,
                                   int32_t partition_size) {
   if (check_cache(cache) != PKV_OK || num_seqs <= 0 || num_q_heads <= 0 ||
-      max_blocks_per_seq <= 0 || partition_size < 0)
+      max_blocks_per_seq <= 0 || partition_size < 0 ||
+      check_attention_shape(cache, num_q_heads) != PKV_OK ||
+      partition_size % cache->block_size != 0)
     return 0;
-  if (partition_size == 0) partition_size = auto_partition(cache, num_seqs, max_blocks_per_seq);
-  if (partition_size % cache->block_size != 0) return 0;
-  const int64_t bpp = partition_size / cache->block_size;
-  const int64_t parts = (max_blocks_per_seq + bpp - 1) / bpp;
-  if (parts <= 1) return 0;
-  return partial_bytes((int64_t)num_seqs * num_q_heads, parts, cache->head_dim);
+  const int64_t C = decode_ctas(cache, num_seqs, num_q_heads, max_blocks_per_seq, partition_size);
+  return decode_workspace(num_seqs, C, num_q_heads / cache->num_kv_heads, cache->head_dim).total;
 }
 
 pkv_status pkv_paged_attention_decode(const pkv_cache_desc* cache, void* out, float* lse,
@@ -338,15 +374,13 @@ pkv_status pkv_paged_attention_decode(const pkv_cache_desc* cache, void* out, fl
   if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return PKV_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return PKV_ERR_INVALID_ARG;
-  if (partition_size == 0) partition_size = auto_partition(cache, num_seqs, max_blocks_per_seq);
   if (partition_size % cache->block_size != 0) return PKV_ERR_INVALID_ARG;
-  const int32_t bpp = partition_size / cache->block_size;
-  const int64_t parts = (max_blocks_per_seq + (int64_t)bpp - 1) / bpp;
-  if (parts > 65535) return PKV_ERR_UNSUPPORTED;
-  const size_t need = parts > 1 ? partial_bytes((int64_t)num_seqs * num_q_heads, parts,
-                                                cache->head_dim) : 0;
-  if (workspace_bytes < need || (need > 0 && !workspace)) return PKV_ERR_INVALID_ARG;
-  if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PKV_ERR_INVALID_ARG;
+  const int G = num_q_heads / cache->num_kv_heads;
+  const int64_t C = decode_ctas(cache, num_seqs, num_q_heads, max_blocks_per_seq, partition_size);
+  if (C > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  const DecodeWorkspace w = decode_workspace(num_seqs, C, G, cache->head_dim);
+  if (workspace_bytes < w.total || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return PKV_ERR_INVALID_ARG;
 
   const int rows = pkv::box_rows_for(cache->block_size);
   CUtensorMap tmk, tmv;
@@ -359,50 +393,61 @@ pkv_status pkv_paged_attention_decode(const pkv_cache_desc* cache, void* out, fl
   a.q = q;
   a.block_tables = block_tables;
   a.seq_lens = seq_lens;
-  const size_t rows_parts = (size_t)num_seqs * num_q_heads * (size_t)parts;
-  a.part_o = need ? static_cast<float*>(workspace) : nullptr;
-  a.part_lse = need ? reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) +
-                                               align256(rows_parts * cache->head_dim * 4))
-                    : nullptr;
   a.out = out;
   a.lse_out = lse;
   a.err = err;
+  bind_decode_workspace(&a, workspace, w);
   a.num_blocks = cache->num_blocks;
   a.max_blocks = max_blocks_per_seq;
   a.num_seqs = num_seqs;
   a.num_q_heads = num_q_heads;
   a.num_kv_heads = cache->num_kv_heads;
   a.block_size = cache->block_size;
-  a.blocks_per_part = bpp;
-  a.max_parts = (int32_t)parts;
-  a.part_offset = 0;
-  a.parts_stride = (int32_t)parts;
-  a.num_stages = pkv::decode_num_stages(cache->block_size, cache->head_dim, elem_bytes(cache->dtype));
+  a.num_ctas = (int32_t)C;
+  a.num_stages = pkv::decode_num_stages(cache->head_dim, elem_bytes(cache->dtype));
   a.qscale = scale * 1.4426950408889634f;
-  a.direct = parts <= 1 ? 1 : 0;
-  cudaError_t e = pkv::launch_paged_decode(cache->dtype, cache->head_dim,
-                                           num_q_heads / cache->num_kv_heads, tmk, tmv, a,
+  cudaError_t e = pkv::launch_paged_decode(cache->dtype, cache->head_dim, G, tmk, tmv, a,
                                            as_stream(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// Shared-prefix workspace: prefix states plus the suffix's whole-segment
+// state ([B, Hq, prefix splits + 1] x (D + 1) fp32), then the suffix
+// decode's plan and piece records.
+struct SharedWorkspace {
+  int32_t split_len, prefix_parts;
+  int64_t ctas;
+  size_t st_lse_off, dec_off, total;
+  DecodeWorkspace dec;
+};
+
+SharedWorkspace shared_workspace(const pkv_cache_desc* c, int32_t num_seqs, int32_t num_q_heads,
+                                 int32_t prefix_len, int32_t max_suffix_blocks,
+                                 int32_t partition_size) {
+  SharedWorkspace w{};
+  if (prefix_len > 0) {
+    w.split_len = prefix_split_len(c, num_seqs, num_q_heads, prefix_len);
+    w.prefix_parts = (prefix_len + w.split_len - 1) / w.split_len;
+  }
+  const int64_t rows = (int64_t)num_seqs * num_q_heads, stride = w.prefix_parts + 1;
+  w.st_lse_off = align256((size_t)(rows * stride * c->head_dim) * 4);
+  w.dec_off = states_bytes(rows, stride, c->head_dim);
+  w.ctas = decode_ctas(c, num_seqs, num_q_heads, max_suffix_blocks, partition_size);
+  w.dec = decode_workspace(num_seqs, w.ctas, num_q_heads / c->num_kv_heads, c->head_dim);
+  w.total = w.dec_off + w.dec.total;
+  return w;
 }
 
 size_t pkv_shared_prefix_workspace_bytes(const pkv_cache_desc* cache, int32_t num_seqs,
                                          int32_t num_q_heads, int32_t prefix_len,
                                          int32_t max_suffix_blocks, int32_t partition_size) {
   if (check_cache(cache) != PKV_OK || num_seqs <= 0 || num_q_heads <= 0 || max_suffix_blocks <= 0 ||
-      partition_size < 0 || check_prefix_shape(cache, num_q_heads, prefix_len) != PKV_OK)
+      partition_size < 0 || check_prefix_shape(cache, num_q_heads, prefix_len) != PKV_OK ||
+      partition_size % cache->block_size != 0)
     return 0;
-  if (partition_size == 0) partition_size = auto_partition(cache, num_seqs, max_suffix_blocks);
-  if (partition_size % cache->block_size != 0) return 0;
-  const int64_t bpp = partition_size / cache->block_size;
-  const int64_t suffix_parts = (max_suffix_blocks + bpp - 1) / bpp;
-  int64_t prefix_parts = 0;
-  if (prefix_len > 0) {
-    const int32_t sl = prefix_split_len(cache, num_seqs, num_q_heads, prefix_len);
-    prefix_parts = (prefix_len + sl - 1) / sl;
-  }
-  return partial_bytes((int64_t)num_seqs * num_q_heads, prefix_parts + suffix_parts,
-                       cache->head_dim);
+  return shared_workspace(cache, num_seqs, num_q_heads, prefix_len, max_suffix_blocks,
+                          partition_size)
+      .total;
 }
 
 pkv_status pkv_shared_prefix_attention(
@@ -423,39 +468,31 @@ pkv_status pkv_shared_prefix_attention(
     return PKV_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return PKV_ERR_INVALID_ARG;
-  if (partition_size == 0) partition_size = auto_partition(cache, num_seqs, max_suffix_blocks);
   if (partition_size % cache->block_size != 0) return PKV_ERR_INVALID_ARG;
-  const int32_t bpp = partition_size / cache->block_size;
-  const int64_t suffix_parts = (max_suffix_blocks + (int64_t)bpp - 1) / bpp;
-  int32_t split_len = 0, prefix_parts = 0;
-  if (prefix_len > 0) {
-    split_len = prefix_split_len(cache, num_seqs, num_q_heads, prefix_len);
-    prefix_parts = (prefix_len + split_len - 1) / split_len;
-  }
-  const int64_t parts = prefix_parts + suffix_parts;
-  if (suffix_parts > 65535 || parts > INT32_MAX) return PKV_ERR_UNSUPPORTED;
-  const size_t need = partial_bytes((int64_t)num_seqs * num_q_heads, parts, cache->head_dim);
-  if (workspace_bytes < need || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+  const SharedWorkspace w = shared_workspace(cache, num_seqs, num_q_heads, prefix_len,
+                                             max_suffix_blocks, partition_size);
+  if (w.ctas > INT32_MAX || w.prefix_parts >= INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  if (workspace_bytes < w.total || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return PKV_ERR_INVALID_ARG;
   const int G = num_q_heads / cache->num_kv_heads;
   unsigned int* err = device_error_word();
   if (!err) return PKV_ERR_CUDA;
-  const size_t rows_parts = (size_t)num_seqs * num_q_heads * (size_t)parts;
-  float* part_o = static_cast<float*>(workspace);
-  float* part_lse = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) +
-                                             align256(rows_parts * cache->head_dim * 4));
+  unsigned char* base = static_cast<unsigned char*>(workspace);
+  float* st_o = reinterpret_cast<float*>(base);
+  float* st_lse = reinterpret_cast<float*>(base + w.st_lse_off);
+  const int32_t stride = w.prefix_parts + 1;
   const float qscale = scale * 1.4426950408889634f;
   cudaStream_t s = as_stream(stream);
 
-  if (prefix_parts > 0) {
+  if (w.prefix_parts > 0) {
     CUtensorMap tmq;
     if ((st = encode_q_map_sw128(&tmq, q, num_seqs, num_q_heads, cache->head_dim, G,
                                  pkv::kPrefixRows / G)) != PKV_OK)
       return st;
     pkv::PrefixArgs pa{};
     pa.prefix_block_ids = prefix_block_ids;
-    pa.part_o = part_o;
-    pa.part_lse = part_lse;
+    pa.part_o = st_o;
+    pa.part_lse = st_lse;
     pa.err = err;
     pa.num_blocks = cache->num_blocks;
     pa.num_seqs = num_seqs;
@@ -463,13 +500,13 @@ pkv_status pkv_shared_prefix_attention(
     pa.num_kv_heads = cache->num_kv_heads;
     pa.block_size = cache->block_size;
     pa.prefix_len = prefix_len;
-    pa.split_len = split_len;
-    pa.parts_stride = (int32_t)parts;
+    pa.split_len = w.split_len;
+    pa.parts_stride = stride;
     pa.qscale = qscale;
     pa.lse_scale = 1.f;
     CUtensorMap ptk, ptv;
     if ((st = encode_prefix_maps(&ptk, &ptv, cache, k_cache, v_cache)) != PKV_OK) return st;
-    if (pkv::launch_prefix_attention(cache->head_dim, G, prefix_parts, tmq, ptk, ptv, pa, s) !=
+    if (pkv::launch_prefix_attention(cache->head_dim, G, w.prefix_parts, tmq, ptk, ptv, pa, s) !=
         cudaSuccess)
       return PKV_ERR_CUDA;
   }
@@ -482,24 +519,23 @@ pkv_status pkv_shared_prefix_attention(
   a.q = q;
   a.block_tables = suffix_block_tables;
   a.seq_lens = suffix_lens;
-  a.part_o = part_o;
-  a.part_lse = part_lse;
   a.out = out;
   a.lse_out = lse;
   a.err = err;
+  bind_decode_workspace(&a, base + w.dec_off, w.dec);
+  a.st_o = st_o;
+  a.st_lse = st_lse;
+  a.st_stride = stride;
+  a.st_slot = w.prefix_parts;
   a.num_blocks = cache->num_blocks;
   a.max_blocks = max_suffix_blocks;
   a.num_seqs = num_seqs;
   a.num_q_heads = num_q_heads;
   a.num_kv_heads = cache->num_kv_heads;
   a.block_size = cache->block_size;
-  a.blocks_per_part = bpp;
-  a.max_parts = (int32_t)suffix_parts;
-  a.part_offset = prefix_parts;
-  a.parts_stride = (int32_t)parts;
-  a.num_stages = pkv::decode_num_stages(cache->block_size, cache->head_dim, elem_bytes(cache->dtype));
+  a.num_ctas = (int32_t)w.ctas;
+  a.num_stages = pkv::decode_num_stages(cache->head_dim, elem_bytes(cache->dtype));
   a.qscale = qscale;
-  a.direct = 0;
   cudaError_t e = pkv::launch_paged_decode(cache->dtype, cache->head_dim, G, tmk, tmv, a, s);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
@@ -620,15 +656,13 @@ pkv_status pkv_paged_attention_decode_static(
     return PKV_ERR_INVALID_ARG;
   if ((st = check_attention_shape(cache, num_q_heads)) != PKV_OK) return st;
   if (num_seqs == 0) return PKV_OK;
-  if (partition_size == 0) partition_size = auto_partition(cache, num_seqs, max_blocks_per_seq);
   if (partition_size % cache->block_size != 0) return PKV_ERR_INVALID_ARG;
-  const int64_t bpp = partition_size / cache->block_size;
-  const int64_t parts = (max_blocks_per_seq + bpp - 1) / bpp;
-  const size_t need =
-      parts > 1 ? partial_bytes((int64_t)num_seqs * num_q_heads, parts, cache->head_dim) : 0;
+  const size_t need = pkv_decode_workspace_bytes(cache, num_seqs, num_q_heads, max_blocks_per_seq,
+                                                 partition_size);
+  if (need == 0) return PKV_ERR_INVALID_ARG;
   if (need > (size_t)PKV_STATIC_SCRATCH_BYTES) return PKV_ERR_CAPACITY;
-  void* scratch = need ? static_scratch_address() : nullptr;
-  if (need && !scratch) return PKV_ERR_CUDA;
+  void* scratch = static_scratch_address();
+  if (!scratch) return PKV_ERR_CUDA;
   return pkv_paged_attention_decode(cache, out, lse, q, k_cache, v_cache, block_tables,
                                     max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, scale,
                                     partition_size, scratch, need, stream);

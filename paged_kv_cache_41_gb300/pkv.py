@@ -25,7 +25,7 @@ EXPORTED = [
     "pkv_kv_append",
     "pkv_kv_block_copy",
     "pkv_decode_workspace_bytes",
-    "pkv_decode_auto_partition",
+    "pkv_decode_num_ctas",
     "pkv_paged_attention_decode",
     "pkv_paged_attention_decode_static",
     "pkv_shared_prefix_workspace_bytes",
@@ -68,8 +68,8 @@ def load_library():
     lib.pkv_kv_block_copy.argtypes = [dp, vp, vp, vp, i64, vp]
     lib.pkv_decode_workspace_bytes.restype = ctypes.c_size_t
     lib.pkv_decode_workspace_bytes.argtypes = [dp, i32, i32, i32, i32]
-    lib.pkv_decode_auto_partition.restype = i32
-    lib.pkv_decode_auto_partition.argtypes = [dp, i32, i32, i32]
+    lib.pkv_decode_num_ctas.restype = i32
+    lib.pkv_decode_num_ctas.argtypes = [dp, i32, i32, i32, i32]
     lib.pkv_paged_attention_decode.restype = ctypes.c_int
     lib.pkv_paged_attention_decode.argtypes = [dp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, f32,
                                                i32, vp, ctypes.c_size_t, vp]
@@ -152,10 +152,10 @@ def decode_workspace_bytes(k_cache, num_seqs, num_q_heads, max_blocks_per_seq,
                                                      max_blocks_per_seq, partition_size)
 
 
-def decode_auto_partition(k_cache, num_seqs, num_q_heads, max_blocks_per_seq) -> int:
+def decode_num_ctas(k_cache, num_seqs, num_q_heads, max_blocks_per_seq, partition_size=0) -> int:
     desc = cache_desc(k_cache)
-    return load_library().pkv_decode_auto_partition(ctypes.byref(desc), num_seqs, num_q_heads,
-                                                    max_blocks_per_seq)
+    return load_library().pkv_decode_num_ctas(ctypes.byref(desc), num_seqs, num_q_heads,
+                                              max_blocks_per_seq, partition_size)
 
 
 def paged_attention_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, *, out=None,
@@ -185,8 +185,8 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, *
 
 def paged_attention_decode_static(q, k_cache, v_cache, block_tables, seq_lens, scale, *,
                                   out=None, lse=None, partition_size=0, stream=None):
-    """Allocation-free paged decode: the split-K partial states use the
-    library's own fixed device array (include/pkv.h), so no workspace is
+    """Allocation-free paged decode: the decode's workspace is the library's
+    own fixed device array (include/pkv.h), so no workspace is
     passed and nothing is allocated by the call itself.  For callers that may
     not allocate device memory.  Raises PkvError (status PKV_ERR_CAPACITY) when
     the sizes need more than STATIC_SCRATCH_BYTES of scratch.  Calls that could
