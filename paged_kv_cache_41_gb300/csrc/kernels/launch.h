@@ -113,10 +113,13 @@ struct PrefixArgs {
 constexpr int kPrefixRows = 128;
 constexpr int kPrefixKeys = 128;
 
+// tmo: the state outputs part_o as a 5-D fp32 tensor (D, parts_stride, G,
+// Hkv, num_seqs) with 128-byte swizzle and a box of 32 columns x 1 x G x 1 x
+// 128 / G requests.
 cudaError_t launch_prefix_attention(int head_dim, int group, int num_splits,
                                     const CUtensorMap& tmq, const CUtensorMap& tmk,
-                                    const CUtensorMap& tmv, const PrefixArgs& args,
-                                    cudaStream_t stream);
+                                    const CUtensorMap& tmv, const CUtensorMap& tmo,
+                                    const PrefixArgs& args, cudaStream_t stream);
 size_t prefix_smem_bytes(int head_dim, int split_len, int block_size);
 
 // Stage count of the partial kernel's shared-memory ring.

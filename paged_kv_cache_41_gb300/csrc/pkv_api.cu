@@ -247,13 +247,32 @@ pkv_status encode_prefix_maps(CUtensorMap* tmk, CUtensorMap* tmv, const pkv_cach
   return st != PKV_OK ? st : encode_cache_map_sw128(tmv, c, v_cache, rows);
 }
 
-// Keys per prefix split: whole 128-key tiles, spread so that (split x query
-// tile x kv head) CTAs cover the SMs about once.
+// Prefix state outputs [B, Hq, parts_stride, D] fp32 as the 5-D tensor
+// (D, parts_stride, G, Hkv, B); one store box is 32 columns (128 bytes, the
+// swizzle span) of one split for the 128 rows (128 / G requests x G heads)
+// of a query tile.
+pkv_status encode_prefix_out_map(CUtensorMap* map, float* part_o, int32_t num_seqs,
+                                 int32_t num_kv_heads, int group, int32_t parts_stride,
+                                 int32_t head_dim) {
+  const cuuint64_t row = (cuuint64_t)head_dim * 4;
+  cuuint64_t dims[5] = {(cuuint64_t)head_dim, (cuuint64_t)parts_stride, (cuuint64_t)group,
+                        (cuuint64_t)num_kv_heads, (cuuint64_t)num_seqs};
+  cuuint64_t strides[4] = {row, row * parts_stride, row * parts_stride * group,
+                           row * parts_stride * group * num_kv_heads};
+  cuuint32_t box[5] = {32, 1, (cuuint32_t)group, 1, (cuuint32_t)(pkv::kPrefixRows / group)};
+  CUresult r = encode_tiled_cached(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, part_o, dims, strides,
+                                   box, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (r == CUDA_ERROR_NOT_INITIALIZED) return PKV_ERR_CUDA;
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_UNSUPPORTED;
+}
+
+// Keys per prefix split: whole 128-key tiles, spread so that (split x pair of
+// query tiles x kv head) CTAs cover the SMs about once.
 int32_t prefix_split_len(const pkv_cache_desc* c, int32_t num_seqs, int32_t num_q_heads,
                          int32_t prefix_len) {
   const int G = num_q_heads / c->num_kv_heads;
   const int64_t m_tiles = ((int64_t)num_seqs * G + pkv::kPrefixRows - 1) / pkv::kPrefixRows;
-  const int64_t pairs = m_tiles * c->num_kv_heads;
+  const int64_t pairs = (m_tiles + 1) / 2 * c->num_kv_heads;
   const int64_t tiles = (prefix_len + pkv::kPrefixKeys - 1) / pkv::kPrefixKeys;
   int64_t splits = (sm_count() + pairs / 2) / pairs;
   if (splits < 1) splits = 1;
@@ -504,10 +523,13 @@ pkv_status pkv_shared_prefix_attention(
     pa.parts_stride = stride;
     pa.qscale = qscale;
     pa.lse_scale = 1.f;
-    CUtensorMap ptk, ptv;
+    CUtensorMap ptk, ptv, pto;
     if ((st = encode_prefix_maps(&ptk, &ptv, cache, k_cache, v_cache)) != PKV_OK) return st;
-    if (pkv::launch_prefix_attention(cache->head_dim, G, w.prefix_parts, tmq, ptk, ptv, pa, s) !=
-        cudaSuccess)
+    if ((st = encode_prefix_out_map(&pto, st_o, num_seqs, cache->num_kv_heads, G, stride,
+                                    cache->head_dim)) != PKV_OK)
+      return st;
+    if (pkv::launch_prefix_attention(cache->head_dim, G, w.prefix_parts, tmq, ptk, ptv, pto, pa,
+                                     s) != cudaSuccess)
       return PKV_ERR_CUDA;
   }
 
@@ -591,10 +613,13 @@ pkv_status pkv_prefix_attention_states(const pkv_cache_desc* cache, float* state
   pa.parts_stride = (int32_t)splits;
   pa.qscale = scale * 1.4426950408889634f;
   pa.lse_scale = 0.6931471805599453f;
-  CUtensorMap ptk, ptv;
+  CUtensorMap ptk, ptv, pto;
   if ((st = encode_prefix_maps(&ptk, &ptv, cache, k_cache, v_cache)) != PKV_OK) return st;
-  cudaError_t e = pkv::launch_prefix_attention(cache->head_dim, G, (int)splits, tmq, ptk, ptv, pa,
-                                               as_stream(stream));
+  if ((st = encode_prefix_out_map(&pto, states_o, num_seqs, cache->num_kv_heads, G, (int32_t)splits,
+                                  cache->head_dim)) != PKV_OK)
+    return st;
+  cudaError_t e = pkv::launch_prefix_attention(cache->head_dim, G, (int)splits, tmq, ptk, ptv, pto,
+                                               pa, as_stream(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
