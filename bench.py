@@ -491,7 +491,8 @@ def run_shared(args, rank, world, local):
         "roofline": {"bound": "tensor", "kernel": "prefix_attention_kernel",
                      "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
                      "peak_kind": "measured bf16_tflops (burst, kernel timed alone)",
-                     "traffic": None, "algorithmic_flops_per_launch": flops},
+                     "traffic": kernel_traffic("prefix_tc.cu", "prefix_attention_shared.md"),
+                     "algorithmic_flops_per_launch": flops},
         "e2e": {"value": world * logical / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s (logical K/V)",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": n * 5,  # prefix states; prefix, plan, partial, reduce
