@@ -32,7 +32,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOADS = ("llama", "long_bs16", "long_bs64", "shared")
+WORKLOADS = ("llama", "long_bs16", "long_bs64", "shared", "churn")
 
 
 def parse():
@@ -160,6 +160,11 @@ def make_batch(name, device, seed_offset=0, batch=0):
         return wl.long_batch(device=device, block_size=16, seed=3 + seed_offset, batch=batch or 8)
     if name == "long_bs64":
         return wl.long_batch(device=device, block_size=64, seed=3 + seed_offset, batch=batch or 8)
+    if name == "churn":
+        # the lengths of the churn trace's first decode step, as a plain batch
+        step = next(wl.ChurnTrace(seed=4 + seed_offset, steps=1).run())
+        return wl.custom_batch(step.seq_lens, dtype="bf16", hq=32, hkv=8, d=128, p=16,
+                               seed=4 + seed_offset, device=device)
     raise ValueError(name)
 
 
@@ -501,6 +506,118 @@ def run_shared(args, rank, world, local):
     return res, sp
 
 
+# ------------------------------------------------------------------ churn trace
+def run_churn(args, rank, world, local):
+    """256 concurrent requests; each step appends one row per request, then
+    decodes.  Requests finish (geometric output lengths) and are replaced by
+    arrivals whose whole prompt is appended first (untimed, as prefill).  The
+    first W steps are warm-up; the next K are timed per step with CUDA events
+    around the step's append and around its decode."""
+    import torch
+    from paged_kv_cache_41_gb300 import pkv
+    from paged_kv_cache_41_gb300 import workloads as wl
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    pkv.load_library()
+    tr = wl.ChurnTrace(seed=4 + rank, steps=args.warmup + args.steps)
+    hkv, d, hq, p = 8, 128, 32, tr.block_size
+    shape = (tr.num_blocks, p, hkv, d)
+    kc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    gen = wl.make_generator(4 + rank, dev)
+    B = tr.concurrency
+    q = wl.randn((B, hq, d), "bf16", gen, dev)
+    out = torch.empty_like(q)
+    row = 2 * hkv * d * 2
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local)
+    t_app = t_dec = t_e2e = 0.0
+    kv_bytes = 0
+    h2d = d2h = 0
+    n_timed = 0
+    ws = None
+    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    for i, st in enumerate(tr.run()):
+        timed = i >= args.warmup
+        if i == args.warmup:
+            torch.cuda.synchronize()
+            barrier(world)
+            clocks.start()
+        if st.arrival_rows:
+            ak = wl.randn((st.arrival_rows, hkv, d), "bf16", gen, dev)
+            av = wl.randn((st.arrival_rows, hkv, d), "bf16", gen, dev)
+            pkv.kv_append(kc, vc, ak, av, torch.from_numpy(st.arrival_slots).to(dev))
+        nk = wl.randn((B, hkv, d), "bf16", gen, dev)
+        nv = wl.randn((B, hkv, d), "bf16", gen, dev)
+        h_slots = torch.from_numpy(st.step_slots).pin_memory()
+        h_bt = torch.from_numpy(st.block_tables).pin_memory()
+        h_sl = torch.from_numpy(st.seq_lens).pin_memory()
+        h_k, h_v = nk.cpu().pin_memory(), nv.cpu().pin_memory()
+        need = pkv.decode_workspace_bytes(kc, B, hq, h_bt.shape[1])
+        if ws is None or ws.numel() < need:
+            ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        # end to end: this step's inputs from pinned host memory, output back
+        ev[0].record(stream)
+        d_slots = h_slots.to(dev, non_blocking=True)
+        d_bt = h_bt.to(dev, non_blocking=True)
+        d_sl = h_sl.to(dev, non_blocking=True)
+        d_k = h_k.to(dev, non_blocking=True)
+        d_v = h_v.to(dev, non_blocking=True)
+        ev[1].record(stream)
+        pkv.kv_append(kc, vc, d_k, d_v, d_slots)
+        ev[2].record(stream)
+        pkv.paged_attention_decode(q, kc, vc, d_bt, d_sl, 1.0 / math.sqrt(d), out=out,
+                                   workspace=ws)
+        ev[3].record(stream)
+        h_out.copy_(out, non_blocking=True)
+        ev[4].record(stream)
+        if timed:
+            torch.cuda.synchronize()
+            t_app += ev[1].elapsed_time(ev[2])
+            t_dec += ev[2].elapsed_time(ev[3])
+            t_e2e += ev[0].elapsed_time(ev[4])
+            kv_bytes += int(st.seq_lens.astype(np.int64).sum()) * row
+            h2d += sum(t.numel() * t.element_size() for t in (h_slots, h_bt, h_sl, h_k, h_v))
+            d2h += h_out.numel() * h_out.element_size()
+            n_timed += 1
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    assert pkv.get_device_error() == 0
+    t_dec = all_max(t_dec, world)
+    t_app = all_max(t_app, world)
+    t_e2e = all_max(t_e2e, world)
+    peak, peak_kind = load_peaks()
+    achieved = kv_bytes / (t_dec * 1e-3) / 1e9
+    ms_step = (t_app + t_dec) / n_timed
+    res = {
+        "metric": "paged-decode KV GB/s (% of HBM peak) and decode rows/s at 1 GB300",
+        "value": world * achieved, "unit": "GB/s", "n_gpus": world, "steps": n_timed,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded churn trace: lognormal prompts, geometric outputs, N(0,1) q/k/v)",
+        "config": {"workload": "churn trace decode", "concurrency": B, "num_q_heads": hq,
+                   "num_kv_heads": hkv, "head_dim": d, "block_size": p,
+                   "pool_blocks": tr.num_blocks, "kv_bytes_timed": kv_bytes,
+                   "l2": "inputs larger than L2 (K/V read per step >> 129 MB)",
+                   "parallelism": f"replicas x{world} (sequences shard, no collective)"},
+        "rows_per_s": world * B * n_timed / ((t_app + t_dec) * 1e-3),
+        "pct_of_hbm_peak": 100.0 * achieved / peak,
+        "decode_ms": t_dec / n_timed, "append_ms": t_app / n_timed,
+        "roofline": {"bound": "hbm", "kernel": "decode_partial_kernel + decode_reduce_kernel",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": f"{peak_kind} hbm_gbs (copy)", "traffic": None,
+                     "algorithmic_bytes_per_launch": kv_bytes / max(1, n_timed)},
+        "e2e": {"value": world * kv_bytes / (t_e2e * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": t_e2e / n_timed, "h2d_bytes_per_step": h2d // max(1, n_timed),
+                "d2h_bytes_per_step": d2h // max(1, n_timed)},
+        "gpu_launches": n_timed * 3,  # append, partial, reduce
+        "clocks": clk,
+    }
+    return res, make_batch("churn", "cpu", seed_offset=rank)
+
+
 def kv_row_bytes_dims(hkv, d, elem):
     return 2 * hkv * d * elem
 
@@ -560,6 +677,10 @@ def main():
         res, sp = run_shared(args, rank, world, local)
         if rank == 0 and not args.no_cpu_baseline and world == 1:
             res["cpu_baseline"] = shared_cpu_baseline(sp, args.cpu_sample_seconds)
+    elif args.workload == "churn":
+        res, b = run_churn(args, rank, world, local)
+        if rank == 0 and not args.no_cpu_baseline and world == 1:
+            res["cpu_baseline"] = cpu_baseline(b, args.cpu_sample_seconds)
     else:
         res, b = run_pkv(args, rank, world, local)
         if rank == 0 and not args.no_cpu_baseline and world == 1:

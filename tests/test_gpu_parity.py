@@ -189,6 +189,60 @@ def test_host_validation_rejects_before_launch():
     assert pkv.get_device_error() == 0
 
 
+# ------------------------------------------------------------------ churn trace
+def test_churn_trace_small():
+    """A short churn trace: requests finish and arrivals take blocks from the
+    free FIFO, so stale rows of finished requests stay in the pool.  After
+    every step (arrival prompts, then one row per request) the pools must
+    equal the oracle's bit for bit, and every step's decode must match the
+    oracle, which derives every slot itself from that step's block tables."""
+    tr = wl.ChurnTrace(seed=44, concurrency=12, steps=10, median=60, sigma=1.0, cap=600,
+                       mean_out=4)
+    hkv, d, hq, p = 2, 64, 8, tr.block_size
+    B = tr.concurrency
+    shape = (tr.num_blocks, p, hkv, d)
+    kc = torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    hk = np.full(shape, 0x7FC0, np.uint16)
+    hv = np.full(shape, 0x7FC0, np.uint16)
+    gen = wl.make_generator(44, "cuda")
+    q = wl.randn((B, hq, d), "bf16", gen, "cuda")
+    qh = wl.to_numpy_storage(q)
+    scale = 1.0 / np.sqrt(d)
+    arrivals = 0
+    for step in tr.run():
+        if step.arrival_rows:
+            arrivals += 1
+            ak = wl.randn((step.arrival_rows, hkv, d), "bf16", gen, "cuda")
+            av = wl.randn((step.arrival_rows, hkv, d), "bf16", gen, "cuda")
+            pkv.kv_append(kc, vc, ak, av, torch.from_numpy(step.arrival_slots).cuda())
+            slots = np.array([oracle.slot_for_position(step.block_tables[i], p, int(pos))
+                              for i, pos in zip(step.arrival_seq_index, step.arrival_positions)],
+                             np.int64)
+            assert oracle.kv_append(hk, hv, wl.to_numpy_storage(ak), wl.to_numpy_storage(av),
+                                    slots) == oracle.OK
+        nk = wl.randn((B, hkv, d), "bf16", gen, "cuda")
+        nv = wl.randn((B, hkv, d), "bf16", gen, "cuda")
+        pkv.kv_append(kc, vc, nk, nv, torch.from_numpy(step.step_slots).cuda())
+        slots = np.array([oracle.slot_for_position(step.block_tables[i], p,
+                                                   int(step.seq_lens[i]) - 1)
+                          for i in range(B)], np.int64)
+        assert oracle.kv_append(hk, hv, wl.to_numpy_storage(nk), wl.to_numpy_storage(nv),
+                                slots) == oracle.OK
+        bt = torch.from_numpy(step.block_tables).cuda()
+        sl = torch.from_numpy(step.seq_lens).cuda()
+        lse = torch.empty(B, hq, dtype=torch.float32, device="cuda")
+        out = pkv.paged_attention_decode(q, kc, vc, bt, sl, scale, lse=lse)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+        assert pu.pools_equal_bytes(kc, hk) and pu.pools_equal_bytes(vc, hv)
+        ref, ref_lse = oracle.paged_decode(qh, hk, hv, step.block_tables, step.seq_lens, scale,
+                                           nthreads=pu.NTHREADS)
+        pu.assert_close(out.float().cpu().numpy(), ref, "churn out")
+        pu.assert_close(lse.cpu().numpy(), ref_lse, "churn lse")
+    assert arrivals >= 3  # the trace did churn
+
+
 # ------------------------------------------------------------------ shared prefix
 def _shared_prefix_run(sp, rows=None, suffix_lens=None, partition_size=0):
     """Device: append parent rows, CoW copies, child rows, then the shared-prefix
