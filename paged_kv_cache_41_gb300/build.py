@@ -24,12 +24,14 @@ CUDA_SOURCES = [
     "pkv_api.cu",
     "kernels/append_copy.cu",
     "kernels/decode.cu",
+    "kernels/decode_tc.cu",
     "kernels/prefix_tc.cu",
 ]
 # Attention kernels take exp2/log2/division from the hardware approximations
 # (softmax in base 2, well inside the attention tolerance).
 PER_SOURCE_FLAGS = {
     "kernels/decode.cu": ["--use_fast_math"],
+    "kernels/decode_tc.cu": ["--use_fast_math"],
     "kernels/prefix_tc.cu": ["--use_fast_math"],
 }
 

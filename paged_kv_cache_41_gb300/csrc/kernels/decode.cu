@@ -46,6 +46,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "plan.cuh"
 
 namespace pkv {
 
@@ -54,8 +55,6 @@ constexpr int kDecodeThreads = kConsumerWarps * 32;
 constexpr int kChunk = 16;             // token rows per softmax update
 constexpr float kRescaleLog2 = 8.0f;   // move the exponent base past 2^8 growth
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kPlanPer = 8;           // sequences per thread per pass of the length scan
-constexpr int kPlanChunk = kDecodeThreads * kPlanPer;
 
 // Stage descriptor flags.
 constexpr int kPieceStart = 1;   // first stage of a piece: reset the state, load q
@@ -93,13 +92,6 @@ int decode_num_stages(int head_dim, int elem_bytes) {
   if (ns < 2) ns = 2;
   if (ns > 8) ns = 8;
   return ns;
-}
-
-// Stages per CTA: CTA c streams stages [c w, min((c + 1) w, S)) with
-// w = ceil(S / C), so only trailing CTAs can be empty and stage p belongs to
-// CTA p / w.
-__host__ __device__ __forceinline__ long long stages_per_cta(long long S, int C) {
-  return (S + C - 1) / C;
 }
 
 // One 16-row chunk of a stage for one consumer warp: rows row0 and row0 + 1
@@ -202,8 +194,8 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
   constexpr int NV = 2 * G;    // (row, head) partial sums per lane per chunk
   static_assert(NV <= 16 && (NV & (NV - 1)) == 0, "group must be 1, 2, 4 or 8");
 
-  const int c = blockIdx.x, C = a.num_ctas;
-  const int Hkv = a.num_kv_heads, B = a.num_seqs, P = a.block_size;
+  const int c = blockIdx.x;
+  const int Hkv = a.num_kv_heads, P = a.block_size;
   const int TB = box_rows_for(P);  // rows per TMA box
   const DecodeSmem L = decode_smem_layout(D, (int)sizeof(T), G, a.num_stages);
   const int NS = a.num_stages;
@@ -224,90 +216,10 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---------------------------------------------------------------- plan
-  // Every CTA scans the lengths: stages per sequence ceil(T / 32), their
-  // total S (times Hkv), its own range, and the (sequence, kv head, stage)
-  // of its first stage.  CTA 0 also stores the exclusive prefix of stages per
-  // sequence for the reduction and reports bad lengths.  The scan runs in
-  // passes of kPlanChunk sequences, kPlanPer consecutive ones per thread.
-  long long* wsum = reinterpret_cast<long long*>(scratch);  // [4] warp totals, then the start
-  auto scan_chunk = [&](int base, int (&nt)[kPlanPer], long long& excl, long long& total,
-                        bool report) {
-    long long mine = 0;
-#pragma unroll
-    for (int j = 0; j < kPlanPer; ++j) {
-      const int r = base + threadIdx.x * kPlanPer + j;
-      nt[j] = r < B ? (effective_len(__ldg(a.seq_lens + r), a.max_blocks, P, a.err, report) +
-                       kStageRows - 1) / kStageRows
-                    : 0;
-      mine += nt[j];
-    }
-    long long x = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) wsum[warp] = x;
-    __syncthreads();
-    long long before = 0;
-    total = 0;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      const long long t = wsum[w];
-      if (w < warp) before += t;
-      total += t;
-    }
-    excl = before + x - mine;
-    __syncthreads();  // wsum is rewritten by the next pass
-  };
-  long long carry = 0;
-  for (int base = 0; base < B; base += kPlanChunk) {
-    int nt[kPlanPer];
-    long long excl, total;
-    scan_chunk(base, nt, excl, total, c == 0);
-    if (c == 0) {
-      long long p = carry + excl;
-#pragma unroll
-      for (int j = 0; j < kPlanPer; ++j) {
-        const int r = base + threadIdx.x * kPlanPer + j;
-        if (r < B) a.plan_pre[r] = p;
-        p += nt[j];
-      }
-    }
-    carry += total;
-  }
-  if (c == 0 && threadIdx.x == 0) a.plan_pre[B] = carry;
-  const long long S = carry * Hkv;
-  const long long wct = stages_per_cta(S, C);
-  const long long p0 = min((long long)c * wct, S);
-  const int n = (int)(min(p0 + wct, S) - p0);
+  int4 d0;
+  const int n = plan_cta_stages<kDecodeThreads, kStageRows>(
+      a, reinterpret_cast<long long*>(scratch), &d0);
   if (n <= 0) return;  // no stages: the whole CTA leaves before any barrier
-  // the sequence holding stage p0, found in a second pass
-  int* start = reinterpret_cast<int*>(wsum + kConsumerWarps);
-  carry = 0;
-  for (int base = 0; base < B; base += kPlanChunk) {
-    int nt[kPlanPer];
-    long long excl, total;
-    scan_chunk(base, nt, excl, total, false);
-    if (p0 < (carry + total) * Hkv) {
-      long long p = carry + excl;
-#pragma unroll
-      for (int j = 0; j < kPlanPer; ++j) {
-        if (nt[j] > 0 && p * Hkv <= p0 && p0 < (p + nt[j]) * Hkv) {
-          const long long off = p0 - p * Hkv;
-          start[0] = base + threadIdx.x * kPlanPer + j;
-          start[1] = (int)(off / nt[j]);
-          start[2] = (int)(off % nt[j]);
-        }
-        p += nt[j];
-      }
-      __syncthreads();
-      break;
-    }
-    carry += total;
-  }
-  const int4 d0 = make_int4(start[0], start[1], start[2], 0);
-  __syncthreads();  // the scratch is the consumers' from here on
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -693,6 +605,15 @@ static cudaError_t launch_reduce_t(const DecodeArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_decode_reduce(int dtype, int head_dim, const DecodeArgs& a,
+                                 cudaStream_t stream) {
+  if (dtype == PKV_BF16)
+    return head_dim == 128 ? launch_reduce_t<__nv_bfloat16, 128>(a, stream)
+                           : launch_reduce_t<__nv_bfloat16, 64>(a, stream);
+  return head_dim == 128 ? launch_reduce_t<float, 128>(a, stream)
+                         : launch_reduce_t<float, 64>(a, stream);
+}
+
 cudaError_t launch_paged_decode(int dtype, int head_dim, int group, const CUtensorMap& tmk,
                                 const CUtensorMap& tmv, const DecodeArgs& a,
                                 cudaStream_t stream) {
@@ -704,11 +625,7 @@ cudaError_t launch_paged_decode(int dtype, int head_dim, int group, const CUtens
     e = head_dim == 128 ? dispatch_group<float, 128>(group, tmk, tmv, a, stream)
                         : dispatch_group<float, 64>(group, tmk, tmv, a, stream);
   if (e != cudaSuccess) return e;
-  if (dtype == PKV_BF16)
-    return head_dim == 128 ? launch_reduce_t<__nv_bfloat16, 128>(a, stream)
-                           : launch_reduce_t<__nv_bfloat16, 64>(a, stream);
-  return head_dim == 128 ? launch_reduce_t<float, 128>(a, stream)
-                         : launch_reduce_t<float, 64>(a, stream);
+  return launch_decode_reduce(dtype, head_dim, a, stream);
 }
 
 }  // namespace pkv

@@ -89,6 +89,23 @@ cudaError_t launch_paged_decode(int dtype, int head_dim, int group, const CUtens
 // CTAs of one wave of the partial kernel (resident CTAs per SM x SMs).
 int decode_resident_ctas(int dtype, int head_dim, int group);
 
+// The LSE reduction of cut segments (and, in states mode, extra states).
+cudaError_t launch_decode_reduce(int dtype, int head_dim, const DecodeArgs& args,
+                                 cudaStream_t stream);
+
+// Tensor-core decode for eight query heads per kv head (decode_tc.cu): bf16,
+// head_dim 128, block sizes dividing 128 or multiples of it.  Stages are
+// decode_tc_rows() rows; one CTA per SM.  tmk / tmv: 128-byte-swizzled maps
+// whose box is 64 columns x 1 head x min(P, 128) rows x 1 block; tmq: a
+// 128-byte-swizzled map over q [B, Hq, D] whose box is 64 columns x 8 heads
+// x 1 request.  Launches the reduction too.
+bool decode_tc_supported(int dtype, int head_dim, int group, int block_size);
+int decode_tc_rows();
+int decode_tc_resident_ctas();
+cudaError_t launch_paged_decode_tc(const CUtensorMap& tmk, const CUtensorMap& tmv,
+                                   const CUtensorMap& tmq, const DecodeArgs& args,
+                                   cudaStream_t stream);
+
 // Arguments of the shared-prefix tensor-core kernel.  Grid: (key split,
 // 128-row query tile, kv head).  Its states go to slots [0, num_splits) of
 // [B, Hq, parts_stride] state arrays.

@@ -158,11 +158,23 @@ int sm_count() {
   return n;
 }
 
-// Stages (kStageRows rows of one kv head) in the decode work list at most:
-// every (sequence, kv head) at max_blocks * P rows.
-int64_t max_decode_stages(const pkv_cache_desc* c, int32_t num_seqs, int32_t max_blocks) {
+// Whether the decode runs on the tensor cores (eight query heads per kv
+// head) or on the CUDA cores, and the rows of one stage of its work list.
+bool use_tc_decode(const pkv_cache_desc* c, int group) {
+  return pkv::decode_tc_supported(c->dtype, c->head_dim, group, c->block_size);
+}
+
+int decode_stage_rows(const pkv_cache_desc* c, int group) {
+  return use_tc_decode(c, group) ? pkv::decode_tc_rows() : pkv::kStageRows;
+}
+
+// Stages in the decode work list at most: every (sequence, kv head) at
+// max_blocks * P rows.
+int64_t max_decode_stages(const pkv_cache_desc* c, int group, int32_t num_seqs,
+                          int32_t max_blocks) {
   const int64_t rows = (int64_t)max_blocks * c->block_size;
-  return (int64_t)num_seqs * c->num_kv_heads * ((rows + pkv::kStageRows - 1) / pkv::kStageRows);
+  const int sr = decode_stage_rows(c, group);
+  return (int64_t)num_seqs * c->num_kv_heads * ((rows + sr - 1) / sr);
 }
 
 // CTAs of the persistent decode kernel: one wave of resident CTAs (fewer
@@ -171,12 +183,14 @@ int64_t max_decode_stages(const pkv_cache_desc* c, int32_t num_seqs, int32_t max
 int64_t decode_ctas(const pkv_cache_desc* c, int32_t num_seqs, int32_t num_q_heads,
                     int32_t max_blocks, int32_t partition_size) {
   const int G = num_q_heads / c->num_kv_heads;
-  int64_t resident = pkv::decode_resident_ctas(c->dtype, c->head_dim, G);
-  if (resident <= 0) resident = 4LL * sm_count();
-  const int64_t smax = max_decode_stages(c, num_seqs, max_blocks);
+  const bool tc = use_tc_decode(c, G);
+  int64_t resident = tc ? pkv::decode_tc_resident_ctas()
+                        : pkv::decode_resident_ctas(c->dtype, c->head_dim, G);
+  if (resident <= 0) resident = (tc ? 1LL : 4LL) * sm_count();
+  const int64_t smax = max_decode_stages(c, G, num_seqs, max_blocks);
   int64_t C = resident < smax ? resident : smax;
   if (partition_size > 0) {
-    int64_t cap = partition_size / pkv::kStageRows;
+    int64_t cap = partition_size / decode_stage_rows(c, G);
     if (cap < 1) cap = 1;
     const int64_t need = (smax + cap - 1) / cap;
     if (need > C) C = need;
@@ -184,6 +198,37 @@ int64_t decode_ctas(const pkv_cache_desc* c, int32_t num_seqs, int32_t num_q_hea
   const int64_t fit = (smax + (1LL << 30) - 1) >> 30;  // stages per CTA fit an int
   if (fit > C) C = fit;
   return C < 1 ? 1 : C;
+}
+
+pkv_status encode_q_map_sw128(CUtensorMap* map, const void* q, int32_t num_seqs,
+                              int32_t num_q_heads, int32_t head_dim, int group, int rpb);
+pkv_status encode_cache_map_sw128(CUtensorMap* map, const pkv_cache_desc* c, const void* base,
+                                  int rows);
+
+// Encode the maps and launch the decode (partial kernel + reduction) on the
+// path use_tc_decode picks.
+pkv_status launch_decode(const pkv_cache_desc* cache, int G, const void* q, const void* k_cache,
+                         const void* v_cache, const pkv::DecodeArgs& a, cudaStream_t stream) {
+  pkv_status st;
+  CUtensorMap tmk, tmv;
+  cudaError_t e;
+  if (use_tc_decode(cache, G)) {
+    const int rows = cache->block_size < pkv::decode_tc_rows() ? cache->block_size
+                                                               : pkv::decode_tc_rows();
+    CUtensorMap tmq;
+    if ((st = encode_cache_map_sw128(&tmk, cache, k_cache, rows)) != PKV_OK) return st;
+    if ((st = encode_cache_map_sw128(&tmv, cache, v_cache, rows)) != PKV_OK) return st;
+    if ((st = encode_q_map_sw128(&tmq, q, a.num_seqs, a.num_q_heads, cache->head_dim, G, 1)) !=
+        PKV_OK)
+      return st;
+    e = pkv::launch_paged_decode_tc(tmk, tmv, tmq, a, stream);
+  } else {
+    const int rows = pkv::box_rows_for(cache->block_size);
+    if ((st = encode_cache_map(&tmk, cache, k_cache, rows)) != PKV_OK) return st;
+    if ((st = encode_cache_map(&tmv, cache, v_cache, rows)) != PKV_OK) return st;
+    e = pkv::launch_paged_decode(cache->dtype, cache->head_dim, G, tmk, tmv, a, stream);
+  }
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 // Decode workspace: stage prefix [B + 1] int64, piece LSEs [2C, G] and piece
@@ -401,10 +446,6 @@ pkv_status pkv_paged_attention_decode(const pkv_cache_desc* cache, void* out, fl
   if (workspace_bytes < w.total || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return PKV_ERR_INVALID_ARG;
 
-  const int rows = pkv::box_rows_for(cache->block_size);
-  CUtensorMap tmk, tmv;
-  if ((st = encode_cache_map(&tmk, cache, k_cache, rows)) != PKV_OK) return st;
-  if ((st = encode_cache_map(&tmv, cache, v_cache, rows)) != PKV_OK) return st;
   unsigned int* err = device_error_word();
   if (!err) return PKV_ERR_CUDA;
 
@@ -425,9 +466,7 @@ pkv_status pkv_paged_attention_decode(const pkv_cache_desc* cache, void* out, fl
   a.num_ctas = (int32_t)C;
   a.num_stages = pkv::decode_num_stages(cache->head_dim, elem_bytes(cache->dtype));
   a.qscale = scale * 1.4426950408889634f;
-  cudaError_t e = pkv::launch_paged_decode(cache->dtype, cache->head_dim, G, tmk, tmv, a,
-                                           as_stream(stream));
-  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return launch_decode(cache, G, q, k_cache, v_cache, a, as_stream(stream));
 }
 
 // Shared-prefix workspace: prefix states plus the suffix's whole-segment
@@ -533,10 +572,6 @@ pkv_status pkv_shared_prefix_attention(
       return PKV_ERR_CUDA;
   }
 
-  const int rows = pkv::box_rows_for(cache->block_size);
-  CUtensorMap tmk, tmv;
-  if ((st = encode_cache_map(&tmk, cache, k_cache, rows)) != PKV_OK) return st;
-  if ((st = encode_cache_map(&tmv, cache, v_cache, rows)) != PKV_OK) return st;
   pkv::DecodeArgs a{};
   a.q = q;
   a.block_tables = suffix_block_tables;
@@ -558,8 +593,7 @@ pkv_status pkv_shared_prefix_attention(
   a.num_ctas = (int32_t)w.ctas;
   a.num_stages = pkv::decode_num_stages(cache->head_dim, elem_bytes(cache->dtype));
   a.qscale = qscale;
-  cudaError_t e = pkv::launch_paged_decode(cache->dtype, cache->head_dim, G, tmk, tmv, a, s);
-  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return launch_decode(cache, G, q, k_cache, v_cache, a, s);
 }
 
 int32_t pkv_prefix_split_len(const pkv_cache_desc* cache, int32_t num_seqs, int32_t num_q_heads,

@@ -66,6 +66,28 @@ def test_edge_lengths(dtype, d, hq, hkv, p, partition_size):
     _run_batch(b, partition_size=ps)
 
 
+# Eight query heads per kv head run on the tensor cores (128-row stages);
+# these cover every block size that path takes, ragged and empty lengths,
+# pieces cut at every stage boundary, and the NaN-poisoned stale rows.
+G8_LENS = [1, 127, 128, 129, 255, 0, 700, 16, 2000, 33]
+
+
+@pytest.mark.parametrize("p", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("partition_size", [0, 128, 384, "whole"])
+def test_gqa8_tensor_core_decode(p, partition_size):
+    b = wl.custom_batch(G8_LENS, dtype="bf16", hq=64, hkv=8, d=128, p=p, seed=61, device="cuda")
+    ps = b.max_blocks * p if partition_size == "whole" else partition_size
+    if ps % p:
+        ps = p * ((ps + p - 1) // p)
+    _run_batch(b, partition_size=ps)
+
+
+def test_gqa8_tensor_core_decode_long_sampled():
+    lens = np.array([40000, 3000, 65536, 1], np.int32)
+    b = wl.custom_batch(lens, dtype="bf16", hq=32, hkv=4, d=128, p=16, seed=62, device="cuda")
+    _run_batch(b, rows=np.array([0, 2, 3]))
+
+
 def test_empty_batch_rows_and_all_empty():
     b = wl.custom_batch([0, 0, 5], dtype="bf16", hq=8, hkv=2, d=128, p=16, seed=5, device="cuda")
     _run_batch(b)
@@ -291,6 +313,7 @@ def _shared_prefix_run(sp, rows=None, suffix_lens=None, partition_size=0):
 
 @pytest.mark.parametrize("batch,prefix,hq,hkv,d", [
     (16, 256, 32, 8, 128), (5, 384, 8, 2, 128), (40, 128, 16, 16, 64), (3, 512, 16, 2, 128),
+    (24, 256, 64, 8, 128),  # eight heads per kv head: the suffixes decode on the tensor cores
     # 2, 3 (padded to 4) and 5 (padded to 8) query tiles: clusters of 2 and 4 CTAs
     (50, 256, 32, 8, 128), (80, 384, 32, 8, 128), (150, 256, 32, 8, 64),
 ])
