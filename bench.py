@@ -32,7 +32,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOADS = ("llama", "long_bs16", "long_bs64", "shared", "churn")
+WORKLOADS = ("llama", "long_bs16", "long_bs64", "shared", "churn", "gqa8")
 
 
 def parse():
@@ -160,6 +160,14 @@ def make_batch(name, device, seed_offset=0, batch=0):
         return wl.long_batch(device=device, block_size=16, seed=3 + seed_offset, batch=batch or 8)
     if name == "long_bs64":
         return wl.long_batch(device=device, block_size=64, seed=3 + seed_offset, batch=batch or 8)
+    if name == "gqa8":
+        # the Llama-shaped lengths with eight query heads per kv head (64 / 8)
+        rng = np.random.default_rng(2 + seed_offset)
+        lens = rng.integers(512, 8192, size=batch or 64, endpoint=True)
+        b = wl.custom_batch(lens, dtype="bf16", hq=64, hkv=8, d=128, p=16, seed=2 + seed_offset,
+                            device=device)
+        b.name = "gqa8"
+        return b
     if name == "churn":
         # the lengths of the churn trace's first decode step, as a plain batch
         step = next(wl.ChurnTrace(seed=4 + seed_offset, steps=1).run())
@@ -333,7 +341,9 @@ def run_pkv(args, rank, world, local):
 
     peak, peak_kind = load_peaks()
     achieved = kv_bytes / (decode_ms * 1e-3) / 1e9
-    traffic = kernel_traffic("decode.cu", "decode_partial_llama.md") if args.workload == "llama" else None
+    traffic = (kernel_traffic("decode.cu", "decode_partial_llama.md") if args.workload == "llama"
+               else kernel_traffic("decode_tc.cu", "decode_tc_gqa8.md")
+               if args.workload == "gqa8" else None)
     res = {
         "metric": "paged-decode KV GB/s (% of HBM peak) and decode rows/s at 1 GB300",
         "value": world * kv_bytes / (ms_step * 1e-3) / 1e9,
@@ -350,7 +360,9 @@ def run_pkv(args, rank, world, local):
         "config": {
             "workload": {"llama": "llama3-8b-shaped decode layer",
                          "long_bs16": "long-context decode, block size 16",
-                         "long_bs64": "long-context decode, block size 64"}[args.workload],
+                         "long_bs64": "long-context decode, block size 64",
+                         "gqa8": "decode layer with 8 query heads per kv head (64/8)"
+                         }[args.workload],
             "batch": B, "num_q_heads": b.num_q_heads, "num_kv_heads": b.num_kv_heads,
             "head_dim": b.head_dim, "block_size": b.block_size,
             "seq_len_min": int(b.seq_lens.min()), "seq_len_max": int(b.seq_lens.max()),
@@ -365,7 +377,8 @@ def run_pkv(args, rank, world, local):
         "decode_ms": decode_ms,
         "append_ms": append_ms,
         "roofline": {"bound": "hbm",
-                     "kernel": "decode_plan_kernel + decode_partial_kernel + decode_reduce_kernel",
+                     "kernel": ("decode_tc_kernel" if args.workload == "gqa8"
+                                else "decode_partial_kernel") + " + decode_reduce_kernel",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs (copy)",
                      "traffic": traffic,
