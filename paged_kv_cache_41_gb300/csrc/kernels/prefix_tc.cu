@@ -98,11 +98,12 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
   unsigned char* ks = qs + 2 * kTile;      // two stages
   unsigned char* vs = ks + 2 * kTile;      // two stages
   unsigned char* ps = vs + 2 * kTile;      // 128 rows x 128 keys bf16 (two halves)
-  // qbar: Q by TMA; kfull/vfull: a producer filled a stage; kfree/vfree: the
-  // MMAs that read a stage completed; sfull[x]: QK^T of tile x done; pfull[x]:
-  // tile x's softmax wrote P; ofull[x]: PV of tile x done; pfree: a PV read P.
-  __shared__ uint64_t qbar, kfull[2], vfull[2], kfree[2], vfree[2], sfull[2], pfull[2], ofull[2],
-      pfree;
+  // qbar[x]: Q of tile x by TMA; kfull/vfull: a producer filled a stage;
+  // kfree/vfree: the MMAs that read a stage completed; sfull[x]: QK^T of tile
+  // x done; pfull[x]: tile x's softmax wrote P; ofull[x]: PV of tile x done;
+  // pfree: a PV read P.
+  __shared__ uint64_t qbar[2], kfull[2], vfull[2], kfree[2], vfree[2], sfull[2], pfull[2],
+      ofull[2], pfree;
   __shared__ uint32_t tmem_base;
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -124,8 +125,8 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     box1 = box_block(1);
   }
   if (t == 0) {
-    mbar_init(&qbar, 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&qbar[i], 1);
       mbar_init(&kfull[i], 1);
       mbar_init(&vfull[i], 1);
       mbar_init(&kfree[i], 1);
@@ -136,19 +137,22 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     }
     mbar_init(&pfree, 1);
     fence_barrier_init();
-    // Q needs no block ids: start it before anything else
+    // tile A's Q needs no block ids: start it before anything else (tile B's
+    // follows the first K tile, from the producer)
     prefetch_tensormap(&tmq);
-    mbar_arrive_expect_tx(&qbar, (hasB ? 2u : 1u) * kTile);
-    for (int x = 0; x < (hasB ? 2 : 1); ++x)
+    mbar_arrive_expect_tx(&qbar[0], kTile);
 #pragma unroll
-      for (int h = 0; h < H; ++h)
-        tma_load_3d(qs + x * kTile + h * kHalfBytes, &tmq, h * 64, kvh * G, (2 * mp + x) * RPB,
-                    &qbar);
+    for (int h = 0; h < H; ++h)
+      tma_load_3d(qs + h * kHalfBytes, &tmq, h * 64, kvh * G, 2 * mp * RPB, &qbar[0]);
   }
+  __syncthreads();  // barriers initialised: the producer starts streaming now
+  // Every warp but the producer waits for the TMEM allocation.
   if (warp == 0) tc::tmem_alloc(&tmem_base, 512);
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
+  if (warp != 9) {
+    tc::fence_before_sync();
+    named_barrier_sync(3, kPrefixThreads - 32);
+    tc::fence_after_sync();
+  }
   const uint32_t tmem = tmem_base;  // S_A, S_B at columns 0, 128; O_A, O_B at 256, 384
 
   if (warp == 9) {
@@ -162,6 +166,7 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
       prefetch_tensormap(&tmk);
       prefetch_tensormap(&tmv);
     }
+    __syncwarp();
     int2 bn = box1;  // tile jt + 1
     int blk = box0.x, row = box0.y;  // tile jt
     for (int jt = 0; jt < J; ++jt) {
@@ -185,6 +190,13 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
         if (lane < nbox)
           tma_load_4d((kv ? vs : ks) + st * kTile + hcol * kHalfBytes + bsub * PB * 128,
                       kv ? &tmv : &tmk, hcol * 64, kvh, row, blk, &fullb[st]);
+        if (jt == 0 && kv == 0 && hasB && lane == 0) {  // tile B's Q, after the first K tile
+          mbar_arrive_expect_tx(&qbar[1], kTile);
+#pragma unroll
+          for (int h = 0; h < H; ++h)
+            tma_load_3d(qs + kTile + h * kHalfBytes, &tmq, h * 64, kvh * G, (2 * mp + 1) * RPB,
+                        &qbar[1]);
+        }
       }
       if (!ok) break;
       blk = bn.x;
@@ -195,6 +207,7 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     // ============================================================ MMA issue
     if (lane == 0) {
       auto issue_qk = [&](int x, int jt) -> bool {
+        if (jt == 0 && !mbar_wait(&qbar[x], 0)) return false;
         if (!mbar_wait(&kfull[jt & 1], (jt >> 1) & 1)) return false;
         tc::fence_after_sync();
         const uint32_t kb = smem_u32(ks + (jt & 1) * kTile), qb = smem_u32(qs + x * kTile);
@@ -226,7 +239,7 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
         if (x == 1 || !hasB) tc::commit(&vfree[jt & 1]);
         return true;
       };
-      bool ok = mbar_wait(&qbar, 0) && issue_qk(0, 0) && (!hasB || issue_qk(1, 0));
+      bool ok = issue_qk(0, 0) && (!hasB || issue_qk(1, 0));
       for (int j = 0; j < J && ok; ++j) {
         ok = issue_pv(0, j) && (j + 1 >= J || issue_qk(0, j + 1));
         if (ok && hasB) ok = issue_pv(1, j) && (j + 1 >= J || issue_qk(1, j + 1));
