@@ -21,6 +21,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint4* __restrict__ kc,
                                                         const int64_t* __restrict__ slots,
                                                         int64_t num_tokens, int64_t num_slots,
                                                         int64_t row_vecs, unsigned int* err) {
+  pdl_launch_dependents();  // a decode after this append may be scheduled now
   const int64_t tok = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x / 32);
   const int lane = threadIdx.x & 31;
   if (tok >= num_tokens) return;

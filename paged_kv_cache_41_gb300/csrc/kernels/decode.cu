@@ -216,6 +216,8 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---------------------------------------------------------------- plan
+  pdl_wait();                // inputs written by earlier kernels are visible
+  pdl_launch_dependents();   // the reduction may be scheduled as CTAs retire
   int4 d0;
   const int n = plan_cta_stages<kDecodeThreads, kStageRows>(
       a, reinterpret_cast<long long*>(scratch), &d0);
@@ -461,6 +463,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
 template <typename T, int D>
 __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) {
   constexpr int EPL = D / 32;
+  pdl_wait();  // the partial kernel's records and plan are complete
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t rh = (int64_t)blockIdx.x * 4 + warp;
   if (rh >= (int64_t)a.num_seqs * a.num_q_heads) return;
@@ -539,8 +542,8 @@ static cudaError_t launch_partial(const CUtensorMap& tmk, const CUtensorMap& tmv
   static SmemAttrCache attr_cache;
   cudaError_t e = ensure_smem_limit(kern, (int)smem, attr_cache);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)a.num_ctas, kDecodeThreads, smem, stream>>>(tmk, tmv, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3((unsigned)a.num_ctas), dim3(kDecodeThreads), smem, stream, tmk, tmv,
+                    a);
 }
 
 // Resident CTAs per SM of one partial-kernel instance, looked up once per
@@ -601,8 +604,8 @@ static cudaError_t dispatch_group(int group, const CUtensorMap& tmk, const CUten
 template <typename T, int D>
 static cudaError_t launch_reduce_t(const DecodeArgs& a, cudaStream_t stream) {
   const int64_t rows = (int64_t)a.num_seqs * a.num_q_heads;
-  decode_reduce_kernel<T, D><<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(decode_reduce_kernel<T, D>, dim3((unsigned)((rows + 3) / 4)), dim3(128), 0,
+                    stream, a);
 }
 
 cudaError_t launch_decode_reduce(int dtype, int head_dim, const DecodeArgs& a,

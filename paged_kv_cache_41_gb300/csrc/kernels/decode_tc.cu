@@ -80,6 +80,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ uint32_t tmem_base;
 
   const int c = blockIdx.x;
+  pdl_wait();               // inputs written by earlier kernels are visible
+  pdl_launch_dependents();  // the reduction may be scheduled as CTAs retire
   int4 d0;
   const int n = plan_cta_stages<kTcThreads, kTcRows>(a, wsum, &d0);
   if (n <= 0) return;  // no stages: the whole CTA leaves before any barrier
@@ -455,8 +457,8 @@ cudaError_t launch_paged_decode_tc(const CUtensorMap& tmk, const CUtensorMap& tm
   static SmemAttrCache attr_cache;
   cudaError_t e = ensure_smem_limit(kern, kTcSmem, attr_cache);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)a.num_ctas, kTcThreads, kTcSmem, stream>>>(tmk, tmv, tmq, a);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, dim3((unsigned)a.num_ctas), dim3(kTcThreads), kTcSmem, stream, tmk, tmv,
+                 tmq, a);
   if (e != cudaSuccess) return e;
   return launch_decode_reduce(PKV_BF16, kTcD, a, stream);
 }

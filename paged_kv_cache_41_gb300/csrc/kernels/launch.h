@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include <mutex>
+#include <utility>
 
 namespace pkv {
 
@@ -26,6 +27,25 @@ cudaError_t ensure_smem_limit(Kernel kern, int smem, SmemAttrCache& cache) {
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess && dev >= 0 && dev < 64) cache.set[dev] = smem;
   return e;
+}
+
+// Launch `kern` so that it may be scheduled while the previous kernel of the
+// stream finishes (programmatic dependent launch); the kernel must call
+// pdl_wait() before it reads anything an earlier kernel wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k, const void* v,

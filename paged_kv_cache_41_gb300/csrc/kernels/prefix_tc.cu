@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
   constexpr uint32_t kIdQK = tc::idesc_bf16_f32(kPrefixRows, kPrefixKeys, 0, 0);
   constexpr uint32_t kIdPV = tc::idesc_bf16_f32(kPrefixRows, D, 0, 1);
 
+  pdl_launch_dependents();  // the suffix decode may be scheduled as SMs free up
   const int split = blockIdx.x, mp = blockIdx.y, kvh = blockIdx.z;
   const int P = a.block_size;
   const int key0 = split * a.split_len;
