@@ -169,8 +169,9 @@ def test_bad_slot_sets_error_and_writes_nothing():
     assert pkv.get_device_error() == 0  # read-and-clear
 
 
-def test_bad_block_in_table_and_pair_set_error():
-    b = wl.custom_batch([40, 20], dtype="bf16", hq=8, hkv=2, d=128, p=16, seed=61, device="cuda")
+@pytest.mark.parametrize("hq", [8, 16])  # 16 / 2: eight heads per kv head, the tensor-core path
+def test_bad_block_in_table_and_pair_set_error(hq):
+    b = wl.custom_batch([40, 20], dtype="bf16", hq=hq, hkv=2, d=128, p=16, seed=61, device="cuda")
     kc, vc = pu.device_pool(b)
     pu.device_fill(b, kc, vc)
     bt = torch.from_numpy(b.block_tables).cuda()
@@ -182,8 +183,9 @@ def test_bad_block_in_table_and_pair_set_error():
     assert pkv.get_device_error() == pkv.DEVERR_BLOCK
 
 
-def test_length_beyond_table_sets_error():
-    b = wl.custom_batch([40, 20], dtype="bf16", hq=8, hkv=2, d=128, p=16, seed=62, device="cuda")
+@pytest.mark.parametrize("hq", [8, 16])
+def test_length_beyond_table_sets_error(hq):
+    b = wl.custom_batch([40, 20], dtype="bf16", hq=hq, hkv=2, d=128, p=16, seed=62, device="cuda")
     kc, vc = pu.device_pool(b)
     pu.device_fill(b, kc, vc)
     sl = torch.tensor([40, 10_000], dtype=torch.int32, device="cuda")

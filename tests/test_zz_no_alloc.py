@@ -4,7 +4,7 @@ pkv_paged_attention_decode_static serves callers that may not allocate device
 memory (a host framework that owns every allocation, or a steady-state serving
 loop that must never call cudaMalloc/cudaFree).  Its split-K scratch is a fixed
 array the library declares in device memory and shares between calls.  This
-test calls it twice in a row through the C ABI, on two different batches, and
+test calls it three times in a row through the C ABI, on different batches, and
 checks each result against pkv_paged_attention_decode with a caller-owned
 workspace, within the attention tolerance |a - b| <= 2e-3 + 1e-2 |b|.  It also
 checks that sizes beyond the array are refused.  The file is named to be
@@ -41,12 +41,15 @@ def _close(a, b):
     return bool(np.all(err <= ATOL + RTOL * np.where(both_inf, 0.0, np.abs(b))))
 
 
-def test_static_scratch_matches_workspace_version_on_two_calls():
+def test_static_scratch_matches_workspace_version_on_successive_calls():
     batches = [
         wl.custom_batch([1000, 37, 4096, 0, 513, 2000], dtype="bf16", hq=32, hkv=8, d=128, p=16,
                         seed=71, device="cuda"),
         wl.custom_batch([300, 7000, 64, 1500], dtype="bf16", hq=16, hkv=4, d=128, p=64,
                         seed=72, device="cuda"),
+        # eight query heads per kv head: the tensor-core decode
+        wl.custom_batch([900, 5, 3000, 129], dtype="bf16", hq=64, hkv=8, d=128, p=16,
+                        seed=73, device="cuda"),
     ]
     for b in batches:
         kc, vc = _pool(b)
