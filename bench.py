@@ -32,7 +32,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOADS = ("llama", "long_bs16", "long_bs64", "shared", "churn", "gqa8")
+WORKLOADS = ("llama", "long_bs16", "long_bs64", "long_bs64_k16", "shared", "churn", "gqa8")
 
 
 def parse():
@@ -158,7 +158,7 @@ def make_batch(name, device, seed_offset=0, batch=0):
         return wl.llama_batch(device=device, seed=2 + seed_offset, batch=batch or 64)
     if name == "long_bs16":
         return wl.long_batch(device=device, block_size=16, seed=3 + seed_offset, batch=batch or 8)
-    if name == "long_bs64":
+    if name in ("long_bs64", "long_bs64_k16"):
         return wl.long_batch(device=device, block_size=64, seed=3 + seed_offset, batch=batch or 8)
     if name == "gqa8":
         # the Llama-shaped lengths with eight query heads per kv head (64 / 8)
@@ -254,9 +254,24 @@ def run_pkv(args, rank, world, local):
     sl = torch.from_numpy(b.seq_lens).to(dev)
     q = b.q.contiguous()
     out = torch.empty_like(q)
+    # long_bs64_k16: the bs64 allocator pool read as bs16 kernel blocks
+    # ([M5.3] 0x0AC); each step expands the tables on the device first.
+    kblock = 16 if args.workload == "long_bs64_k16" else b.block_size
+    ratio = b.block_size // kblock
+    kview = (b.num_blocks * ratio, kblock, b.num_kv_heads, b.head_dim)
+    kck, vck = kc.view(kview), vc.view(kview)
+    btk = torch.empty(B, b.max_blocks * ratio, dtype=torch.int32, device=dev)
+
+    def decode_call(qq, tables, lens):
+        if ratio > 1:
+            pkv.expand_block_tables(tables, b.block_size, kblock, out=btk)
+            tables = btk
+        pkv.paged_attention_decode(qq, kck, vck, tables, lens, b.scale, out=out,
+                                   partition_size=psize, workspace=ws)
+
     psize = args.partition_size
-    ctas = pkv.decode_num_ctas(kc, B, b.num_q_heads, b.max_blocks, psize)
-    ws_bytes = pkv.decode_workspace_bytes(kc, B, b.num_q_heads, b.max_blocks, psize)
+    ctas = pkv.decode_num_ctas(kck, B, b.num_q_heads, b.max_blocks * ratio, psize)
+    ws_bytes = pkv.decode_workspace_bytes(kck, B, b.num_q_heads, b.max_blocks * ratio, psize)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
     assert pkv.get_device_error() == 0
@@ -264,8 +279,7 @@ def run_pkv(args, rank, world, local):
 
     def step():
         pkv.kv_append(kc, vc, new_k, new_v, step_slots)
-        pkv.paged_attention_decode(q, kc, vc, bt, sl, b.scale, out=out, partition_size=psize,
-                                   workspace=ws)
+        decode_call(q, bt, sl)
 
     kv_bytes = int(b.seq_lens.astype(np.int64).sum()) * kv_row_bytes(b)
     for _ in range(args.warmup):
@@ -287,8 +301,7 @@ def run_pkv(args, rank, world, local):
         ea.record(stream)
         pkv.kv_append(kc, vc, new_k, new_v, step_slots)
         eb.record(stream)
-        pkv.paged_attention_decode(q, kc, vc, bt, sl, b.scale, out=out, partition_size=psize,
-                                   workspace=ws)
+        decode_call(q, bt, sl)
         ec.record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
@@ -321,8 +334,7 @@ def run_pkv(args, rank, world, local):
         d_bt.copy_(h_bt, non_blocking=True)
         d_sl.copy_(h_sl, non_blocking=True)
         pkv.kv_append(kc, vc, d_k, d_v, d_slots)
-        pkv.paged_attention_decode(d_q, kc, vc, d_bt, d_sl, b.scale, out=out,
-                                   partition_size=psize, workspace=ws)
+        decode_call(d_q, d_bt, d_sl)
         h_out.copy_(out, non_blocking=True)
 
     for _ in range(max(3, args.warmup)):
@@ -361,10 +373,12 @@ def run_pkv(args, rank, world, local):
             "workload": {"llama": "llama3-8b-shaped decode layer",
                          "long_bs16": "long-context decode, block size 16",
                          "long_bs64": "long-context decode, block size 64",
+                         "long_bs64_k16": "long-context decode, block size 64 read as "
+                                          "16-row kernel blocks (tables expanded per step)",
                          "gqa8": "decode layer with 8 query heads per kv head (64/8)"
                          }[args.workload],
             "batch": B, "num_q_heads": b.num_q_heads, "num_kv_heads": b.num_kv_heads,
-            "head_dim": b.head_dim, "block_size": b.block_size,
+            "head_dim": b.head_dim, "block_size": b.block_size, "kernel_block_size": kblock,
             "seq_len_min": int(b.seq_lens.min()), "seq_len_max": int(b.seq_lens.max()),
             "total_tokens": int(b.seq_lens.sum()), "pool_blocks": b.num_blocks,
             "partition_size": psize, "decode_ctas": ctas,
@@ -385,7 +399,7 @@ def run_pkv(args, rank, world, local):
                      "algorithmic_bytes_per_launch": kv_bytes},
         "e2e": {"value": world * kv_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * 4,  # append, plan, partial, reduce
+        "gpu_launches": args.steps * (3 + (ratio > 1)),  # append, [expand,] partial, reduce
         "clocks": clk,
     }
     return res, b

@@ -98,6 +98,28 @@ pkv_status pkv_kv_block_copy(const pkv_cache_desc* cache, void* k_cache,
                              void* v_cache, const int64_t* src_dst_pairs,
                              int64_t num_pairs, void* stream);
 
+/* Split allocator blocks for the kernel (M5.3 0x0AC).  A pool whose
+ * allocator blocks hold P_a = q * P_k token rows is, byte for byte, a pool of
+ * q * num_blocks kernel blocks of P_k rows: [NB, P_a, Hkv, D] and
+ * [q * NB, P_k, Hkv, D] are the same array, and allocator block a is kernel
+ * blocks a q, a q + 1, ..., a q + q - 1.  This writes the kernel-visible
+ * tables:
+ *   out[r, c * q + j] = tables[r, c] * q + j     (j = 0 .. q - 1),
+ * with a padding entry (< 0) becoming q entries of -1.  Slot ids are the same
+ * in both views, so kv_append needs no change; decode the view with
+ * cache->block_size = P_k and num_blocks = q * NB.
+ *   tables: int32 [num_seqs, max_blocks] (device).
+ *   out:    int32 [num_seqs, max_blocks * q] (device), caller-owned.
+ *   alloc_block_size, kernel_block_size: P_a and P_k.  P_k must divide P_a:
+ *     the reverse direction would need several separately allocated blocks to
+ *     form one kernel block, so it is PKV_ERR_INVALID_ARG.
+ * An id whose expansion passes INT32_MAX sets PKV_DEVERR_BLOCK and is written
+ * as -1.  Bit-exact. */
+pkv_status pkv_expand_block_tables(const int32_t* tables, int32_t num_seqs,
+                                   int32_t max_blocks, int32_t alloc_block_size,
+                                   int32_t kernel_block_size, int32_t* out,
+                                   void* stream);
+
 /* Bytes of device workspace pkv_paged_attention_decode needs for these sizes
  * and partition_size (see below); 0 for unsupported or invalid sizes.  It
  * depends on the device (its SM count), so query it with the device current. */

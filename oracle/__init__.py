@@ -72,6 +72,8 @@ def _load():
                                                  vp, i32, vp, i32, i32, dbl, vp, vp, i32]
         lib.pkv_oracle_row_ledger.restype = i32
         lib.pkv_oracle_row_ledger.argtypes = [vp, i32, vp, i32, i64, i32, p64, p64]
+        lib.pkv_oracle_expand_table.restype = i32
+        lib.pkv_oracle_expand_table.argtypes = [vp, i64, i32, vp]
         _lib = lib
     return _lib
 
@@ -194,3 +196,15 @@ def row_ledger(block_tables: np.ndarray, seq_lens: np.ndarray, num_pool_blocks: 
     if st != OK:
         raise ValueError(f"oracle row_ledger rejected its inputs (status {st})")
     return lo.value, un.value
+
+
+def expand_table(table, q: int) -> np.ndarray:
+    """Kernel block ids for allocator block ids ([M5.3] 0x0AC): the last axis
+    of ``table`` grows q-fold, allocator id a becoming a q .. a q + q - 1 and
+    padding (-1) becoming q entries of -1."""
+    t = np.ascontiguousarray(table, dtype=np.int32)
+    out = np.empty(t.shape[:-1] + (t.shape[-1] * q,), np.int32)
+    st = _load().pkv_oracle_expand_table(_ptr(t), t.size, q, _ptr(out))
+    if st != OK:
+        raise ValueError(f"oracle expand_table rejected its inputs (status {st})")
+    return out

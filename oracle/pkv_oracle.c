@@ -9,6 +9,7 @@
 #include "pkv_oracle.h"
 
 #include <math.h>
+#include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -277,4 +278,21 @@ int pkv_oracle_row_ledger(const int32_t* block_tables, int max_blocks,
   *logical_rows = logical;
   *unique_rows = unique;
   return status;
+}
+
+int pkv_oracle_expand_table(const int32_t* table, int64_t n, int32_t q, int32_t* out) {
+  if (q < 1 || n < 0) return PKV_ORACLE_BAD_ARG;
+  for (int64_t c = 0; c < n; ++c) {
+    const int32_t a = table[c];
+    for (int32_t j = 0; j < q; ++j) {
+      if (a < 0) {
+        out[c * q + j] = -1;
+        continue;
+      }
+      const int64_t k = (int64_t)a * q + j;
+      if (k > INT32_MAX) return PKV_ORACLE_BAD_ARG;
+      out[c * q + j] = (int32_t)k;
+    }
+  }
+  return PKV_ORACLE_OK;
 }

@@ -134,6 +134,13 @@ int pkv_oracle_row_ledger(const int32_t* block_tables, int max_blocks,
                           int64_t num_blocks, int block_size,
                           int64_t* logical_rows, int64_t* unique_rows);
 
+/* Split allocator blocks for a kernel ([M5.3] 0x0AC): with P_a = q P_k,
+ * allocator block id a becomes the kernel block ids a q, a q + 1, ...,
+ * a q + q - 1, in that order; a negative (padding) entry becomes q padding
+ * entries (-1).  out receives n * q entries.  Returns PKV_ORACLE_BAD_ARG for
+ * q < 1 or an id whose expansion passes INT32_MAX. */
+int pkv_oracle_expand_table(const int32_t* table, int64_t n, int32_t q, int32_t* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -8,6 +8,8 @@
 //     cache row slot_mapping[i] of the [NB * P, Hkv * D] view of the pool.
 //   kv_block_copy: M5.3 0x04C / 0x05A and the fused block-copy kernel of
 //     PagedAttention: whole blocks, K and V, for every (src, dst) pair.
+//   expand_block_tables: M5.3 0x0AC, allocator blocks of P_a = q P_k rows
+//     split into q kernel blocks: id a becomes a q .. a q + q - 1.
 #include "common.cuh"
 #include "launch.h"
 
@@ -84,6 +86,32 @@ __global__ void __launch_bounds__(kCopyThreads) kv_block_copy_kernel(
     const int64_t i = lo + j * kCopyThreads + threadIdx.x;
     if (i < block_vecs) d[i] = tmp[j];
   }
+}
+
+// One thread per output entry: out[i] = in[i / q] * q + i % q, padding kept.
+__global__ void __launch_bounds__(256) expand_block_tables_kernel(const int32_t* __restrict__ in,
+                                                                  int64_t n_out, int32_t q,
+                                                                  int32_t* __restrict__ out,
+                                                                  unsigned int* err) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_out) return;
+  const int32_t a = __ldg(in + i / q);
+  int32_t v = -1;
+  if (a >= 0) {
+    const int64_t k = (int64_t)a * q + i % q;
+    if (k > INT32_MAX) atomicOr(err, PKV_DEVERR_BLOCK);
+    else v = (int32_t)k;
+  }
+  out[i] = v;
+}
+
+cudaError_t launch_expand_block_tables(const int32_t* in, int64_t n_in, int32_t q, int32_t* out,
+                                       unsigned int* err, cudaStream_t stream) {
+  const int64_t n_out = n_in * q;
+  if (n_out == 0) return cudaSuccess;
+  expand_block_tables_kernel<<<(unsigned)((n_out + 255) / 256), 256, 0, stream>>>(in, n_out, q,
+                                                                                 out, err);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_kv_block_copy(void* k_cache, void* v_cache, const int64_t* pairs,

@@ -52,6 +52,9 @@ cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k, const 
                              const int64_t* slots, int64_t num_tokens, int64_t num_slots,
                              int64_t row_bytes, unsigned int* err, cudaStream_t stream);
 
+cudaError_t launch_expand_block_tables(const int32_t* in, int64_t n_in, int32_t q, int32_t* out,
+                                       unsigned int* err, cudaStream_t stream);
+
 cudaError_t launch_kv_block_copy(void* k_cache, void* v_cache, const int64_t* pairs,
                                  int64_t num_pairs, int64_t num_blocks, int64_t block_bytes,
                                  unsigned int* err, cudaStream_t stream);

@@ -400,6 +400,24 @@ pkv_status pkv_kv_block_copy(const pkv_cache_desc* cache, void* k_cache, void* v
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+pkv_status pkv_expand_block_tables(const int32_t* tables, int32_t num_seqs, int32_t max_blocks,
+                                   int32_t alloc_block_size, int32_t kernel_block_size,
+                                   int32_t* out, void* stream) {
+  if (num_seqs < 0 || max_blocks < 0 || alloc_block_size <= 0 || kernel_block_size <= 0 ||
+      alloc_block_size % kernel_block_size != 0)
+    return PKV_ERR_INVALID_ARG;
+  const int64_t n_in = (int64_t)num_seqs * max_blocks;
+  if (n_in == 0) return PKV_OK;
+  if (!tables || !out) return PKV_ERR_INVALID_ARG;
+  const int32_t q = alloc_block_size / kernel_block_size;
+  if ((int64_t)max_blocks * q > INT32_MAX || n_in * q > ((int64_t)1 << 40))
+    return PKV_ERR_UNSUPPORTED;
+  unsigned int* err = device_error_word();
+  if (!err) return PKV_ERR_CUDA;
+  cudaError_t e = pkv::launch_expand_block_tables(tables, n_in, q, out, err, as_stream(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 int32_t pkv_decode_num_ctas(const pkv_cache_desc* cache, int32_t num_seqs, int32_t num_q_heads,
                             int32_t max_blocks_per_seq, int32_t partition_size) {
   if (check_cache(cache) != PKV_OK || max_blocks_per_seq <= 0 || num_seqs <= 0 ||

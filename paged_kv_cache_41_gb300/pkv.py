@@ -26,6 +26,7 @@ EXPORTED = [
     "pkv_kv_block_copy",
     "pkv_decode_workspace_bytes",
     "pkv_decode_num_ctas",
+    "pkv_expand_block_tables",
     "pkv_paged_attention_decode",
     "pkv_paged_attention_decode_static",
     "pkv_shared_prefix_workspace_bytes",
@@ -68,6 +69,8 @@ def load_library():
     lib.pkv_kv_block_copy.argtypes = [dp, vp, vp, vp, i64, vp]
     lib.pkv_decode_workspace_bytes.restype = ctypes.c_size_t
     lib.pkv_decode_workspace_bytes.argtypes = [dp, i32, i32, i32, i32]
+    lib.pkv_expand_block_tables.restype = i32
+    lib.pkv_expand_block_tables.argtypes = [vp, i32, i32, i32, i32, vp, vp]
     lib.pkv_decode_num_ctas.restype = i32
     lib.pkv_decode_num_ctas.argtypes = [dp, i32, i32, i32, i32]
     lib.pkv_paged_attention_decode.restype = ctypes.c_int
@@ -150,6 +153,19 @@ def decode_workspace_bytes(k_cache, num_seqs, num_q_heads, max_blocks_per_seq,
     desc = cache_desc(k_cache)
     return load_library().pkv_decode_workspace_bytes(ctypes.byref(desc), num_seqs, num_q_heads,
                                                      max_blocks_per_seq, partition_size)
+
+
+def expand_block_tables(tables, alloc_block_size, kernel_block_size, out=None, stream=None):
+    """Kernel-visible tables for a pool of P_a-row allocator blocks read as
+    P_k-row kernel blocks (include/pkv.h): int32 [B, max_blocks * P_a / P_k]."""
+    b, m = tables.shape
+    q = alloc_block_size // kernel_block_size if kernel_block_size > 0 else 0
+    if out is None:
+        out = torch.empty(b, m * max(q, 1), dtype=torch.int32, device=tables.device)
+    _check(load_library().pkv_expand_block_tables(_ptr(tables), b, m, alloc_block_size,
+                                                  kernel_block_size, _ptr(out), _stream(stream)),
+           "pkv_expand_block_tables")
+    return out
 
 
 def decode_num_ctas(k_cache, num_seqs, num_q_heads, max_blocks_per_seq, partition_size=0) -> int:

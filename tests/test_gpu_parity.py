@@ -213,6 +213,51 @@ def test_host_validation_rejects_before_launch():
     assert pkv.get_device_error() == 0
 
 
+# ------------------------------------------------------------------ allocator vs kernel blocks
+@pytest.mark.parametrize("q", [1, 2, 4, 16])
+def test_expand_block_tables_bit_exact(q):
+    rng = np.random.default_rng(70 + q)
+    t = rng.integers(0, 5000, size=(7, 33)).astype(np.int32)
+    t[2, 10:] = -1
+    t[5, :] = -1
+    got = pkv.expand_block_tables(torch.from_numpy(t).cuda(), 16 * q, 16)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    assert np.array_equal(got.cpu().numpy(), oracle.expand_table(t, q))
+
+
+@pytest.mark.parametrize("pa,pk,hq", [(64, 16, 8), (256, 32, 16), (256, 16, 16)])
+def test_decode_through_kernel_blocks(pa, pk, hq):
+    """A pool of P_a-row allocator blocks decoded as P_k-row kernel blocks
+    through the expanded tables (16 / 2 heads: the tensor-core path) equals
+    the oracle's decode of the allocator-block view."""
+    b = wl.custom_batch([700, 1, 129, 0, 2050, 64], dtype="bf16", hq=hq, hkv=2, d=128, p=pa,
+                        seed=74, device="cuda")
+    kc, vc = pu.device_pool(b)
+    pu.device_fill(b, kc, vc)
+    hk, hv = pu.host_pool(b)
+    pu.oracle_fill(b, hk, hv)
+    r = pa // pk
+    view = (b.num_blocks * r, pk, b.num_kv_heads, b.head_dim)
+    bt = pkv.expand_block_tables(torch.from_numpy(b.block_tables).cuda(), pa, pk)
+    sl = torch.from_numpy(b.seq_lens).cuda()
+    lse = torch.empty(b.num_seqs, b.num_q_heads, dtype=torch.float32, device="cuda")
+    out = pkv.paged_attention_decode(b.q, kc.view(view), vc.view(view), bt, sl, b.scale, lse=lse)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    ref, ref_lse = pu.oracle_decode(b, hk, hv)
+    pu.assert_close(out.float().cpu().numpy(), ref, "kernel-block view out")
+    pu.assert_close(lse.cpu().numpy(), ref_lse, "kernel-block view lse")
+
+
+def test_expand_rejects_a_kernel_block_larger_than_the_allocator_block():
+    t = torch.zeros(2, 3, dtype=torch.int32, device="cuda")
+    for pa, pk in ((16, 32), (48, 32)):
+        with pytest.raises(pkv.PkvError) as ei:
+            pkv.expand_block_tables(t, pa, pk)
+        assert ei.value.status == pkv.PKV_ERR_INVALID_ARG
+
+
 # ------------------------------------------------------------------ churn trace
 def test_churn_trace_small():
     """A short churn trace: requests finish and arrivals take blocks from the

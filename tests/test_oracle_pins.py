@@ -221,6 +221,45 @@ def test_decode_permutation_invariance_is_bitwise():
     assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
 
 
+def test_table_expansion_printed_in_pages():
+    rows = _rows("table_expansion.txt")
+    assert len(rows) == 2
+    for pa, pk, ids, kernel in rows:
+        q = int(pa) // int(pk)
+        if ids == "*":
+            assert oracle.expand_table(np.array([[9]], np.int32), q).shape == (1, int(kernel))
+        else:
+            got = oracle.expand_table(np.array([int(x) for x in ids.split(",")], np.int32), q)
+            assert got.tolist() == [int(x) for x in kernel.split(",")]
+
+
+def test_table_expansion_padding_identity_and_order():
+    t = np.array([[5, 0, -1], [2, -1, -1]], np.int32)
+    assert np.array_equal(oracle.expand_table(t, 1), t)
+    e = oracle.expand_table(t, 3)
+    assert e.tolist() == [[15, 16, 17, 0, 1, 2, -1, -1, -1], [6, 7, 8, -1, -1, -1, -1, -1, -1]]
+    with pytest.raises(ValueError):
+        oracle.expand_table(t, 0)
+    with pytest.raises(ValueError):  # 2^30 * 2 does not fit an int32 id
+        oracle.expand_table(np.array([1 << 30], np.int32), 2)
+
+
+@pytest.mark.parametrize("pa,pk", [(32, 16), (64, 16), (256, 64), (16, 16)])
+def test_decode_through_expanded_table_is_bitwise_equal(pa, pk):
+    """[M5.3] 0x0AC: the payload is not duplicated -- the same pool bytes,
+    viewed as q-fold more blocks of P_k rows and read through the expanded
+    table, give the very same attention (bitwise, in the oracle)."""
+    b = wl.custom_batch([37, 1, 200, 64, 0], dtype="bf16", hq=4, hkv=2, d=16, p=pa, seed=13)
+    kc, vc = _oracle_pool_from_batch(b)
+    q = wl.to_numpy_storage(b.q)
+    out, lse = oracle.paged_decode(q, kc, vc, b.block_tables, b.seq_lens, b.scale)
+    r = pa // pk
+    view = (b.num_blocks * r, pk, b.num_kv_heads, b.head_dim)
+    out2, lse2 = oracle.paged_decode(q, kc.reshape(view), vc.reshape(view),
+                                     oracle.expand_table(b.block_tables, r), b.seq_lens, b.scale)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
 def _one_seq(k, v, q, scale, p=4):
     """Pack one sequence (rows [T, 1, D]) into a pool with reversed block order."""
     t, d = k.shape[0], k.shape[-1]
