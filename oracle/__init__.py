@@ -74,6 +74,9 @@ def _load():
         lib.pkv_oracle_row_ledger.argtypes = [vp, i32, vp, i32, i64, i32, p64, p64]
         lib.pkv_oracle_expand_table.restype = i32
         lib.pkv_oracle_expand_table.argtypes = [vp, i64, i32, vp]
+        lib.pkv_oracle_chunk_tree.restype = i32
+        lib.pkv_oracle_chunk_tree.argtypes = [i32, vp, vp, vp, i64, i32, i32, i32, vp, vp, vp, vp,
+                                              i32, vp, i64, i32, i32, dbl, vp, vp, i32]
         _lib = lib
     return _lib
 
@@ -181,6 +184,35 @@ def shared_prefix(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
                                           float(scale), _ptr(out), _ptr(lse), int(nthreads))
     if st != OK:
         raise ValueError(f"oracle shared_prefix rejected its inputs (status {st})")
+    return out, lse
+
+
+def chunk_tree(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, chunks,
+               block_ids, scale: float, nthreads: int = 1):
+    """Attention over a prefix-tree snapshot by definition ([M5.3] 0x0BB,
+    0x0BE): ``chunks`` is [n, 4] int rows (first id, rows, seq begin, seq
+    end); each sequence attends to the concatenation of the chunks covering
+    it.  Returns (out [B, Hq, D] float64, lse [B, Hq] float64)."""
+    nb, p, hkv, d = k_cache.shape
+    b, hq, dq = q.shape
+    assert dq == d and q.dtype == k_cache.dtype
+    ch = np.ascontiguousarray(chunks, dtype=np.int32).reshape(-1, 4)
+    cols = [np.ascontiguousarray(ch[:, i]) for i in range(4)]
+    ids = np.ascontiguousarray(block_ids, dtype=np.int32).reshape(-1)
+    if ids.size == 0:
+        ids = np.zeros(1, np.int32)
+        n_ids = 0
+    else:
+        n_ids = ids.size
+    out = np.zeros((b, hq, d), dtype=np.float64)
+    lse = np.zeros((b, hq), dtype=np.float64)
+    st = _load().pkv_oracle_chunk_tree(_dtype_code(k_cache), _ptr(np.ascontiguousarray(q)),
+                                       _ptr(k_cache), _ptr(v_cache), nb, p, hkv, d,
+                                       _ptr(cols[0]), _ptr(cols[1]), _ptr(cols[2]),
+                                       _ptr(cols[3]), len(ch), _ptr(ids), n_ids, b, hq,
+                                       float(scale), _ptr(out), _ptr(lse), int(nthreads))
+    if st != OK:
+        raise ValueError(f"oracle chunk_tree rejected its inputs (status {st})")
     return out, lse
 
 

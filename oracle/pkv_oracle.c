@@ -8,6 +8,7 @@
  */
 #include "pkv_oracle.h"
 
+#include <limits.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -248,6 +249,68 @@ int pkv_oracle_shared_prefix(int dtype, const void* q, const void* k_cache,
   free(tables);
   free(lens);
   return st;
+}
+
+int pkv_oracle_chunk_tree(int dtype, const void* q, const void* k_cache,
+                          const void* v_cache, int64_t num_blocks,
+                          int block_size, int num_kv_heads, int head_dim,
+                          const int32_t* chunk_first_id,
+                          const int32_t* chunk_lens,
+                          const int32_t* chunk_begin, const int32_t* chunk_end,
+                          int num_chunks, const int32_t* block_ids,
+                          int64_t num_block_ids, int num_seqs, int num_q_heads,
+                          double scale, double* out, double* lse,
+                          int nthreads) {
+  if (block_size <= 0 || num_blocks <= 0 || num_chunks < 0 || num_seqs < 0)
+    return PKV_ORACLE_BAD_ARG;
+  const int64_t P = block_size;
+  for (int c = 0; c < num_chunks; ++c) {
+    if (chunk_lens[c] < 1 || chunk_first_id[c] < 0 || chunk_begin[c] < 0 ||
+        chunk_begin[c] >= chunk_end[c] || chunk_end[c] > num_seqs)
+      return PKV_ORACLE_BAD_ARG;
+    if ((int64_t)chunk_first_id[c] + (chunk_lens[c] + P - 1) / P > num_block_ids)
+      return PKV_ORACLE_BAD_ARG;
+  }
+  /* each sequence's history length: the rows of the chunks on its path */
+  int32_t* lens = (int32_t*)calloc((size_t)(num_seqs > 0 ? num_seqs : 1), sizeof(int32_t));
+  int width = 0;
+  for (int r = 0; r < num_seqs; ++r) {
+    int64_t T = 0;
+    for (int c = 0; c < num_chunks; ++c)
+      if (chunk_begin[c] <= r && r < chunk_end[c]) T += chunk_lens[c];
+    if (T > INT32_MAX) {
+      free(lens);
+      return PKV_ORACLE_BAD_ARG;
+    }
+    lens[r] = (int32_t)T;
+    if (lens[r] > width) width = lens[r];
+  }
+  /* slot table of every history: row t of chunk c is pool slot
+   * block * P + t % P, i.e. block (block * P + t % P) of a one-row pool */
+  int32_t* slots = (int32_t*)malloc(sizeof(int32_t) * (size_t)(num_seqs > 0 ? num_seqs : 1) *
+                                    (size_t)(width > 0 ? width : 1));
+  int status = PKV_ORACLE_OK;
+  for (int r = 0; r < num_seqs && status == PKV_ORACLE_OK; ++r) {
+    int64_t pos = 0;
+    for (int c = 0; c < num_chunks && status == PKV_ORACLE_OK; ++c) {
+      if (!(chunk_begin[c] <= r && r < chunk_end[c])) continue;
+      for (int64_t t = 0; t < chunk_lens[c]; ++t) {
+        const int64_t blk = block_ids[chunk_first_id[c] + t / P];
+        if (blk < 0 || blk >= num_blocks || blk * P + P - 1 > INT32_MAX) {
+          status = PKV_ORACLE_BAD_BLOCK;
+          break;
+        }
+        slots[(int64_t)r * width + pos++] = (int32_t)(blk * P + t % P);
+      }
+    }
+  }
+  if (status == PKV_ORACLE_OK)
+    status = pkv_oracle_paged_decode(dtype, q, k_cache, v_cache, num_blocks * P, 1,
+                                     num_kv_heads, head_dim, slots, width, lens, num_seqs,
+                                     num_q_heads, scale, out, lse, nthreads);
+  free(slots);
+  free(lens);
+  return status;
 }
 
 int pkv_oracle_row_ledger(const int32_t* block_tables, int max_blocks,

@@ -12,7 +12,7 @@
  *
  * Sources (page titles, sections):
  *   [M5.3]  "M5.3 - KV Memory Layout and Exact Reuse", sections 0x02C, 0x03C-0x03I,
- *           0x04E, 0x0A, 0x0BA, 0x0BC, 0x0BE, 0x0BI.
+ *           0x04E, 0x0A, 0x0BA, 0x0BB, 0x0BC, 0x0BE, 0x0BI.
  *   [Ch7]   "7. Memory Management and Local Model State", "Logical tokens,
  *           physical blocks" and "Choosing a block size".
  *   [Cache] "Cache Concepts: Prefix Matching vs. Storage" (TokenSpeed), the
@@ -124,6 +124,27 @@ int pkv_oracle_shared_prefix(int dtype, const void* q, const void* k_cache,
                              const int32_t* suffix_lens, int num_seqs,
                              int num_q_heads, double scale, double* out,
                              double* lse, int nthreads);
+
+/* Attention over a prefix-tree snapshot by definition ([M5.3] 0x0BB, 0x0BE
+ * "reference" schedule): chunk c holds chunk_lens[c] K/V rows, row t in pool
+ * block block_ids[chunk_first_id[c] + t / P] at offset t % P, and covers the
+ * sequences [chunk_begin[c], chunk_end[c]).  Sequence r's logical history is
+ * the concatenation, in array (tree) order, of the rows of every chunk that
+ * covers r; one monolithic softmax row runs over it.  The pool is viewed as
+ * num_blocks * P blocks of one row each, so each history becomes a table of
+ * slot ids for pkv_oracle_paged_decode.  Returns PKV_ORACLE_BAD_ARG for a
+ * chunk with len < 1, an empty or out-of-range coverage, or ids outside
+ * block_ids; PKV_ORACLE_BAD_BLOCK for a block id outside the pool. */
+int pkv_oracle_chunk_tree(int dtype, const void* q, const void* k_cache,
+                          const void* v_cache, int64_t num_blocks,
+                          int block_size, int num_kv_heads, int head_dim,
+                          const int32_t* chunk_first_id,
+                          const int32_t* chunk_lens,
+                          const int32_t* chunk_begin, const int32_t* chunk_end,
+                          int num_chunks, const int32_t* block_ids,
+                          int64_t num_block_ids, int num_seqs, int num_q_heads,
+                          double scale, double* out, double* lse,
+                          int nthreads);
 
 /* K/V row ledger of a batch ([M5.3] 0x02D, 0x0BI): logical rows are the sum of
  * the requests' context lengths, unique rows the number of distinct

@@ -14,6 +14,7 @@ import torch
 from scipy.special import logsumexp
 
 import oracle
+from oracle import prefix_tree
 from paged_kv_cache_41_gb300 import workloads as wl
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -414,56 +415,216 @@ def _lse_merge(parts):
     return o, mx + np.log(w.sum())
 
 
-def test_loop9_tree_partitioned_schedule_agrees_with_oracle():
-    kv = {}
-    for r in _rows("ledgers.txt"):
-        if r[0] == "loop9":
-            kv.setdefault(r[1], []).append(r[2:])
-    chunks = dict((c.split(":")[0], int(c.split(":")[1])) for c in kv["chunks"][0])
-    paths = [p.split(":")[1].split(",") for p in kv["paths"][0]]
-    counts = ["logical"] + kv["logical"][0]
-    want = dict(zip(counts[::2], counts[1::2]))
-    d = 2
-    rng = np.random.default_rng(99)
-    ck = {c: rng.standard_normal((n, d)).astype(np.float32) for c, n in chunks.items()}
-    cv = {c: rng.standard_normal((n, d)).astype(np.float32) for c, n in chunks.items()}
-    q = rng.standard_normal((len(paths), 1, d)).astype(np.float32)
-    # page the tree with block size 1: every chunk row is one physical block
-    ids, nxt = {}, 0
-    for c, n in chunks.items():
-        ids[c] = list(range(nxt, nxt + n))
+def _loop9():
+    """The printed fixture: chunk (name, rows, begin, end) in tree order, the
+    shapes and the ledger."""
+    rows = _rows("chunk_tree_loop9.txt")
+    chunks = [(r[1], int(r[2]), int(r[3]), int(r[4])) for r in rows if r[0] == "chunk"]
+    shape = {r[1]: int(r[2]) for r in rows if r[0] == "shape"}
+    ledger = {r[1]: int(r[2]) for r in rows if r[0] == "ledger"}
+    bound = float(next(r[2] for r in rows if r[0] == "bound"))
+    return chunks, shape, ledger, bound
+
+
+def _loop9_dense(seed):
+    chunks, shape, _, _ = _loop9()
+    rng = np.random.default_rng(seed)
+    dense = [prefix_tree.Chunk(rng.standard_normal((n, shape["d_qk"])),
+                               rng.standard_normal((n, shape["d_v"])), b, e)
+             for _, n, b, e in chunks]
+    return rng.standard_normal((shape["B"], shape["d_qk"])), dense, shape
+
+
+def test_loop9_ledger_printed_in_pages():
+    chunks, shape, want, _ = _loop9()
+    _, dense, _ = _loop9_dense(0)
+    got = prefix_tree.ledger(dense, shape["d_qk"], shape["d_v"], elem_bytes=2, state_bytes=4,
+                             threshold=1)
+    assert got == want
+    # the paths the intervals imply: S0 C0,C1,C3; S1 C0,C1,C4; S2 C0,C2,C5; S3 C0,C2,C6
+    names = [c[0][:2] for c in chunks]
+    assert [[names[i] for i in prefix_tree.path(dense, r)] for r in range(4)] == [
+        ["C0", "C1", "C3"], ["C0", "C1", "C4"], ["C0", "C2", "C5"], ["C0", "C2", "C6"]]
+
+
+def test_loop9_row_ledger_through_a_paged_pool():
+    # the same counts from the oracle's slot ledger: page the tree with block
+    # size 1 (one pool block per chunk row) and count logical vs unique slots
+    chunks, _, want, _ = _loop9()
+    ids, nxt = [], 0
+    for _, n, _, _ in chunks:
+        ids.append(list(range(nxt, nxt + n)))
         nxt += n
-    kc = np.zeros((nxt, 1, 1, d), np.float32)
-    vc = np.zeros_like(kc)
-    for c in chunks:
-        kc[ids[c], 0, 0] = ck[c]
-        vc[ids[c], 0, 0] = cv[c]
-    lens = [sum(chunks[c] for c in p) for p in paths]
-    width = max(lens)
-    tables = np.full((len(paths), width), -1, np.int32)
-    for r, p in enumerate(paths):
-        row = sum((ids[c] for c in p), [])
-        tables[r, :len(row)] = row
-    scale = 1.0 / math.sqrt(d)
-    out, lse = oracle.paged_decode(q, kc, vc, tables, np.array(lens, np.int32), scale)
-    # the page's counts
-    lo, un = oracle.row_ledger(tables, np.array(lens, np.int32), nxt, 1)
-    assert (lo, un, lo - un) == (int(want["logical"]), int(want["unique"]), int(want["saved"]))
-    cover = {c: sum(c in p for p in paths) for c in chunks}
-    assert sum(v for v in cover.values() if v > 1) == int(want["partial_rows"])
-    # Hydragen coordinates: attention per chunk with its LSE, then the merge
-    qd = q.astype(np.float64)
-    for r, p in enumerate(paths):
-        parts = []
-        for c in p:
-            s = scale * (ck[c].astype(np.float64) @ qd[r, 0])
-            l = logsumexp(s)
-            parts.append((np.exp(s - l) @ cv[c].astype(np.float64), l))
-        o, l = _lse_merge(parts)
-        # the page reports agreement within 2.3e-16 on its values; these are
-        # other values of magnitude ~1, so allow a few units in the last place
-        assert np.abs(o - out[r, 0]).max() <= 1e-15
-        assert abs(l - lse[r, 0]) <= 4e-16 * max(1.0, abs(l))
+    tables, lens = [], []
+    for r in range(4):
+        row = sum((ids[i] for i, c in enumerate(chunks) if c[2] <= r < c[3]), [])
+        tables.append(row + [-1] * (8 - len(row)))
+        lens.append(len(row))
+    lo, un = oracle.row_ledger(np.array(tables, np.int32), np.array(lens, np.int32), nxt, 1)
+    assert (lo, un, lo - un) == (want["logical_pairs"], want["physical_rows"], want["saved_reads"])
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_loop9_three_schedules_agree(seed):
+    # 0x0BE: both partitioned schedules match the monolithic row to rounding
+    # (2.3e-16 absolute on the page's values).  These are other seeded values
+    # with |o| up to ~3, so the bound is scaled by (1 + |ref|) and given a
+    # factor of 4.
+    _, _, _, bound = _loop9()
+    Q, dense, shape = _loop9_dense(seed)
+    scale = 1.0 / math.sqrt(shape["d_qk"])
+    o0, l0 = prefix_tree.monolithic(Q, dense, scale)
+    o1, l1 = prefix_tree.hydragen(Q, dense, scale)
+    o2, l2, n_partial = prefix_tree.chunk_attention(Q, dense, scale, threshold=1)
+    assert n_partial == 8
+    tol = 4 * bound
+    for o, l in ((o1, l1), (o2, l2)):
+        assert np.all(np.abs(o - o0) <= tol * (1 + np.abs(o0)))
+        assert np.all(np.abs(l - l0) <= tol * (1 + np.abs(l0)))
+
+
+def test_loop9_monolithic_matches_library_softmax():
+    # the reference schedule against scipy's logsumexp on each gathered path
+    Q, dense, shape = _loop9_dense(7)
+    scale = 1.0 / math.sqrt(shape["d_qk"])
+    o0, l0 = prefix_tree.monolithic(Q, dense, scale)
+    for r in range(shape["B"]):
+        K = np.concatenate([dense[i].k for i in prefix_tree.path(dense, r)])
+        V = np.concatenate([dense[i].v for i in prefix_tree.path(dense, r)])
+        s = scale * (K @ Q[r])
+        lse = logsumexp(s)
+        assert abs(lse - l0[r]) <= 1e-14
+        assert np.allclose(np.exp(s - lse) @ V, o0[r], rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("threshold", [0, 1, 2, 4])
+def test_chunk_attention_threshold_changes_buffer_not_result(threshold):
+    # 0x0BD: the threshold only moves chunks between the phases
+    Q, dense, shape = _loop9_dense(3)
+    scale = 1.0 / math.sqrt(shape["d_qk"])
+    o0, _ = prefix_tree.monolithic(Q, dense, scale)
+    o, _, n_partial = prefix_tree.chunk_attention(Q, dense, scale, threshold=threshold)
+    assert n_partial == sum(c.coverage for c in dense if c.coverage > threshold)
+    assert np.all(np.abs(o - o0) <= 1e-15 * (1 + np.abs(o0)))
+
+
+def test_merge_empty_state_is_identity():
+    # 0x0BA: the empty part is a two-sided identity, never exp(-inf - -inf)
+    s = (np.array([1.0, -2.0, 0.5]), 0.3, 2.0)
+    assert prefix_tree.merge_states(prefix_tree.EMPTY, s) is s
+    assert prefix_tree.merge_states(s, prefix_tree.EMPTY) is s
+    o, l = prefix_tree.finalize(prefix_tree.EMPTY, 3)
+    assert np.all(o == 0) and l == -np.inf
+
+
+def _paged_tree(chunk_rows, cover, hq, hkv, d, p, seed, dtype=np.float32):
+    """A pool holding a prefix tree: chunk c gets its own blocks (a ragged
+    chunk leaves the rest of its last block holding NaN), placed at seeded
+    shuffled ids.  Returns (q, kc, vc, chunks [n, 4], block_ids)."""
+    rng = np.random.default_rng(seed)
+    nblk = [oracle.num_blocks(n, p) for n in chunk_rows]
+    total = sum(nblk) + 3
+    perm = rng.permutation(total).astype(np.int32)
+    kc = np.full((total, p, hkv, d), np.nan, np.float32)
+    vc = np.full((total, p, hkv, d), np.nan, np.float32)
+    ids, chunks, nxt = [], [], 0
+    for n, (b, e), nb in zip(chunk_rows, cover, nblk):
+        blk = perm[nxt:nxt + nb]
+        chunks.append((len(ids), n, b, e))
+        ids.extend(blk.tolist())
+        nxt += nb
+        for t in range(n):
+            kc[blk[t // p], t % p] = rng.standard_normal((hkv, d))
+            vc[blk[t // p], t % p] = rng.standard_normal((hkv, d))
+    B = max(e for _, e in cover)
+    q = rng.standard_normal((B, hq, d)).astype(np.float32)
+    return q, kc, vc, np.array(chunks, np.int32), np.array(ids, np.int32)
+
+
+def test_chunk_tree_oracle_matches_dense_monolithic():
+    # the paged tree oracle (slot tables over a one-row-block view of the
+    # pool) against the dense reference schedule, head by head
+    rows, cover = [2, 1, 2, 2, 1, 1, 1], [(0, 4), (0, 2), (2, 4), (0, 1), (1, 2), (2, 3), (3, 4)]
+    rows = [r * 3 + 1 for r in rows]  # ragged chunks over 4-row blocks
+    q, kc, vc, ch, ids = _paged_tree(rows, cover, hq=4, hkv=2, d=8, p=4, seed=5)
+    scale = 1 / math.sqrt(8)
+    out, lse = oracle.chunk_tree(q, kc, vc, ch, ids, scale)
+    for h in range(4):
+        kvh = h // 2
+        dense = []
+        for (f, n, b, e) in ch:
+            slots = [(ids[f + t // 4], t % 4) for t in range(n)]
+            dense.append(prefix_tree.Chunk(np.array([kc[s][kvh] for s in slots], np.float64),
+                                           np.array([vc[s][kvh] for s in slots], np.float64),
+                                           int(b), int(e)))
+        o, l = prefix_tree.monolithic(q[:, h].astype(np.float64), dense, scale)
+        assert np.allclose(out[:, h], o, rtol=0, atol=1e-13)
+        assert np.allclose(lse[:, h], l, rtol=0, atol=1e-13)
+
+
+def test_chunk_tree_two_levels_equal_shared_prefix_bitwise():
+    # a root chunk over every sequence plus one private chunk each is the
+    # shared-prefix case: the same rows in the same order, so bit-equal
+    sp = wl.shared_prefix_batch(batch=5, prefix_len=48, shared_tail=3, suffix_lo=4, suffix_hi=30,
+                                hq=4, hkv=2, d=16, p=16, seed=8)
+    kc, vc, npre = _shared_prefix_pools(sp)
+    q = wl.to_numpy_storage(sp.q)
+    out, lse = oracle.shared_prefix(q, kc, vc, sp.prefix_block_ids, sp.prefix_len,
+                                    sp.suffix_tables, sp.suffix_lens, sp.scale)
+    ids = list(sp.prefix_block_ids)
+    chunks = [(0, sp.prefix_len, 0, sp.num_seqs)]
+    for r in range(sp.num_seqs):
+        n = int(sp.suffix_lens[r])
+        chunks.append((len(ids), n, r, r + 1))
+        ids.extend(int(x) for x in sp.suffix_tables[r][:oracle.num_blocks(n, sp.block_size)])
+    out2, lse2 = oracle.chunk_tree(q, kc, vc, np.array(chunks), np.array(ids), sp.scale)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+def test_chunk_tree_private_chunks_equal_paged_decode_bitwise():
+    b = wl.tiny_batch()
+    kc, vc = _oracle_pool_from_batch(b)
+    q = wl.to_numpy_storage(b.q)
+    tables, lens = b.block_tables, np.asarray(b.seq_lens)
+    out, lse = oracle.paged_decode(q, kc, vc, tables, lens, b.scale)
+    ids, chunks = [], []
+    for r in range(len(lens)):
+        nb = oracle.num_blocks(int(lens[r]), kc.shape[1])
+        chunks.append((len(ids), int(lens[r]), r, r + 1))
+        ids.extend(int(x) for x in tables[r][:nb])
+    out2, lse2 = oracle.chunk_tree(q, kc, vc, np.array(chunks), np.array(ids), b.scale)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+def test_chunk_tree_invariant_under_chunk_order_and_relabeling():
+    rows, cover = [9, 5, 7, 3, 6, 1, 2], [(0, 4), (0, 2), (2, 4), (0, 1), (1, 2), (2, 3), (3, 4)]
+    q, kc, vc, ch, ids = _paged_tree(rows, cover, hq=2, hkv=1, d=8, p=4, seed=2)
+    out, lse = oracle.chunk_tree(q, kc, vc, ch, ids, 0.3)
+    # another order of the chunk list: the same keys per row, summed in
+    # another order
+    perm = [6, 2, 0, 5, 1, 4, 3]
+    out2, lse2 = oracle.chunk_tree(q, kc, vc, ch[perm], ids, 0.3)
+    assert np.allclose(out, out2, rtol=0, atol=1e-14) and np.allclose(lse, lse2, rtol=0, atol=1e-14)
+    # move every block to another physical id: bit-identical
+    nb = kc.shape[0]
+    relabel = np.random.default_rng(4).permutation(nb)
+    kc2, vc2 = np.empty_like(kc), np.empty_like(vc)
+    kc2[relabel], vc2[relabel] = kc, vc
+    out3, lse3 = oracle.chunk_tree(q, kc2, vc2, ch, relabel[ids].astype(np.int32), 0.3)
+    assert np.array_equal(out, out3) and np.array_equal(lse, lse3)
+
+
+def test_chunk_tree_oracle_rejects_bad_snapshots():
+    q, kc, vc, ch, ids = _paged_tree([3, 2], [(0, 2), (1, 2)], hq=1, hkv=1, d=4, p=4, seed=0)
+    for bad in ([0, 0, 0, 2], [0, 3, 1, 1], [0, 3, 0, 3], [0, 3, -1, 1], [5, 3, 0, 2]):
+        c2 = ch.copy()
+        c2[0] = bad
+        with pytest.raises(ValueError):
+            oracle.chunk_tree(q, kc, vc, c2, ids, 1.0)
+    ids2 = ids.copy()
+    ids2[0] = kc.shape[0]
+    with pytest.raises(ValueError):
+        oracle.chunk_tree(q, kc, vc, ch, ids2, 1.0)
 
 
 def test_loop10_shared_work_ledger():
