@@ -32,7 +32,8 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOADS = ("llama", "long_bs16", "long_bs64", "long_bs64_k16", "shared", "churn", "gqa8")
+WORKLOADS = ("llama", "long_bs16", "long_bs64", "long_bs64_k16", "shared", "churn", "gqa8",
+             "tree")
 
 
 def parse():
@@ -533,6 +534,167 @@ def run_shared(args, rank, world, local):
     return res, sp
 
 
+# ------------------------------------------------------------------ prefix tree
+TREE_SHAPE = dict(root_len=2048, groups=4, group_len=1024, leaf_lo=16, leaf_hi=512)
+
+
+def tree_batch(device, seed, batch):
+    from paged_kv_cache_41_gb300 import workloads as wl
+    tree = wl.multi_level_tree(batch=batch, seed=seed, **TREE_SHAPE)
+    return wl.prefix_tree_batch(tree, device=device, seed=seed)
+
+
+def run_tree(args, rank, world, local):
+    """Multi-level shared prefixes: 128 requests under one 2048-token root,
+    four groups of 32 under their own chunk of 512..1024 tokens, and a private
+    leaf of 16..512 tokens each.  One call attends every request over its
+    whole path (chunk-first tensor-core phase, decode of the leaves, merge)."""
+    import torch
+    from paged_kv_cache_41_gb300 import pkv
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    pkv.load_library()
+    tb = tree_batch(dev, 6 + rank, args.batch or 128)
+    shape = (tb.num_blocks, tb.block_size, tb.num_kv_heads, tb.head_dim)
+    kc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    pkv.kv_append(kc, vc, tb.k_rows, tb.v_rows, torch.from_numpy(tb.slots).to(dev))
+    B, Hq, D = tb.num_seqs, tb.num_q_heads, tb.head_dim
+    plan = pkv.chunk_tree_plan(kc, tb.chunks, tb.block_ids, B, Hq)
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(tb.q)
+    flush = torch.empty(1 << 30, dtype=torch.uint8, device=dev)  # > L2 (129 MB)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    stream = torch.cuda.current_stream()
+
+    def call():
+        pkv.chunk_tree_attention(tb.q, kc, vc, plan, tb.scale, out=out, workspace=ws)
+
+    def timed(fn, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for a, b in evs:
+            flush.fill_(1)  # evict the K/V, states and q from L2 before each call
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b) for a, b in evs]))
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = ClockSampler(local)
+    clocks.start()
+    n = max(args.steps, 20)
+    call_ms = all_max(timed(call, n), world)
+    clk = clocks.stop()
+    assert pkv.get_device_error() == 0
+
+    # end to end: each step re-plans the snapshot on the host (the leaves grow
+    # every decode step), copies the plan and q from pinned memory, attends
+    # and reads the output back.  Two pinned plan buffers alternate; a buffer
+    # is re-planned only after the copy that read it has run.
+    cap = int(plan.host.numel()) + 4096
+    h_plans = [torch.empty(cap, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
+    d_plans = [torch.empty(cap, dtype=torch.uint8, device=dev) for _ in range(2)]
+    copied = [None, None]
+    h_q = tb.q.cpu().pin_memory()
+    d_q = torch.empty_like(tb.q)
+    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    step = [0]
+
+    def e2e():
+        i = step[0] % 2
+        step[0] += 1
+        if copied[i] is not None:
+            copied[i].synchronize()
+        p = pkv.chunk_tree_plan(kc, tb.chunks, tb.block_ids, B, Hq, host_buffer=h_plans[i],
+                                device_buffer=d_plans[i])
+        copied[i] = torch.cuda.Event()
+        copied[i].record(stream)
+        d_q.copy_(h_q, non_blocking=True)
+        pkv.chunk_tree_attention(d_q, kc, vc, p, tb.scale, out=out, workspace=ws)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e()
+    e2e_ms = timed(e2e, n)
+    assert pkv.get_device_error() == 0
+    h2d = int(plan.host.numel()) + h_q.numel() * h_q.element_size()
+    d2h = h_out.numel() * h_out.element_size()
+
+    hbm, kind = load_peaks()
+    row = kv_row_bytes_dims(tb.num_kv_heads, D, 2)
+    ch = tb.chunks.astype(np.int64)
+    cov = ch[:, 3] - ch[:, 2]
+    logical = float((ch[:, 1] * cov).sum()) * row
+    unique = float(ch[:, 1].sum()) * row
+    shared = cov > 1
+    flops_cf = 4.0 * float((ch[shared, 1] * cov[shared]).sum()) * Hq * D
+    achieved = unique / (call_ms * 1e-3) / 1e9
+    res = {
+        "metric": "prefix-tree attention: logical KV GB/s (K/V bytes per-request decode "
+                  "would read / call time)",
+        "value": world * logical / (call_ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": world,
+        "steps": n, "warmup": args.warmup, "ms_per_step": call_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v, seeded chunk lengths and block placement)",
+        "config": {"workload": "three-level prefix tree", "batch": B, **TREE_SHAPE,
+                   "chunks": int(len(ch)), "num_q_heads": Hq, "num_kv_heads": tb.num_kv_heads,
+                   "head_dim": D, "block_size": tb.block_size, "threshold": 1,
+                   "l2": "flushed (1 GiB write) before every timed call"},
+        "tree_call_ms": call_ms,
+        "logical_kv_bytes": logical, "unique_kv_bytes": unique,
+        "saved_kv_reads": logical - unique,
+        "chunk_first_flops": flops_cf,
+        "roofline": {"bound": "hbm", "kernel": "whole call (prefix_attention_kernel, "
+                     "decode_partial_kernel, decode_reduce_kernel, tree_merge_kernel)",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "peak_kind": f"{kind} hbm_gbs (copy)", "traffic": None,
+                     "algorithmic_bytes_per_launch": unique},
+        "e2e": {"value": world * logical / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s (logical K/V)",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "includes": "host planning of the snapshot every step"},
+        "gpu_launches": n * 4,  # chunk-first, decode partial, reduce, merge
+        "clocks": clk,
+    }
+    return res, tb
+
+
+def tree_cpu_baseline(tb, seconds):
+    """The oracle's definition on whole requests of the tree batch."""
+    import oracle
+    from paged_kv_cache_41_gb300 import workloads as wl
+    nthreads = len(os.sched_getaffinity(0))
+    shape = (tb.num_blocks, tb.block_size, tb.num_kv_heads, tb.head_dim)
+    hk = np.zeros(shape, np.uint16)
+    hv = np.zeros(shape, np.uint16)
+    slots = np.concatenate([
+        np.array([oracle.slot_for_position(tb.block_ids[f:], tb.block_size, t)
+                  for t in range(int(n))], np.int64) for f, n, _, _ in tb.chunks])
+    oracle.kv_append(hk, hv, wl.to_numpy_storage(tb.k_rows), wl.to_numpy_storage(tb.v_rows), slots)
+    q = wl.to_numpy_storage(tb.q)
+    row = kv_row_bytes_dims(tb.num_kv_heads, tb.head_dim, 2)
+    done, el, nbytes = 0, 0.0, 0.0
+    while el < seconds and done < tb.num_seqs:
+        r = done
+        mine = [c for c in tb.chunks if c[2] <= r < c[3]]
+        sub = np.array([(f, n, 0, 1) for f, n, _, _ in mine], np.int32)
+        t0 = time.perf_counter()
+        oracle.chunk_tree(np.ascontiguousarray(q[r:r + 1]), hk, hv, sub, tb.block_ids, tb.scale,
+                          nthreads=nthreads)
+        el += time.perf_counter() - t0
+        nbytes += sum(int(n) for _, n, _, _ in mine) * row
+        done += 1
+    return {"value": nbytes / el / 1e9, "unit": "GB/s (logical K/V)", "cores": nthreads,
+            "kind": "oracle",
+            "sample": f"{done} of {tb.num_seqs} requests, all heads, whole path, fp64 oracle"}
+
+
 # ------------------------------------------------------------------ churn trace
 def run_churn(args, rank, world, local):
     """256 concurrent requests; each step appends one row per request, then
@@ -704,6 +866,10 @@ def main():
         res, sp = run_shared(args, rank, world, local)
         if rank == 0 and not args.no_cpu_baseline and world == 1:
             res["cpu_baseline"] = shared_cpu_baseline(sp, args.cpu_sample_seconds)
+    elif args.workload == "tree":
+        res, tb = run_tree(args, rank, world, local)
+        if rank == 0 and not args.no_cpu_baseline and world == 1:
+            res["cpu_baseline"] = tree_cpu_baseline(tb, args.cpu_sample_seconds)
     elif args.workload == "churn":
         res, b = run_churn(args, rank, world, local)
         if rank == 0 and not args.no_cpu_baseline and world == 1:

@@ -238,6 +238,91 @@ pkv_status pkv_prefix_attention_states(const pkv_cache_desc* cache,
                                        int32_t num_seqs, int32_t num_q_heads,
                                        float scale, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Attention over a prefix tree (multi-level shared prefixes).
+ *
+ * A batch whose sequences share prefixes at several levels is described as a
+ * tree snapshot ("M5.3 - KV Memory Layout and Exact Reuse", 0x0BB): an
+ * ordered list of chunks, parents before children, each holding some K/V
+ * rows in pool blocks and covering a half-open interval of sequence indices.
+ * Sequence r's keys are the rows of every chunk whose interval holds r (its
+ * root-to-leaf path); the result is exact attention of q[r] over them, as if
+ * the path were one contiguous history (0x0BE's reference schedule).
+ *
+ * Execution follows ChunkAttention's two phases (0x0BD), and Hydragen's
+ * batched attention per shared chunk (0x0BC):
+ *   - chunk-first: a chunk covering more than `threshold` sequences is
+ *     attended once for all of them, on the tensor cores (every covered
+ *     sequence's G query heads against the chunk's keys, split in 128-key
+ *     tiles); its partial softmax states are kept in the workspace;
+ *   - sequence-first: every other (sequence, chunk) pair runs through the
+ *     paged decode as one segment, leaving one state;
+ *   - a merge kernel combines each sequence's states by log-sum-exp (0x0BA).
+ * threshold = 0 attends every chunk chunk-first (hierarchical Hydragen);
+ * a threshold >= the batch size attends everything sequence-first.  The
+ * chunk-first phase needs bf16, head_dim 64 or 128, Hq / Hkv in {1, 2, 4,
+ * 8} and 128 % P == 0 or P % 128 == 0; for other caches every chunk is
+ * attended sequence-first.
+ *
+ * The snapshot is planned on the host into an opaque byte plan (the
+ * metadata ChunkAttention builds on the host and transfers: chunk-first
+ * work items and block ids, the decode's segment tables, each sequence's
+ * state list).  The caller copies the plan verbatim to device memory and
+ * passes both copies to pkv_chunk_tree_attention; a plan is valid for any
+ * q, K/V contents and scale, as long as the tree, the pool shape and the
+ * device it was planned on (SM count) stay the same. */
+
+/* One chunk of a tree snapshot (host struct). */
+typedef struct {
+  int32_t first_id;  /* index in block_ids of the chunk's first block          */
+  int32_t len;       /* K/V rows, >= 1: row t is in block                       */
+                     /* block_ids[first_id + t / P] at offset t % P             */
+  int32_t seq_begin; /* covered sequences: [seq_begin, seq_end), non-empty     */
+  int32_t seq_end;
+} pkv_chunk;
+
+/* Plan a tree snapshot.
+ *   chunks:        HOST [num_chunks], in tree order (parents first; any
+ *                  order gives the same result up to rounding).
+ *   block_ids:     HOST int32 [num_block_ids], every id in [0, num_blocks).
+ *                  A chunk owns its blocks: a chunk whose len is not a
+ *                  multiple of P leaves the rest of its last block unread.
+ *   threshold:     chunks covering more than this many sequences go
+ *                  chunk-first; < 0 picks 1 (every shared chunk).
+ *   plan:          HOST buffer of plan_capacity bytes, or NULL to query the
+ *                  sizes only.
+ *   plan_bytes:    out (may be NULL): the plan's size.
+ *   workspace_bytes: out (may be NULL): the device workspace
+ *                  pkv_chunk_tree_attention needs.
+ * Returns PKV_ERR_INVALID_ARG for a chunk with len < 1, an empty or
+ * out-of-range interval, ids past num_block_ids or a block id outside the
+ * pool; PKV_ERR_CAPACITY (sizes still reported) when plan_capacity is too
+ * small.  Planning reads the device's SM count (the current device). */
+pkv_status pkv_chunk_tree_plan(const pkv_cache_desc* cache, const pkv_chunk* chunks,
+                               int32_t num_chunks, const int32_t* block_ids,
+                               int64_t num_block_ids, int32_t num_seqs,
+                               int32_t num_q_heads, int32_t threshold, void* plan,
+                               size_t plan_capacity, size_t* plan_bytes,
+                               size_t* workspace_bytes);
+
+/* Attention over a planned tree snapshot.
+ *   out:           [num_seqs, Hq, D] (cache dtype); a sequence no chunk
+ *                  covers gets 0.
+ *   lse:           fp32 [num_seqs, Hq] natural-log LSE (-inf for an empty
+ *                  path), or NULL.
+ *   q:             [num_seqs, Hq, D]; scale as in the decode.
+ *   plan_host:     the plan as pkv_chunk_tree_plan wrote it (HOST).
+ *   plan_device:   the same bytes in device memory, 256-byte aligned.
+ *   workspace:     at least the planned workspace_bytes, 256-byte aligned.
+ * Returns PKV_ERR_INVALID_ARG when the plan does not describe this cache,
+ * num_seqs and num_q_heads (it checks the plan's header), or for a
+ * workspace that is too small. */
+pkv_status pkv_chunk_tree_attention(const pkv_cache_desc* cache, void* out, float* lse,
+                                    const void* q, const void* k_cache, const void* v_cache,
+                                    int32_t num_seqs, int32_t num_q_heads, float scale,
+                                    const void* plan_host, const void* plan_device,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
 /* Capacity in bytes of the library-owned scratch array used by
  * pkv_paged_attention_decode_static (16 MiB on every device that loads the
  * library, held until the process exits). */

@@ -26,6 +26,7 @@ CUDA_SOURCES = [
     "kernels/decode.cu",
     "kernels/decode_tc.cu",
     "kernels/prefix_tc.cu",
+    "kernels/tree.cu",
 ]
 # Attention kernels take exp2/log2/division from the hardware approximations
 # (softmax in base 2, well inside the attention tolerance).
@@ -33,6 +34,7 @@ PER_SOURCE_FLAGS = {
     "kernels/decode.cu": ["--use_fast_math"],
     "kernels/decode_tc.cu": ["--use_fast_math"],
     "kernels/prefix_tc.cu": ["--use_fast_math"],
+    "kernels/tree.cu": ["--use_fast_math"],
 }
 
 LIB = os.path.join(HERE, "libpkv.so")

@@ -348,8 +348,9 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
     const T* kt = tiles + (size_t)s * 2 * L.tile_elems;
     const T* vt = kt + L.tile_elems;
     if (flags & kPieceStart) {
+      const int64_t qr = a.q_rows ? __ldg(a.q_rows + dsc.x) : dsc.x;
       const T* qp = static_cast<const T*>(a.q) +
-                    ((int64_t)dsc.x * a.num_q_heads + (int64_t)dsc.y * G) * D + l16 * EPL;
+                    (qr * a.num_q_heads + (int64_t)dsc.y * G) * D + l16 * EPL;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         float f[EPL];
@@ -484,7 +485,9 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) 
     c_first = (int)(seg0 / wct);
     const int c_last = (int)((seg0 + nt - 1) / wct);
     if (c_first == c_last) {
-      if (!a.st_o) return;  // written whole by its CTA
+      // written whole by its CTA: to out, or to its state slot, which is
+      // already the result when only states are wanted and none merge in
+      if (!a.st_o || (!a.out && n_ext == 0)) return;
       whole_state = true;
     } else {
       n_pc = c_last - c_first + 1;
@@ -523,6 +526,14 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) 
     }
   }
   const bool nonempty = Lsum > 0.f;
+  if (!a.out) {  // states only: the merged pieces become the segment's state
+    const int64_t slot = rh * a.st_stride + a.st_slot;
+    float* so = a.st_o + slot * D + lane * EPL;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) so[e] = nonempty ? acc[e] / Lsum : 0.f;
+    if (lane == 0) a.st_lse[slot] = nonempty ? M + log2f(Lsum) : -INFINITY;
+    return;
+  }
   T* out = static_cast<T*>(a.out) + rh * D + lane * EPL;
 #pragma unroll
   for (int e = 0; e < EPL; ++e) store_out(out + e, nonempty ? acc[e] / Lsum : 0.f);

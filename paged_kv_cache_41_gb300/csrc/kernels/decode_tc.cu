@@ -15,6 +15,8 @@
 //         S^T [128 keys x 16]  = K_tile [128 x 128] . Q^T
 //         O^T [128 d    x 16] += V_tile^T . P^T    (V consumed MN-major)
 //     with bf16 operands, fp32 accumulators in TMEM (S^T double-buffered);
+//     P^T goes in as two bf16 terms, hi + lo, so the weights keep about 16
+//     bits (two PV MMAs per stage: the tensor pipe has room to spare);
 //   * the work split, the pieces and their records are those of decode.cu
 //     with 128-row stages: one persistent CTA per SM takes an equal share of
 //     the stages of every (sequence, kv head) segment, writes whole segments
@@ -53,10 +55,18 @@ constexpr int kTcTile = kTcRows * kTcD * 2;   // 32 KiB: one K (or V) tile
 constexpr int kTcHalf = kTcRows * 128;        // 16 KiB: 64 columns of a tile
 constexpr int kQBytes = kTcN * kTcD * 2;      // 4 KiB: Q (or P^T) as 16 rows x 128
 constexpr int kQHalf = kTcN * 128;            // 2 KiB: 64 columns of it
-constexpr int kTcSmem = kTcStages * 2 * kTcTile + 3 * kQBytes + 1024;  // +1024: alignment
+// Q buffers, one per piece in turn.  A piece's Q is loaded with its first
+// stage; with kTcStages ring stages the producer runs at most that many
+// stages ahead, and a third piece after p starts at least three stages after
+// p's last one, once the ring wait has seen p's last QK complete.  Two
+// buffers would let a CTA's third stage overwrite its first piece's Q before
+// that piece's QK has run.
+constexpr int kQBufs = 3;
+// Q[kQBufs], then P^T as two bf16 terms (hi, lo)
+constexpr int kTcSmem = kTcStages * 2 * kTcTile + (kQBufs + 2) * kQBytes + 1024;  // +1024: alignment
 constexpr float kLn2f = 0.6931471805599453f;
 
-// Stage descriptor flags (as in decode.cu); bit 4 holds the Q buffer.
+// Stage descriptor flags (as in decode.cu); bits 4-5 hold the Q buffer.
 constexpr int kStart = 1, kEnd = 2, kWholeSeg = 4, kSlotOne = 8;
 
 }  // namespace
@@ -92,12 +102,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // Align by offsetting the array itself, so accesses stay in shared space.
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   unsigned char* ring = sm;                            // [stage][K tile, V tile]
-  unsigned char* qs = ring + kTcStages * 2 * kTcTile;  // Q[2] (one per piece parity)
-  unsigned char* pt = qs + 2 * kQBytes;                // P^T
+  unsigned char* qs = ring + kTcStages * 2 * kTcTile;  // Q[kQBufs], one per piece in turn
+  unsigned char* pt = qs + kQBufs * kQBytes;           // P^T: hi term, then lo term
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   // rows G..15 of Q and P^T stay zero: the padding of the MMA's N
-  for (int i = t; i < 3 * kQBytes / 16; i += kTcThreads)
+  for (int i = t; i < (kQBufs + 2) * kQBytes / 16; i += kTcThreads)
     reinterpret_cast<uint4*>(qs)[i] = make_uint4(0u, 0u, 0u, 0u);
   if (t == 0) {
     for (int s = 0; s < kTcStages; ++s) {
@@ -153,7 +163,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool start = k == 0 || i == 0;
       const bool end = k == n - 1 || i == nt - 1;
       if (start) ++pieces;
-      const int qb = (pieces - 1) & 1;
+      const int qb = (pieces - 1) % kQBufs;
       const int flags = (start ? kStart : 0) | (end ? kEnd : 0) |
                         (end && i == nt - 1 && dseg >= 0 ? kWholeSeg : 0) |
                         (dseg > 0 ? kSlotOne : 0) | (qb << 4);
@@ -185,7 +195,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (start && lane == 0) {
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf)
-          tma_load_3d(qs + qb * kQBytes + hf * kQHalf, &tmq, hf * 64, h * G, r, &full[s]);
+          tma_load_3d(qs + qb * kQBytes + hf * kQHalf, &tmq, hf * 64, h * G,
+                      a.q_rows ? __ldg(a.q_rows + r) : r, &full[s]);
       }
       issued = k + 1;
       if (k + 1 < n && ++i == nt) {  // on to the next non-empty segment
@@ -214,13 +225,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           return false;
         tc::fence_after_sync();
         const uint32_t vb = smem_u32(ring + (size_t)(j % kTcStages) * 2 * kTcTile + kTcTile);
-        const uint32_t pb = smem_u32(pt);
+        // P^T = hi + lo: both terms through the same V tile
 #pragma unroll
-        for (int kk = 0; kk < kTcRows / 16; ++kk) {
-          // V MN-major: 64-column d chunks kTcHalf apart, 8-key groups 1 KiB apart
-          const uint64_t ad = tc::smem_desc_sw128(vb + kk * 2048, kTcHalf, 1024);
-          const uint64_t bd = tc::smem_desc_sw128(pb + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
-          tc::mma_bf16(tmem + 32, ad, bd, kIdPV, (kk > 0 || !(fl & kStart)) ? 1u : 0u);
+        for (int term = 0; term < 2; ++term) {
+          const uint32_t pb = smem_u32(pt + term * kQBytes);
+#pragma unroll
+          for (int kk = 0; kk < kTcRows / 16; ++kk) {
+            // V MN-major: 64-column d chunks kTcHalf apart, 8-key groups 1 KiB apart
+            const uint64_t ad = tc::smem_desc_sw128(vb + kk * 2048, kTcHalf, 1024);
+            const uint64_t bd =
+                tc::smem_desc_sw128(pb + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
+            tc::mma_bf16(tmem + 32, ad, bd, kIdPV,
+                         (term > 0 || kk > 0 || !(fl & kStart)) ? 1u : 0u);
+          }
         }
         tc::commit(&ofull);
         tc::commit(&kvfree[j % kTcStages]);
@@ -237,7 +254,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::fence_after_sync();
         const int fl = sdesc[s].w;
         const uint32_t kb = smem_u32(ring + (size_t)s * 2 * kTcTile);
-        const uint32_t qb = smem_u32(qs + ((fl >> 4) & 1) * kQBytes);
+        const uint32_t qb = smem_u32(qs + ((fl >> 4) & 3) * kQBytes);
 #pragma unroll
         for (int kk = 0; kk < kTcD / 16; ++kk) {
           const uint64_t ad = tc::smem_desc_sw128(kb + (kk >> 2) * kTcHalf + (kk & 3) * 32, 16, 1024);
@@ -345,13 +362,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc::wait_st();
         }
       }
-      // ---- P^T[g][row] in bf16: K-major, 128-byte swizzle, 64-key halves
+      // ---- P^T[g][row] as two bf16 terms, p = hi + lo to about 2^-17
+      // relative (one bf16 term alone errs by up to 2^-9 per weight, which a
+      // few keys of opposite-signed values can lift to the attention
+      // tolerance): K-major, 128-byte swizzle, 64-key halves
       {
         const int hf = row >> 6, cch = (row & 63) >> 3, e = row & 7;
 #pragma unroll
-        for (int g = 0; g < G; ++g)
-          *reinterpret_cast<__nv_bfloat16*>(pt + hf * kQHalf + g * 128 + ((cch ^ (g & 7)) << 4) +
-                                            e * 2) = __float2bfloat16_rn(p[g]);
+        for (int g = 0; g < G; ++g) {
+          const __nv_bfloat16 hi = __float2bfloat16_rn(p[g]);
+          const __nv_bfloat16 lo = __float2bfloat16_rn(p[g] - __bfloat162float(hi));
+          unsigned char* at = pt + hf * kQHalf + g * 128 + ((cch ^ (g & 7)) << 4) + e * 2;
+          *reinterpret_cast<__nv_bfloat16*>(at) = hi;
+          *reinterpret_cast<__nv_bfloat16*>(at + kQBytes) = lo;
+        }
       }
       if (row >= nvalid) {  // zero this row of V: its weight is 0, its bytes may be NaN
         unsigned char* vrow = ring + (size_t)s * 2 * kTcTile + kTcTile + row * 128;

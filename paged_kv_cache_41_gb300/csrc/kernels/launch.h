@@ -76,7 +76,8 @@ __host__ __device__ constexpr int box_rows_for(int block_size) {
 // record per piece, slot 0 of its CTA for the piece holding the CTA's first
 // stage and slot 1 for a last piece that is not also the first.
 struct DecodeArgs {
-  const void* q;                // [B, Hq, D]
+  const void* q;                // [B_q, Hq, D]
+  const int32_t* q_rows;        // [B] query row of each sequence, or null: row r
   const int32_t* block_tables;  // [B, max_blocks]
   const int32_t* seq_lens;      // [B]
   void* out;                    // [B, Hq, D]
@@ -87,8 +88,9 @@ struct DecodeArgs {
   float* rec_lse;               // [2C, G] piece LSEs, base 2
   // States mode (shared prefix): a whole segment writes (O, LSE base 2) to
   // slot st_slot of st_o / st_lse instead of out, and the reduction also
-  // merges the st_slot extra states held in slots [0, st_slot).  Plain
-  // decode: st_o == nullptr.
+  // merges the st_slot extra states held in slots [0, st_slot).  With out ==
+  // nullptr as well (states only), the reduction writes its merge to slot
+  // st_slot instead of out.  Plain decode: st_o == nullptr.
   float* st_o;                  // [B, Hq, st_stride, D]
   float* st_lse;                // [B, Hq, st_stride]
   int32_t st_stride;
@@ -129,11 +131,27 @@ cudaError_t launch_paged_decode_tc(const CUtensorMap& tmk, const CUtensorMap& tm
                                    const CUtensorMap& tmq, const DecodeArgs& args,
                                    cudaStream_t stream);
 
+// One CTA's work when the prefix kernel runs over a list of chunks (the
+// chunk-first phase of a prefix tree): one key split of one chunk against up
+// to two 128-row query tiles of the sequences the chunk covers.
+struct PrefixItem {
+  int32_t ids_off;  // index in prefix_block_ids of the chunk's first block
+  int32_t key0;     // first key of the split, counted from the chunk's start
+  int32_t nkeys;    // keys in the split (>= 1)
+  int32_t req0;     // q row (sequence) of query tile A's first request
+  int32_t nreq;     // requests of the pair, <= 2 * 128 / G (tile B iff > 128 / G)
+  int32_t st_req0;  // state row of tile A's first request
+  int32_t split;    // state slot
+  int32_t pad;
+};
+
 // Arguments of the shared-prefix tensor-core kernel.  Grid: (key split,
-// 128-row query tile, kv head).  Its states go to slots [0, num_splits) of
-// [B, Hq, parts_stride] state arrays.
+// 128-row query tile pair, kv head) over one prefix, or (item, 1, kv head)
+// with an item list.  Its states go to slots [0, num_splits) of
+// [rows, Hq, parts_stride] state arrays.
 struct PrefixArgs {
-  const int32_t* prefix_block_ids;  // [ceil(prefix_len / P)]
+  const int32_t* prefix_block_ids;  // [ceil(prefix_len / P)], or every chunk's ids
+  const PrefixItem* items;          // [num_items], or null: one prefix over all sequences
   float* part_o;                    // [B, Hq, parts_stride, D]
   float* part_lse;                  // [B, Hq, parts_stride], base 2
   unsigned int* err;
@@ -145,9 +163,31 @@ struct PrefixArgs {
   int32_t prefix_len;
   int32_t split_len;     // keys per split, a multiple of 128
   int32_t parts_stride;
+  int32_t num_items;
   float qscale;          // softmax scale * log2(e)
   float lse_scale;       // 1: LSE in base 2 (partial states); ln 2: natural log
 };
+
+// Arguments of the merge at the end of attention over a prefix tree.  The
+// states: chunk-first rows [0, cf_rows) at ((row * Hq + h) * s_max + split),
+// then one state per later row at (cf_rows * Hq * s_max + (row - cf_rows) *
+// Hq + h); O fp32 [.., D], LSE base 2.  Sequence r merges the states of
+// entries [seq_ptr[r], seq_ptr[r + 1]), entry (row, n) naming n slots of a
+// row.
+struct TreeMergeArgs {
+  const float* st_o;
+  const float* st_lse;
+  const int32_t* seq_ptr;  // [B + 1]
+  const int2* entries;     // [seq_ptr[B]]
+  void* out;               // [B, Hq, D]
+  float* lse_out;          // [B, Hq] natural log, or null
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t cf_rows;
+  int32_t s_max;
+};
+cudaError_t launch_tree_merge(int dtype, int head_dim, const TreeMergeArgs& args,
+                              cudaStream_t stream);
 
 // Query rows per CTA and keys per tile of the prefix kernel.
 constexpr int kPrefixRows = 128;

@@ -82,14 +82,33 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
   constexpr uint32_t kIdPV = tc::idesc_bf16_f32(kPrefixRows, D, 0, 1);
 
   pdl_launch_dependents();  // the suffix decode may be scheduled as SMs free up
-  const int split = blockIdx.x, mp = blockIdx.y, kvh = blockIdx.z;
+  const int kvh = blockIdx.z;
   const int P = a.block_size;
-  const int key0 = split * a.split_len;
-  const int nkeys = min(a.split_len, a.prefix_len - key0);
-  if (nkeys <= 0) return;
+  // This CTA's keys and query rows: key split blockIdx.x of the one prefix
+  // over the query-tile pair blockIdx.y, or item blockIdx.x of a chunk list.
+  int split, ids_off, key0, nkeys, req0, nreq, st_req0;
+  if (a.items) {
+    const int4 w0 = __ldg(reinterpret_cast<const int4*>(a.items + blockIdx.x));
+    const int4 w1 = __ldg(reinterpret_cast<const int4*>(a.items + blockIdx.x) + 1);
+    ids_off = w0.x;
+    key0 = w0.y;
+    nkeys = w0.z;
+    req0 = w0.w;
+    nreq = w1.x;
+    st_req0 = w1.y;
+    split = w1.z;
+  } else {
+    split = blockIdx.x;
+    ids_off = 0;
+    key0 = split * a.split_len;
+    nkeys = min(a.split_len, a.prefix_len - key0);
+    req0 = 2 * (int)blockIdx.y * RPB;
+    nreq = min(a.num_seqs - req0, 2 * RPB);
+    st_req0 = req0;
+  }
+  if (nkeys <= 0 || nreq <= 0) return;
   const int J = (nkeys + kPrefixKeys - 1) / kPrefixKeys;
-  const int m_tiles = (a.num_seqs * G + kPrefixRows - 1) / kPrefixRows;
-  const bool hasB = 2 * mp + 1 < m_tiles;  // the pair's second query tile holds rows
+  const bool hasB = nreq > RPB;  // the pair's second query tile holds rows
 
   extern __shared__ unsigned char smem_raw[];
   // Align by offsetting the array itself (not through an integer), so the
@@ -118,7 +137,7 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
   auto box_block = [&](int jt) -> int2 {  // (block, first row) of this lane's box of tile jt
     const int key = key0 + jt * kPrefixKeys + bsub * PB;
     if (lane >= nbox || jt >= J || key >= key0 + nkeys) return make_int2(kZeroFill, 0);
-    return make_int2(__ldg(a.prefix_block_ids + key / P), key % P);
+    return make_int2(__ldg(a.prefix_block_ids + ids_off + key / P), key % P);
   };
   int2 box0 = make_int2(0, 0), box1 = make_int2(0, 0);
   if (warp == 9) {
@@ -144,7 +163,7 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     mbar_arrive_expect_tx(&qbar[0], kTile);
 #pragma unroll
     for (int h = 0; h < H; ++h)
-      tma_load_3d(qs + h * kHalfBytes, &tmq, h * 64, kvh * G, 2 * mp * RPB, &qbar[0]);
+      tma_load_3d(qs + h * kHalfBytes, &tmq, h * 64, kvh * G, req0, &qbar[0]);
   }
   __syncthreads();  // barriers initialised: the producer starts streaming now
   // Every warp but the producer waits for the TMEM allocation.
@@ -195,7 +214,7 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
           mbar_arrive_expect_tx(&qbar[1], kTile);
 #pragma unroll
           for (int h = 0; h < H; ++h)
-            tma_load_3d(qs + kTile + h * kHalfBytes, &tmq, h * 64, kvh * G, (2 * mp + 1) * RPB,
+            tma_load_3d(qs + kTile + h * kHalfBytes, &tmq, h * 64, kvh * G, req0 + RPB,
                         &qbar[1]);
         }
       }
@@ -326,6 +345,21 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
         const int prev = hasB ? w - 1 : j - 1;  // completions of pfree so far
         if (!mbar_wait(&pfree, prev & 1)) { ok = false; break; }
       }
+      if (x == 0 && kvalid < kPrefixKeys) {
+        // The split's last tile ends inside it.  Rows past the last key hold
+        // a zero-filled box, or the stale rest of a chunk's last block: P is
+        // 0 there, but 0 * NaN is not, so clear those V rows before the PVs
+        // read the tile (tile A's PV is issued after this group's P).
+        if (!mbar_wait(&vfull[j & 1], (j >> 1) & 1)) { ok = false; break; }
+        if (row >= kvalid) {
+#pragma unroll
+          for (int h = 0; h < H; ++h) {
+            uint4* vr = reinterpret_cast<uint4*>(vs + (j & 1) * kTile + h * kHalfBytes + row * 128);
+#pragma unroll
+            for (int c16 = 0; c16 < 8; ++c16) vr[c16] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+      }
 #pragma unroll
       for (int ch = 0; ch < kPrefixKeys / 8; ++ch) {
         const int hf = ch >> 3, cc = ch & 7;
@@ -342,13 +376,12 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     const bool done = ok && mbar_wait(&ofull[x], (J - 1) & 1);
     tc::fence_after_sync();
     if (!done && lane == 0) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
-    const int mt = 2 * mp + x;
-    const int r = mt * RPB + row / G;
+    const int rr = x * RPB + row / G;  // request of the pair
     const int g = row % G;
-    const bool row_ok = done && r < a.num_seqs;
+    const bool row_ok = done && rr < nreq;
     const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
     const int64_t slot =
-        ((int64_t)r * a.num_q_heads + (int64_t)kvh * G + g) * a.parts_stride + split;
+        ((int64_t)(st_req0 + rr) * a.num_q_heads + (int64_t)kvh * G + g) * a.parts_stride + split;
     // O row -> registers 32 columns at a time, scaled, into an idle stage
     // pair (tile A: the K stages, every QK^T has completed; tile B: the V
     // stages, its last PV has completed) as D / 32 planes of [128 rows][32
@@ -375,7 +408,8 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     if (row == 0) {
 #pragma unroll
       for (int plane = 0; plane < D / 32; ++plane)
-        tma_store_5d(&tmo, plane * 32, split, 0, kvh, mt * RPB, stage + plane * kPlaneBytes);
+        tma_store_5d(&tmo, plane * 32, split, 0, kvh, st_req0 + x * RPB,
+                     stage + plane * kPlaneBytes);
       bulk_commit_group();
       bulk_wait_group_read0();
     }
@@ -396,7 +430,10 @@ static cudaError_t launch_prefix_t(int num_splits, const CUtensorMap& tmq, const
   cudaError_t e = ensure_smem_limit(kern, (int)smem, attr_cache);
   if (e != cudaSuccess) return e;
   const int m_tiles = (a.num_seqs * G + kPrefixRows - 1) / kPrefixRows;
-  dim3 grid((unsigned)num_splits, (unsigned)((m_tiles + 1) / 2), (unsigned)a.num_kv_heads);
+  const dim3 grid = a.items
+                        ? dim3((unsigned)a.num_items, 1u, (unsigned)a.num_kv_heads)
+                        : dim3((unsigned)num_splits, (unsigned)((m_tiles + 1) / 2),
+                               (unsigned)a.num_kv_heads);
   kern<<<grid, kPrefixThreads, smem, stream>>>(tmq, tmk, tmv, tmo, a);
   return cudaGetLastError();
 }

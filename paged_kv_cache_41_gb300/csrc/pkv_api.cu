@@ -7,7 +7,9 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "kernels/launch.h"
 #include "pkv.h"
@@ -208,7 +210,8 @@ pkv_status encode_cache_map_sw128(CUtensorMap* map, const pkv_cache_desc* c, con
 // Encode the maps and launch the decode (partial kernel + reduction) on the
 // path use_tc_decode picks.
 pkv_status launch_decode(const pkv_cache_desc* cache, int G, const void* q, const void* k_cache,
-                         const void* v_cache, const pkv::DecodeArgs& a, cudaStream_t stream) {
+                         const void* v_cache, const pkv::DecodeArgs& a, cudaStream_t stream,
+                         int32_t q_seqs = 0) {
   pkv_status st;
   CUtensorMap tmk, tmv;
   cudaError_t e;
@@ -218,7 +221,8 @@ pkv_status launch_decode(const pkv_cache_desc* cache, int G, const void* q, cons
     CUtensorMap tmq;
     if ((st = encode_cache_map_sw128(&tmk, cache, k_cache, rows)) != PKV_OK) return st;
     if ((st = encode_cache_map_sw128(&tmv, cache, v_cache, rows)) != PKV_OK) return st;
-    if ((st = encode_q_map_sw128(&tmq, q, a.num_seqs, a.num_q_heads, cache->head_dim, G, 1)) !=
+    if ((st = encode_q_map_sw128(&tmq, q, q_seqs > 0 ? q_seqs : a.num_seqs, a.num_q_heads,
+                                 cache->head_dim, G, 1)) !=
         PKV_OK)
       return st;
     e = pkv::launch_paged_decode_tc(tmk, tmv, tmq, a, stream);
@@ -743,6 +747,345 @@ pkv_status pkv_paged_attention_decode_static(
   return pkv_paged_attention_decode(cache, out, lse, q, k_cache, v_cache, block_tables,
                                     max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, scale,
                                     partition_size, scratch, need, stream);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Attention over a prefix tree ("M5.3 - KV Memory Layout and Exact Reuse",
+// 0x0BB-0x0BE).  The host plans the snapshot into one byte blob: a header,
+// then 256-byte aligned sections
+//   items    PrefixItem [n_items]       chunk-first work (tensor cores)
+//   cf_ids   int32 [..]                 block ids of the chunk-first chunks
+//   ptab     int32 [n_pseudo, pmax]     block table of each sequence-first
+//                                       (sequence, chunk) segment, -1 padded
+//   plen     int32 [n_pseudo]           its rows
+//   pq       int32 [n_pseudo]           its sequence (q row)
+//   seq_ptr  int32 [B + 1]              CSR over entries, per sequence
+//   entries  int2 [n_entries]           (state row, slots): chunk-first rows
+//                                       first, then one row per segment
+// and sizes the device workspace: chunk-first states [cf_rows, Hq, s_max]
+// followed by segment states [n_pseudo, Hq] (O fp32 [.., D] in one array,
+// LSE base 2 in another), then the paged decode's plan and piece records.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr uint32_t kTreePlanMagic = 0x54564B50u;  // bytes "PKVT"
+constexpr uint32_t kTreePlanVersion = 1;
+constexpr size_t kTreePlanHeader = 256;
+
+struct TreePlanHeader {
+  uint32_t magic, version;
+  int64_t num_blocks;
+  int32_t block_size, num_kv_heads, head_dim, dtype;
+  int32_t num_seqs, num_q_heads;
+  int32_t n_items, s_max, cf_rows, n_pseudo, pseudo_max_blocks, n_entries;
+  int64_t decode_ctas;
+  uint64_t items_off, cf_ids_off, ptab_off, plen_off, pq_off, seqptr_off, entries_off, plan_bytes;
+  uint64_t ws_lse_off, ws_dec_off, ws_bytes;
+  uint64_t dec_pre_off, dec_lse_off, dec_o_off, dec_total;
+};
+static_assert(sizeof(TreePlanHeader) <= kTreePlanHeader, "plan header fits its section");
+
+// The chunk-first phase's shapes: bf16 tensor cores, whole or sliced blocks
+// per 128-key tile.
+bool prefix_tc_shape(const pkv_cache_desc* c, int32_t num_q_heads) {
+  if (check_attention_shape(c, num_q_heads) != PKV_OK || c->dtype != PKV_BF16) return false;
+  const int P = c->block_size;
+  return pkv::kPrefixKeys % P == 0 || P % pkv::kPrefixKeys == 0;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_chunk_tree_plan(const pkv_cache_desc* cache, const pkv_chunk* chunks,
+                               int32_t num_chunks, const int32_t* block_ids,
+                               int64_t num_block_ids, int32_t num_seqs, int32_t num_q_heads,
+                               int32_t threshold, void* plan, size_t plan_capacity,
+                               size_t* plan_bytes, size_t* workspace_bytes) {
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if ((st = check_attention_shape(cache, num_q_heads)) != PKV_OK) return st;
+  if (num_chunks < 0 || num_seqs < 0 || num_block_ids < 0) return PKV_ERR_INVALID_ARG;
+  if ((num_chunks > 0 && !chunks) || (num_block_ids > 0 && !block_ids)) return PKV_ERR_INVALID_ARG;
+  if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
+  const int64_t P = cache->block_size, Hkv = cache->num_kv_heads, Hq = num_q_heads;
+  const int G = num_q_heads / cache->num_kv_heads;
+  const int RPB = pkv::kPrefixRows / G;  // requests per 128-row query tile
+  for (int64_t i = 0; i < num_block_ids; ++i)
+    if (block_ids[i] < 0 || block_ids[i] >= cache->num_blocks) return PKV_ERR_INVALID_ARG;
+  const bool tc = prefix_tc_shape(cache, num_q_heads);
+  const int64_t thr = threshold < 0 ? 1 : threshold;
+
+  // ---- classify the chunks; lay out partial rows, ids and segments
+  std::vector<int64_t> where((size_t)num_chunks), ids_at((size_t)num_chunks);
+  std::vector<char> first((size_t)num_chunks);
+  int64_t cf_rows = 0, cf_ids = 0, n_pseudo = 0, pmax = 0, n_entries = 0, max_tiles = 0;
+  for (int32_t c = 0; c < num_chunks; ++c) {
+    const pkv_chunk& k = chunks[c];
+    if (k.len < 1 || k.seq_begin < 0 || k.seq_begin >= k.seq_end || k.seq_end > num_seqs ||
+        k.first_id < 0 || k.first_id + ceil_div(k.len, P) > num_block_ids)
+      return PKV_ERR_INVALID_ARG;
+    const int64_t cov = k.seq_end - k.seq_begin, nb = ceil_div(k.len, P);
+    n_entries += cov;
+    first[c] = tc && cov > thr;
+    if (first[c]) {
+      where[c] = cf_rows;  // a chunk's rows start a query tile: its stores stay inside
+      cf_rows += ceil_div(cov, RPB) * RPB;
+      ids_at[c] = cf_ids;
+      cf_ids += nb;
+      max_tiles = std::max(max_tiles, ceil_div(k.len, pkv::kPrefixKeys));
+    } else {
+      where[c] = n_pseudo;
+      n_pseudo += cov;
+      pmax = std::max(pmax, nb);
+    }
+  }
+  if (cf_rows > INT32_MAX || n_entries > INT32_MAX || cf_ids > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  if (n_pseudo > 65535) return PKV_ERR_UNSUPPORTED;
+
+  // ---- key split of the chunk-first phase: the fewest 128-key tiles per
+  // split whose (item x kv head) CTAs still fit one wave on the SMs
+  auto count_items = [&](int64_t per) {
+    int64_t items = 0;
+    for (int32_t c = 0; c < num_chunks; ++c)
+      if (first[c])
+        items += ceil_div(chunks[c].seq_end - chunks[c].seq_begin, 2 * RPB) *
+                 ceil_div(ceil_div(chunks[c].len, pkv::kPrefixKeys), per);
+    return items;
+  };
+  int64_t per = 1, n_items = 0, s_max = 0;
+  if (max_tiles > 0) {
+    int64_t lo = 1, hi = max_tiles;  // count_items does not grow with per
+    const int64_t wave = sm_count();
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) / 2;
+      if (count_items(mid) * Hkv <= wave) hi = mid; else lo = mid + 1;
+    }
+    per = lo;
+    n_items = count_items(per);
+    for (int32_t c = 0; c < num_chunks; ++c)
+      if (first[c]) s_max = std::max(s_max, ceil_div(chunks[c].len, per * pkv::kPrefixKeys));
+  }
+  if (n_items > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  const int64_t split_len = per * pkv::kPrefixKeys;
+
+  // ---- sizes
+  TreePlanHeader h{};
+  h.magic = kTreePlanMagic;
+  h.version = kTreePlanVersion;
+  h.num_blocks = cache->num_blocks;
+  h.block_size = cache->block_size;
+  h.num_kv_heads = cache->num_kv_heads;
+  h.head_dim = cache->head_dim;
+  h.dtype = cache->dtype;
+  h.num_seqs = num_seqs;
+  h.num_q_heads = num_q_heads;
+  h.n_items = (int32_t)n_items;
+  h.s_max = (int32_t)s_max;
+  h.cf_rows = (int32_t)cf_rows;
+  h.n_pseudo = (int32_t)n_pseudo;
+  h.pseudo_max_blocks = (int32_t)pmax;
+  h.n_entries = (int32_t)n_entries;
+  h.decode_ctas = n_pseudo > 0 ? decode_ctas(cache, (int32_t)n_pseudo, num_q_heads, (int32_t)pmax, 0)
+                               : 0;
+  if (h.decode_ctas > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  size_t off = kTreePlanHeader;
+  auto section = [&](uint64_t* at, size_t bytes) {
+    *at = off;
+    off += align256(bytes);
+  };
+  section(&h.items_off, (size_t)n_items * sizeof(pkv::PrefixItem));
+  section(&h.cf_ids_off, (size_t)cf_ids * 4);
+  section(&h.ptab_off, (size_t)(n_pseudo * pmax) * 4);
+  section(&h.plen_off, (size_t)n_pseudo * 4);
+  section(&h.pq_off, (size_t)n_pseudo * 4);
+  section(&h.seqptr_off, (size_t)(num_seqs + 1) * 4);
+  section(&h.entries_off, (size_t)n_entries * 8);
+  h.plan_bytes = off;
+  const int64_t n_states = cf_rows * Hq * s_max + n_pseudo * Hq;
+  h.ws_lse_off = align256((size_t)n_states * cache->head_dim * 4);
+  h.ws_dec_off = h.ws_lse_off + align256((size_t)n_states * 4);
+  DecodeWorkspace dw{};
+  if (n_pseudo > 0) dw = decode_workspace(n_pseudo, h.decode_ctas, G, cache->head_dim);
+  h.dec_pre_off = dw.pre_off;
+  h.dec_lse_off = dw.lse_off;
+  h.dec_o_off = dw.o_off;
+  h.dec_total = dw.total;
+  h.ws_bytes = h.ws_dec_off + dw.total;
+  if (plan_bytes) *plan_bytes = h.plan_bytes;
+  if (workspace_bytes) *workspace_bytes = h.ws_bytes;
+  if (!plan) return PKV_OK;
+  if (plan_capacity < h.plan_bytes) return PKV_ERR_CAPACITY;
+
+  // ---- fill
+  unsigned char* base = static_cast<unsigned char*>(plan);
+  memset(base, 0, h.plan_bytes);
+  memcpy(base, &h, sizeof(h));
+  auto* items = reinterpret_cast<pkv::PrefixItem*>(base + h.items_off);
+  auto* cfi = reinterpret_cast<int32_t*>(base + h.cf_ids_off);
+  auto* ptab = reinterpret_cast<int32_t*>(base + h.ptab_off);
+  auto* plen = reinterpret_cast<int32_t*>(base + h.plen_off);
+  auto* pq = reinterpret_cast<int32_t*>(base + h.pq_off);
+  auto* sptr = reinterpret_cast<int32_t*>(base + h.seqptr_off);
+  auto* ent = reinterpret_cast<int32_t*>(base + h.entries_off);
+  int64_t it = 0;
+  for (int32_t c = 0; c < num_chunks; ++c) {
+    const pkv_chunk& k = chunks[c];
+    const int64_t cov = k.seq_end - k.seq_begin, nb = ceil_div(k.len, P);
+    if (first[c]) {
+      memcpy(cfi + ids_at[c], block_ids + k.first_id, (size_t)nb * 4);
+      for (int64_t r0 = 0; r0 < cov; r0 += 2 * RPB)
+        for (int64_t key0 = 0; key0 < k.len; key0 += split_len) {
+          pkv::PrefixItem& w = items[it++];
+          w.ids_off = (int32_t)ids_at[c];
+          w.key0 = (int32_t)key0;
+          w.nkeys = (int32_t)std::min<int64_t>(split_len, k.len - key0);
+          w.req0 = (int32_t)(k.seq_begin + r0);
+          w.nreq = (int32_t)std::min<int64_t>(2 * RPB, cov - r0);
+          w.st_req0 = (int32_t)(where[c] + r0);
+          w.split = (int32_t)(key0 / split_len);
+        }
+    } else {
+      for (int64_t j = 0; j < cov; ++j) {
+        const int64_t p = where[c] + j;
+        int32_t* row = ptab + p * pmax;
+        memcpy(row, block_ids + k.first_id, (size_t)nb * 4);
+        for (int64_t b = nb; b < pmax; ++b) row[b] = -1;
+        plen[p] = k.len;
+        pq[p] = (int32_t)(k.seq_begin + j);
+      }
+    }
+  }
+  // longest work first: the CTAs launch in item order
+  std::stable_sort(items, items + n_items, [](const pkv::PrefixItem& x, const pkv::PrefixItem& y) {
+    return x.nkeys * (x.nreq + 0LL) > y.nkeys * (y.nreq + 0LL);
+  });
+  // each sequence's states, in tree order: count, then place
+  std::vector<int32_t> fill((size_t)num_seqs + 1, 0);
+  for (int32_t c = 0; c < num_chunks; ++c)
+    for (int32_t r = chunks[c].seq_begin; r < chunks[c].seq_end; ++r) ++fill[(size_t)r + 1];
+  for (int32_t r = 0; r < num_seqs; ++r) fill[(size_t)r + 1] += fill[(size_t)r];
+  memcpy(sptr, fill.data(), (size_t)(num_seqs + 1) * 4);
+  for (int32_t c = 0; c < num_chunks; ++c) {
+    const pkv_chunk& k = chunks[c];
+    for (int32_t r = k.seq_begin; r < k.seq_end; ++r) {
+      int32_t* e = ent + 2 * (int64_t)fill[(size_t)r]++;
+      if (first[c]) {
+        e[0] = (int32_t)(where[c] + (r - k.seq_begin));
+        e[1] = (int32_t)ceil_div(k.len, split_len);
+      } else {
+        e[0] = (int32_t)(cf_rows + where[c] + (r - k.seq_begin));
+        e[1] = 1;
+      }
+    }
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_chunk_tree_attention(const pkv_cache_desc* cache, void* out, float* lse,
+                                    const void* q, const void* k_cache, const void* v_cache,
+                                    int32_t num_seqs, int32_t num_q_heads, float scale,
+                                    const void* plan_host, const void* plan_device,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if ((st = check_attention_shape(cache, num_q_heads)) != PKV_OK) return st;
+  if (!plan_host || !plan_device || !isfinite(scale) || num_seqs < 0) return PKV_ERR_INVALID_ARG;
+  TreePlanHeader h;
+  memcpy(&h, plan_host, sizeof(h));
+  if (h.magic != kTreePlanMagic || h.version != kTreePlanVersion ||
+      h.num_blocks != cache->num_blocks || h.block_size != cache->block_size ||
+      h.num_kv_heads != cache->num_kv_heads || h.head_dim != cache->head_dim ||
+      h.dtype != cache->dtype || h.num_seqs != num_seqs || h.num_q_heads != num_q_heads)
+    return PKV_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(plan_device) & 255u) || workspace_bytes < h.ws_bytes ||
+      (h.ws_bytes > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))))
+    return PKV_ERR_INVALID_ARG;
+  unsigned int* err = device_error_word();
+  if (!err) return PKV_ERR_CUDA;
+  const int G = num_q_heads / cache->num_kv_heads;
+  const float qscale = scale * 1.4426950408889634f;
+  const unsigned char* dplan = static_cast<const unsigned char*>(plan_device);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  float* st_o = reinterpret_cast<float*>(ws);
+  float* st_lse = reinterpret_cast<float*>(ws + h.ws_lse_off);
+  const int64_t cf_states = (int64_t)h.cf_rows * num_q_heads * h.s_max;
+  cudaStream_t s = as_stream(stream);
+
+  if (h.n_items > 0) {  // chunk-first: every shared chunk on the tensor cores
+    CUtensorMap tmq, ptk, ptv, pto;
+    if ((st = encode_q_map_sw128(&tmq, q, num_seqs, num_q_heads, cache->head_dim, G,
+                                 pkv::kPrefixRows / G)) != PKV_OK)
+      return st;
+    if ((st = encode_prefix_maps(&ptk, &ptv, cache, k_cache, v_cache)) != PKV_OK) return st;
+    if ((st = encode_prefix_out_map(&pto, st_o, h.cf_rows, cache->num_kv_heads, G, h.s_max,
+                                    cache->head_dim)) != PKV_OK)
+      return st;
+    pkv::PrefixArgs pa{};
+    pa.prefix_block_ids = reinterpret_cast<const int32_t*>(dplan + h.cf_ids_off);
+    pa.items = reinterpret_cast<const pkv::PrefixItem*>(dplan + h.items_off);
+    pa.num_items = h.n_items;
+    pa.part_o = st_o;
+    pa.part_lse = st_lse;
+    pa.err = err;
+    pa.num_blocks = cache->num_blocks;
+    pa.num_seqs = num_seqs;
+    pa.num_q_heads = num_q_heads;
+    pa.num_kv_heads = cache->num_kv_heads;
+    pa.block_size = cache->block_size;
+    pa.parts_stride = h.s_max;
+    pa.qscale = qscale;
+    pa.lse_scale = 1.f;
+    if (pkv::launch_prefix_attention(cache->head_dim, G, 0, tmq, ptk, ptv, pto, pa, s) !=
+        cudaSuccess)
+      return PKV_ERR_CUDA;
+  }
+  if (h.n_pseudo > 0) {  // sequence-first: one decode segment per (sequence, chunk)
+    pkv::DecodeArgs a{};
+    a.q = q;
+    a.q_rows = reinterpret_cast<const int32_t*>(dplan + h.pq_off);
+    a.block_tables = reinterpret_cast<const int32_t*>(dplan + h.ptab_off);
+    a.seq_lens = reinterpret_cast<const int32_t*>(dplan + h.plen_off);
+    a.out = nullptr;  // states only
+    a.err = err;
+    DecodeWorkspace dw{h.dec_pre_off, h.dec_lse_off, h.dec_o_off, h.dec_total};
+    bind_decode_workspace(&a, ws + h.ws_dec_off, dw);
+    a.st_o = st_o + cf_states * cache->head_dim;
+    a.st_lse = st_lse + cf_states;
+    a.st_stride = 1;
+    a.st_slot = 0;
+    a.num_blocks = cache->num_blocks;
+    a.max_blocks = h.pseudo_max_blocks;
+    a.num_seqs = h.n_pseudo;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = cache->num_kv_heads;
+    a.block_size = cache->block_size;
+    a.num_ctas = (int32_t)h.decode_ctas;
+    a.num_stages = pkv::decode_num_stages(cache->head_dim, elem_bytes(cache->dtype));
+    a.qscale = qscale;
+    if ((st = launch_decode(cache, G, q, k_cache, v_cache, a, s, num_seqs)) != PKV_OK) return st;
+  }
+  pkv::TreeMergeArgs m{};
+  m.st_o = st_o;
+  m.st_lse = st_lse;
+  m.seq_ptr = reinterpret_cast<const int32_t*>(dplan + h.seqptr_off);
+  m.entries = reinterpret_cast<const int2*>(dplan + h.entries_off);
+  m.out = out;
+  m.lse_out = lse;
+  m.num_seqs = num_seqs;
+  m.num_q_heads = num_q_heads;
+  m.cf_rows = h.cf_rows;
+  m.s_max = h.s_max;
+  return pkv::launch_tree_merge(cache->dtype, cache->head_dim, m, s) == cudaSuccess ? PKV_OK
+                                                                                   : PKV_ERR_CUDA;
 }
 
 }  // extern "C"

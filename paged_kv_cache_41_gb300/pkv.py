@@ -10,6 +10,7 @@ from __future__ import annotations
 import ctypes
 import os
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -33,6 +34,8 @@ EXPORTED = [
     "pkv_shared_prefix_attention",
     "pkv_prefix_split_len",
     "pkv_prefix_attention_states",
+    "pkv_chunk_tree_plan",
+    "pkv_chunk_tree_attention",
     "pkv_get_device_error",
     "pkv_status_string",
 ]
@@ -89,6 +92,13 @@ def load_library():
     lib.pkv_prefix_attention_states.restype = ctypes.c_int
     lib.pkv_prefix_attention_states.argtypes = [dp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32,
                                                 vp]
+    lib.pkv_chunk_tree_plan.restype = ctypes.c_int
+    lib.pkv_chunk_tree_plan.argtypes = [dp, vp, i32, vp, i64, i32, i32, i32, vp, ctypes.c_size_t,
+                                        ctypes.POINTER(ctypes.c_size_t),
+                                        ctypes.POINTER(ctypes.c_size_t)]
+    lib.pkv_chunk_tree_attention.restype = ctypes.c_int
+    lib.pkv_chunk_tree_attention.argtypes = [dp, vp, vp, vp, vp, vp, i32, i32, f32, vp, vp, vp,
+                                             ctypes.c_size_t, vp]
     lib.pkv_get_device_error.restype = ctypes.c_int
     lib.pkv_get_device_error.argtypes = [ctypes.POINTER(i32), vp]
     lib.pkv_status_string.restype = ctypes.c_char_p
@@ -273,6 +283,70 @@ def prefix_attention_states(q, k_cache, v_cache, prefix_block_ids, prefix_len, s
         _ptr(v_cache), _ptr(prefix_block_ids), int(prefix_len), int(split_len), b, hq, float(scale),
         _stream(stream)), "pkv_prefix_attention_states")
     return states_o, states_lse, split_len
+
+
+class ChunkTreePlan:
+    """A planned prefix-tree snapshot (include/pkv.h): the plan's host bytes,
+    their device copy, and the workspace the attention needs."""
+
+    def __init__(self, host, device, workspace_bytes, num_seqs, num_q_heads):
+        self.host = host
+        self.device = device
+        self.workspace_bytes = workspace_bytes
+        self.num_seqs = num_seqs
+        self.num_q_heads = num_q_heads
+
+
+def chunk_tree_plan(k_cache, chunks, block_ids, num_seqs, num_q_heads, threshold=-1,
+                    device=None, host_buffer=None, device_buffer=None) -> ChunkTreePlan:
+    """Plan a tree snapshot.  ``chunks``: int [n, 4] rows (first id, rows,
+    seq begin, seq end) in tree order; ``block_ids``: int32 block ids; both
+    host data.  The plan's bytes are copied to ``device`` (default: the
+    cache's device) with torch.  A serving loop that re-plans every step can
+    pass uint8 buffers to reuse: ``host_buffer`` (pinned, so the copy is
+    asynchronous: do not re-plan into it before that copy has run) and
+    ``device_buffer``."""
+    desc = cache_desc(k_cache)
+    ch = np.ascontiguousarray(np.asarray(chunks, dtype=np.int32).reshape(-1, 4))
+    ids = np.ascontiguousarray(np.asarray(block_ids, dtype=np.int32).reshape(-1))
+    lib = load_library()
+    pb, wb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    args = (ctypes.byref(desc), ctypes.c_void_p(ch.ctypes.data), len(ch),
+            ctypes.c_void_p(ids.ctypes.data), ids.size, int(num_seqs), int(num_q_heads),
+            int(threshold))
+    _check(lib.pkv_chunk_tree_plan(*args, None, 0, ctypes.byref(pb), ctypes.byref(wb)),
+           "pkv_chunk_tree_plan")
+    n = pb.value
+    if host_buffer is not None and host_buffer.numel() >= n:
+        host = host_buffer[:n]
+    else:
+        host = torch.zeros(n, dtype=torch.uint8)
+    _check(lib.pkv_chunk_tree_plan(*args, _ptr(host), n, ctypes.byref(pb), ctypes.byref(wb)),
+           "pkv_chunk_tree_plan")
+    if device_buffer is not None and device_buffer.numel() >= n:
+        dev = device_buffer[:n]
+        dev.copy_(host, non_blocking=host.is_pinned())
+    else:
+        dev = host.to(device if device is not None else k_cache.device)
+    return ChunkTreePlan(host, dev, wb.value, int(num_seqs), int(num_q_heads))
+
+
+def chunk_tree_attention(q, k_cache, v_cache, plan: ChunkTreePlan, scale, *, out=None, lse=None,
+                         workspace=None, stream=None):
+    """Attention of every sequence over its path of the planned tree
+    (include/pkv.h).  Returns out [B, Hq, D]."""
+    desc = cache_desc(k_cache)
+    b, hq, _ = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None and plan.workspace_bytes:
+        workspace = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load_library().pkv_chunk_tree_attention(
+        ctypes.byref(desc), _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), b, hq,
+        float(scale), _ptr(plan.host), _ptr(plan.device), _ptr(workspace), ws_bytes,
+        _stream(stream)), "pkv_chunk_tree_attention")
+    return out
 
 
 def get_device_error(stream=None) -> int:

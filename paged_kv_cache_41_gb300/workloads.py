@@ -17,6 +17,7 @@ Workloads (sizes from the problem statement):
   head_dim 128, block size 16 or 64, shuffled placement.
 * ``churn``: 256 concurrent requests over 200 steps (see :class:`ChurnTrace`).
 * ``shared``: 128 requests on one 2048-token prefix (see :func:`shared_prefix_batch`).
+* ``tree``: a prefix tree of several sharing levels (see :func:`prefix_tree_batch`).
 """
 from __future__ import annotations
 
@@ -244,6 +245,81 @@ def shared_prefix_batch(device="cpu", seed=5, batch=128, prefix_len=2048, shared
         cow_pairs=np.concatenate(cows).astype(np.int64) if cows else np.zeros((0, 2), np.int64),
         child_offsets=offs, child_k=child_k, child_v=child_v,
         child_slots=np.concatenate(child_slots) if child_slots else np.zeros(0, np.int64), q=q)
+
+
+# --------------------------------------------------------------- prefix tree
+@dataclass
+class PrefixTreeBatch:
+    """A tree snapshot in a paged pool: ``chunks`` rows are (first id, rows,
+    seq begin, seq end) in tree order (parents first); chunk c's rows live in
+    blocks block_ids[first id ...] handed out by the host pool, one chunk per
+    pool sequence (a ragged chunk leaves the rest of its last block unused).
+    Chunk rows are drawn in chunk order into k_rows / v_rows; ``slots`` is
+    their host-pool slot, for the device path only."""
+    dtype: str
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    scale: float
+    chunks: np.ndarray             # int32 [n, 4]
+    block_ids: np.ndarray          # int32 [sum of blocks]
+    row_offsets: np.ndarray        # int64 [n + 1] into k_rows / v_rows
+    k_rows: torch.Tensor           # [sum of rows, Hkv, D]
+    v_rows: torch.Tensor
+    slots: np.ndarray              # int64 [sum of rows]
+    q: torch.Tensor                # [B, Hq, D]
+
+    @property
+    def num_seqs(self) -> int:
+        return self.q.shape[0]
+
+
+def multi_level_tree(batch, root_len, groups, group_len, leaf_lo, leaf_hi, seed):
+    """(rows, begin, end) of a three-level tree: one root chunk over every
+    sequence, ``groups`` equal groups of consecutive sequences each with its
+    own chunk, and one private leaf per sequence of U{leaf_lo..leaf_hi}
+    rows.  Group chunk lengths are drawn in [group_len / 2, group_len]."""
+    rng = np.random.default_rng(seed)
+    tree = [(root_len, 0, batch)]
+    per = batch // groups
+    for g in range(groups):
+        lo, hi = g * per, batch if g == groups - 1 else (g + 1) * per
+        tree.append((int(rng.integers(group_len // 2, group_len, endpoint=True)), lo, hi))
+    leaves = rng.integers(leaf_lo, leaf_hi, size=batch, endpoint=True)
+    tree.extend((int(n), r, r + 1) for r, n in enumerate(leaves))
+    return tree
+
+
+def prefix_tree_batch(tree, device="cpu", seed=7, hq=32, hkv=8, d=128, p=16, dtype="bf16",
+                      batch=None) -> PrefixTreeBatch:
+    """Place the chunks of ``tree`` ((rows, begin, end) in tree order) in a
+    shuffled pool of 1.25 x the blocks they need and draw N(0, 1) rows."""
+    nblk = [(n + p - 1) // p for n, _, _ in tree]
+    nb = max(1, int(math.ceil(1.25 * sum(nblk))))
+    pool = BlockPool(nb, p, seed=seed, shuffle=True)
+    chunks, ids, slots, offs = [], [], [], [0]
+    for (n, b, e) in tree:
+        s = pool.new_seq()
+        sl, cow = s.append(n)
+        assert len(cow) == 0
+        chunks.append((len(ids), n, b, e))
+        ids.extend(int(x) for x in s.blocks())
+        slots.append(sl)
+        offs.append(offs[-1] + n)
+    B = batch if batch is not None else max(e for _, _, e in tree)
+    g = make_generator(seed, device)
+    total = offs[-1]
+    k_rows = randn((total, hkv, d), dtype, g, device)
+    v_rows = randn((total, hkv, d), dtype, g, device)
+    q = randn((B, hq, d), dtype, g, device)
+    return PrefixTreeBatch(
+        dtype=dtype, num_q_heads=hq, num_kv_heads=hkv, head_dim=d, block_size=p, num_blocks=nb,
+        scale=1.0 / math.sqrt(d), chunks=np.array(chunks, np.int32).reshape(-1, 4),
+        block_ids=np.array(ids, np.int32), row_offsets=np.array(offs, np.int64), k_rows=k_rows,
+        v_rows=v_rows, slots=np.concatenate(slots).astype(np.int64) if slots else
+        np.zeros(0, np.int64), q=q)
 
 
 # --------------------------------------------------------------- churn trace

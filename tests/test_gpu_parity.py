@@ -82,6 +82,17 @@ def test_gqa8_tensor_core_decode(p, partition_size):
     _run_batch(b, partition_size=ps)
 
 
+@pytest.mark.parametrize("rep", range(3))
+def test_gqa8_tensor_core_decode_one_stage_segments(rep):
+    # every (sequence, kv head) segment fits one 128-row stage, so every stage
+    # starts a new piece with its own Q: a CTA's first stages load three
+    # pieces' Q back to back, before any of their MMAs need have run
+    lens = np.random.default_rng(70 + rep).integers(1, 128, size=400, endpoint=True)
+    b = wl.custom_batch(lens, dtype="bf16", hq=64, hkv=8, d=128, p=16, seed=70 + rep,
+                        device="cuda")
+    _run_batch(b, check_pool=False)
+
+
 def test_gqa8_tensor_core_decode_long_sampled():
     lens = np.array([40000, 3000, 65536, 1], np.int32)
     b = wl.custom_batch(lens, dtype="bf16", hq=32, hkv=4, d=128, p=16, seed=62, device="cuda")
