@@ -55,6 +55,8 @@ constexpr int kDecodeThreads = kConsumerWarps * 32;
 constexpr int kChunk = 16;             // token rows per softmax update
 constexpr float kRescaleLog2 = 8.0f;   // move the exponent base past 2^8 growth
 constexpr float kLn2 = 0.6931471805599453f;
+// Sources a merging warp loads at once (their latencies overlap).
+constexpr int kMergeBatch = 8;
 
 // Stage descriptor flags.
 constexpr int kPieceStart = 1;   // first stage of a piece: reset the state, load q
@@ -82,7 +84,10 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int head_dim, int elem_
   s.desc_off = (s.ok_off + (size_t)stages * 4 + 15) & ~(size_t)15;
   s.ring_off = s.desc_off + (size_t)stages * 16;
   s.scratch_off = s.ring_off + (size_t)2 * 64 * 16;  // two 64-entry stage descriptor rings
-  s.total = s.scratch_off + (size_t)kConsumerWarps * 2 * (2 * group * 16) * 4 + 128;  // +128: base alignment
+  // scratch: the half-warps' cross-lane sums [4][2][2G][16], then the merge's
+  // per-warp maxima and sums [2][4][G]
+  s.total = s.scratch_off + (size_t)kConsumerWarps * 2 * (2 * group * 16) * 4 +
+            (size_t)2 * kConsumerWarps * group * 4 + 128;  // +128: base alignment
   return s;
 }
 
@@ -267,6 +272,11 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
       const bool end = k == n - 1 || i == pnt - 1;
       const int flags = (k == 0 || i == 0 ? kPieceStart : 0) | (end ? kPieceEnd : 0) |
                         (end && i == pnt - 1 && dseg >= 0 ? kWhole : 0) | (dseg > 0 ? kSlot1 : 0);
+      if (flags & kPieceStart) {  // the piece's q rows, into L2 long before they are read
+        const int64_t qr = a.q_rows ? __ldg(a.q_rows + r) : r;
+        prefetch_l2_bulk(static_cast<const T*>(a.q) + (qr * a.num_q_heads + (int64_t)h * G) * D,
+                         (uint32_t)(G * D * sizeof(T)));
+      }
       dA[k & 63] = make_int4(id0, id1, row0 - b0 * P, nbox);
       dB[k & 63] = make_int4(r, h, nvalid, flags);
     }
@@ -323,6 +333,21 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
   const int hw = lane >> 4, l16 = lane & 15;
   float2 q2[G][EP2];
   float2 acc[G][EP2];
+  // q of a piece, scaled, into registers.  The CTA's first piece is known
+  // from the plan; every later one starts right after a piece end, whose
+  // merge the load overlaps.
+  auto load_q = [&](int r, int h) {
+    const int64_t qr = a.q_rows ? __ldg(a.q_rows + r) : r;
+    const T* qp = static_cast<const T*>(a.q) + (qr * a.num_q_heads + (int64_t)h * G) * D + l16 * EPL;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float f[EPL];
+      VecLoad<T, EPL>::run(qp + g * D, f);
+#pragma unroll
+      for (int j = 0; j < EP2; ++j) q2[g][j] = make_float2(f[2 * j] * a.qscale, f[2 * j + 1] * a.qscale);
+    }
+  };
+  load_q(d0.x, d0.y);
   // (m_used, l_run): softmax state of head (l16 / (8 / G)) % G of this lane.
   float m_used = -INFINITY, l_run = 0.f;
   float* red = scratch + (warp * 2 + hw) * (2 * G * 16);
@@ -347,20 +372,11 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
     const int nvalid = dsc.z, flags = dsc.w;
     const T* kt = tiles + (size_t)s * 2 * L.tile_elems;
     const T* vt = kt + L.tile_elems;
-    if (flags & kPieceStart) {
-      const int64_t qr = a.q_rows ? __ldg(a.q_rows + dsc.x) : dsc.x;
-      const T* qp = static_cast<const T*>(a.q) +
-                    (qr * a.num_q_heads + (int64_t)dsc.y * G) * D + l16 * EPL;
+    if (flags & kPieceStart) {  // q2 already holds this piece's q
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float f[EPL];
-        VecLoad<T, EPL>::run(qp + g * D, f);
+      for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int j = 0; j < EP2; ++j) {
-          q2[g][j] = make_float2(f[2 * j] * a.qscale, f[2 * j + 1] * a.qscale);
-          acc[g][j] = make_float2(0.f, 0.f);
-        }
-      }
+        for (int j = 0; j < EP2; ++j) acc[g][j] = make_float2(0.f, 0.f);
       m_used = -INFINITY;
       l_run = 0.f;
     }
@@ -377,10 +393,17 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
       }
     }
     if (flags & kPieceEnd) {
+      // The next stage starts the next piece: fetch its q now (this piece's
+      // is no longer needed).  Its descriptor was written before this
+      // stage's was published (the same batch, or an earlier one).
+      if (k + 1 < n) {
+        const int4 nd = dB[(k + 1) & 63];
+        load_q(nd.x, nd.y);
+      }
       // ---- merge the four warps through this stage's tile, then write
       if (!merge_sync()) break;  // every warp is done with the tile
       float* macc = reinterpret_cast<float*>(const_cast<T*>(kt));  // [4][G][D]
-      float* mm = scratch;                                          // [4][G]
+      float* mm = scratch + kConsumerWarps * 2 * (2 * G * 16);        // [4][G], after the sums
       float* ml = mm + kConsumerWarps * G;                          // [4][G]
 #pragma unroll
       for (int g = 0; g < G; ++g)
@@ -432,7 +455,9 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
           if (e == 0 && a.lse_out) a.lse_out[rh] = lse2 * kLn2;
         }
       }
-      if (!merge_sync()) break;  // merge reads done before the tile is refilled
+      // No barrier here: each warp releases the tile below once its own merge
+      // reads are done, and the producer refills it only after all four have;
+      // mm / ml are rewritten only after the next piece's first barrier.
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
@@ -503,9 +528,19 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) 
     const int64_t cc = c_first + i;
     return (2 * cc + (i == 0 && first_is_slot1 ? 1 : 0)) * G + g;
   };
-  float M = -INFINITY;
-  for (int i = lane; i < n_st + n_pc; i += 32)
-    M = fmaxf(M, i < n_st ? ext_lse[i] : a.rec_lse[piece_rec(i - n_st)]);
+  // Sources 0 .. n-1: lane i holds source i's LSE (sources past 32, rare,
+  // are read again in pass 2); pass 2 loads the outputs kMergeBatch at a
+  // time so their latencies overlap.
+  const int n = n_st + n_pc;
+  auto src_lse = [&](int i) -> float {
+    return i < n_st ? ext_lse[i] : a.rec_lse[piece_rec(i - n_st)];
+  };
+  auto src_o = [&](int i) -> const float* {
+    return i < n_st ? ext_o + (int64_t)i * D : a.rec_o + piece_rec(i - n_st) * D;
+  };
+  const float my0 = lane < n ? src_lse(lane) : -INFINITY;
+  float M = my0;
+  for (int i = lane + 32; i < n; i += 32) M = fmaxf(M, src_lse(i));
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float acc[EPL];
@@ -513,16 +548,28 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) 
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
   float Lsum = 0.f;
   if (M != -INFINITY) {
-    for (int i = 0; i < n_st + n_pc; ++i) {
-      const float l = i < n_st ? ext_lse[i] : a.rec_lse[piece_rec(i - n_st)];
-      if (l == -INFINITY) continue;  // empty state: the merge's identity
-      const float w = exp2f(l - M);
-      Lsum += w;
-      const float* po = i < n_st ? ext_o + (int64_t)i * D : a.rec_o + piece_rec(i - n_st) * D;
-      float x[EPL];
-      VecLoad<float, EPL>::run(po + lane * EPL, x);
+    for (int i0 = 0; i0 < n; i0 += 32) {
+      const int m = min(32, n - i0);
+      const float my = i0 == 0 ? my0 : (lane < m ? src_lse(i0 + lane) : -INFINITY);
+      for (int u0 = 0; u0 < m; u0 += kMergeBatch) {
+        float l[kMergeBatch], x[kMergeBatch][EPL];
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) acc[e] = fmaf(w, x[e], acc[e]);
+        for (int u = 0; u < kMergeBatch; ++u) {
+          l[u] = __shfl_sync(0xffffffffu, my, (u0 + u) & 31);
+          if (u0 + u >= m) l[u] = -INFINITY;  // an empty state: the merge's identity
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) x[u][e] = 0.f;
+          if (l[u] != -INFINITY) VecLoad<float, EPL>::run(src_o(i0 + u0 + u) + lane * EPL, x[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+          if (l[u] == -INFINITY) continue;
+          const float w = exp2f(l[u] - M);
+          Lsum += w;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) acc[e] = fmaf(w, x[u][e], acc[e]);
+        }
+      }
     }
   }
   const bool nonempty = Lsum > 0.f;

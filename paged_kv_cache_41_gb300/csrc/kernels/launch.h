@@ -168,23 +168,19 @@ struct PrefixArgs {
   float lse_scale;       // 1: LSE in base 2 (partial states); ln 2: natural log
 };
 
-// Arguments of the merge at the end of attention over a prefix tree.  The
-// states: chunk-first rows [0, cf_rows) at ((row * Hq + h) * s_max + split),
-// then one state per later row at (cf_rows * Hq * s_max + (row - cf_rows) *
-// Hq + h); O fp32 [.., D], LSE base 2.  Sequence r merges the states of
-// entries [seq_ptr[r], seq_ptr[r + 1]), entry (row, n) naming n slots of a
-// row.
+// Arguments of the merge at the end of attention over a prefix tree.
+// Sequence r merges states [seq_ptr[r], seq_ptr[r + 1]) of `states`; state
+// reference (base, head_stride) names, for query head h, the state at index
+// base + h * head_stride of st_o ([.., D] fp32) and st_lse (base 2).
 struct TreeMergeArgs {
   const float* st_o;
   const float* st_lse;
-  const int32_t* seq_ptr;  // [B + 1]
-  const int2* entries;     // [seq_ptr[B]]
-  void* out;               // [B, Hq, D]
-  float* lse_out;          // [B, Hq] natural log, or null
+  const int32_t* seq_ptr;     // [B + 1]
+  const int64_t* states;      // [seq_ptr[B]][2]: (base, head_stride)
+  void* out;                  // [B, Hq, D]
+  float* lse_out;             // [B, Hq] natural log, or null
   int32_t num_seqs;
   int32_t num_q_heads;
-  int32_t cf_rows;
-  int32_t s_max;
 };
 cudaError_t launch_tree_merge(int dtype, int head_dim, const TreeMergeArgs& args,
                               cudaStream_t stream);

@@ -22,7 +22,8 @@ __host__ __device__ __forceinline__ long long stages_per_cta(long long S, int C)
 // the reduction, and reports bad lengths (PKV_DEVERR_LENGTH).  The scan runs
 // in passes of kThreads * kPer sequences, kPer consecutive ones per thread.
 // `wsum` is shared scratch of at least kThreads / 32 + 2 long longs.  Returns
-// the number of stages of this CTA (<= 0: none; the caller leaves).
+// the number of stages of this CTA (<= 0: none; the caller leaves).  Up to
+// kThreads * kPer sequences the lengths are read once and kept in registers.
 template <int kThreads, int kRows, int kPer = 8>
 __device__ __forceinline__ int plan_cta_stages(const DecodeArgs& a, long long* wsum, int4* d0) {
   constexpr int kWarps = kThreads / 32;
@@ -59,6 +60,43 @@ __device__ __forceinline__ int plan_cta_stages(const DecodeArgs& a, long long* w
     excl = before + x - mine;
     __syncthreads();  // wsum is rewritten by the next pass
   };
+  int* start = reinterpret_cast<int*>(wsum + kWarps);
+  if (B <= kChunk) {
+    // one pass: the lengths stay in registers for the search
+    int nt[kPer];
+    long long excl, total;
+    scan_chunk(0, nt, excl, total, c == 0);
+    if (c == 0) {
+      long long p = excl;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int r = threadIdx.x * kPer + j;
+        if (r < B) a.plan_pre[r] = p;
+        p += nt[j];
+      }
+      if (threadIdx.x == 0) a.plan_pre[B] = total;
+    }
+    const long long S = total * Hkv;
+    const long long wct = stages_per_cta(S, C);
+    const long long p0 = min((long long)c * wct, S);
+    const int n = (int)(min(p0 + wct, S) - p0);
+    if (n <= 0) return n;  // uniform over the CTA
+    long long p = excl;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      if (nt[j] > 0 && p * Hkv <= p0 && p0 < (p + nt[j]) * Hkv) {
+        const long long off = p0 - p * Hkv;
+        start[0] = threadIdx.x * kPer + j;
+        start[1] = (int)(off / nt[j]);
+        start[2] = (int)(off % nt[j]);
+      }
+      p += nt[j];
+    }
+    __syncthreads();
+    *d0 = make_int4(start[0], start[1], start[2], 0);
+    __syncthreads();  // the scratch is the caller's from here on
+    return n;
+  }
   long long carry = 0;
   for (int base = 0; base < B; base += kChunk) {
     int nt[kPer];
@@ -82,7 +120,6 @@ __device__ __forceinline__ int plan_cta_stages(const DecodeArgs& a, long long* w
   const int n = (int)(min(p0 + wct, S) - p0);
   if (n <= 0) return n;  // uniform over the CTA
   // the sequence holding stage p0, found in a second pass
-  int* start = reinterpret_cast<int*>(wsum + kWarps);
   carry = 0;
   for (int base = 0; base < B; base += kChunk) {
     int nt[kPer];

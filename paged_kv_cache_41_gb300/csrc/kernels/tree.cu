@@ -12,9 +12,10 @@
 // with an empty state (LSE = -inf) the merge's identity.
 //
 // Design: one warp per (sequence, query head), D / 32 columns per lane.  The
-// states a sequence merges are listed on the host (a CSR of (row, count)
-// entries), so the kernel walks no tree: pass 1 takes the max LSE, pass 2
-// accumulates.  The states are a few per sequence and are read once.
+// states a sequence merges are listed on the host (a CSR of (base, head
+// stride) references), so the kernel walks no tree: pass 1 takes the max LSE
+// with one state per lane, pass 2 accumulates, loading several states'
+// outputs at once so their latencies overlap.
 #include <math.h>
 
 #include "common.cuh"
@@ -24,6 +25,9 @@ namespace pkv {
 
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Sources a warp loads at once (their latencies overlap).
+constexpr int kBatch = 8;
+
 template <typename T, int D>
 __global__ void __launch_bounds__(128) tree_merge_kernel(const TreeMergeArgs a) {
   constexpr int EPL = D / 32;
@@ -32,19 +36,22 @@ __global__ void __launch_bounds__(128) tree_merge_kernel(const TreeMergeArgs a) 
   const int64_t rh = (int64_t)blockIdx.x * 4 + warp;
   if (rh >= (int64_t)a.num_seqs * a.num_q_heads) return;
   const int r = (int)(rh / a.num_q_heads), qh = (int)(rh % a.num_q_heads);
-  const int e0 = __ldg(a.seq_ptr + r), e1 = __ldg(a.seq_ptr + r + 1);
-  const int Hq = a.num_q_heads, S = a.s_max;
-  // state i of entry (row, n): chunk-first rows [0, cf_rows) keep n split
-  // slots each; later rows are the paged decode's, one state each
-  auto state_index = [&](int row, int s) -> int64_t {
-    return row < a.cf_rows ? ((int64_t)row * Hq + qh) * S + s
-                           : (int64_t)a.cf_rows * Hq * S + (int64_t)(row - a.cf_rows) * Hq + qh;
+  const int s0 = __ldg(a.seq_ptr + r), n = __ldg(a.seq_ptr + r + 1) - s0;
+  // state i of this sequence: base + qh * head_stride
+  auto state = [&](int i) -> int64_t {
+    const longlong2 ref = __ldg(reinterpret_cast<const longlong2*>(a.states) + s0 + i);
+    return ref.x + (int64_t)qh * ref.y;
   };
-  float M = -INFINITY;
-  for (int e = e0; e < e1; ++e) {
-    const int2 en = __ldg(a.entries + e);
-    for (int s = lane; s < en.y; s += 32) M = fmaxf(M, a.st_lse[state_index(en.x, s)]);
+  // lane i holds state i's index and LSE (states past 32, rare, are read
+  // again in pass 2)
+  int64_t my_si0 = 0;
+  float my0 = -INFINITY;
+  if (lane < n) {
+    my_si0 = state(lane);
+    my0 = a.st_lse[my_si0];
   }
+  float M = my0;
+  for (int i = lane + 32; i < n; i += 32) M = fmaxf(M, a.st_lse[state(i)]);
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float acc[EPL];
@@ -52,18 +59,36 @@ __global__ void __launch_bounds__(128) tree_merge_kernel(const TreeMergeArgs a) 
   for (int i = 0; i < EPL; ++i) acc[i] = 0.f;
   float L = 0.f;
   if (M != -INFINITY) {
-    for (int e = e0; e < e1; ++e) {
-      const int2 en = __ldg(a.entries + e);
-      for (int s = 0; s < en.y; ++s) {
-        const int64_t si = state_index(en.x, s);
-        const float l = a.st_lse[si];
-        if (l == -INFINITY) continue;  // an empty part: the identity
-        const float w = exp2f(l - M);
-        L += w;
-        float x[EPL];
-        VecLoad<float, EPL>::run(a.st_o + si * D + lane * EPL, x);
+    for (int i0 = 0; i0 < n; i0 += 32) {
+      const int m = min(32, n - i0);
+      int64_t my_si = my_si0;
+      float my = my0;
+      if (i0 > 0) {
+        my = -INFINITY;
+        if (lane < m) {
+          my_si = state(i0 + lane);
+          my = a.st_lse[my_si];
+        }
+      }
+      for (int u0 = 0; u0 < m; u0 += kBatch) {
+        float l[kBatch], x[kBatch][EPL];
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) acc[i] = fmaf(w, x[i], acc[i]);
+        for (int u = 0; u < kBatch; ++u) {
+          l[u] = __shfl_sync(0xffffffffu, my, (u0 + u) & 31);
+          const int64_t si = __shfl_sync(0xffffffffu, my_si, (u0 + u) & 31);
+          if (u0 + u >= m) l[u] = -INFINITY;  // an empty part: the identity
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) x[u][e] = 0.f;
+          if (l[u] != -INFINITY) VecLoad<float, EPL>::run(a.st_o + si * D + lane * EPL, x[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          if (l[u] == -INFINITY) continue;
+          const float w = exp2f(l[u] - M);
+          L += w;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) acc[e] = fmaf(w, x[u][e], acc[e]);
+        }
       }
     }
   }

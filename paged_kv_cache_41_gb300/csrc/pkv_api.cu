@@ -761,9 +761,9 @@ pkv_status pkv_paged_attention_decode_static(
 //                                       (sequence, chunk) segment, -1 padded
 //   plen     int32 [n_pseudo]           its rows
 //   pq       int32 [n_pseudo]           its sequence (q row)
-//   seq_ptr  int32 [B + 1]              CSR over entries, per sequence
-//   entries  int2 [n_entries]           (state row, slots): chunk-first rows
-//                                       first, then one row per segment
+//   seq_ptr  int32 [B + 1]              CSR over states, per sequence
+//   states   int64 [n_states][2]        (base, head stride): the state of
+//                                       query head h is base + h * stride
 // and sizes the device workspace: chunk-first states [cf_rows, Hq, s_max]
 // followed by segment states [n_pseudo, Hq] (O fp32 [.., D] in one array,
 // LSE base 2 in another), then the paged decode's plan and piece records.
@@ -779,9 +779,9 @@ struct TreePlanHeader {
   int64_t num_blocks;
   int32_t block_size, num_kv_heads, head_dim, dtype;
   int32_t num_seqs, num_q_heads;
-  int32_t n_items, s_max, cf_rows, n_pseudo, pseudo_max_blocks, n_entries;
+  int32_t n_items, s_max, cf_rows, n_pseudo, pseudo_max_blocks, n_states;
   int64_t decode_ctas;
-  uint64_t items_off, cf_ids_off, ptab_off, plen_off, pq_off, seqptr_off, entries_off, plan_bytes;
+  uint64_t items_off, cf_ids_off, ptab_off, plen_off, pq_off, seqptr_off, states_off, plan_bytes;
   uint64_t ws_lse_off, ws_dec_off, ws_bytes;
   uint64_t dec_pre_off, dec_lse_off, dec_o_off, dec_total;
 };
@@ -823,14 +823,13 @@ pkv_status pkv_chunk_tree_plan(const pkv_cache_desc* cache, const pkv_chunk* chu
   // ---- classify the chunks; lay out partial rows, ids and segments
   std::vector<int64_t> where((size_t)num_chunks), ids_at((size_t)num_chunks);
   std::vector<char> first((size_t)num_chunks);
-  int64_t cf_rows = 0, cf_ids = 0, n_pseudo = 0, pmax = 0, n_entries = 0, max_tiles = 0;
+  int64_t cf_rows = 0, cf_ids = 0, n_pseudo = 0, pmax = 0, max_tiles = 0;
   for (int32_t c = 0; c < num_chunks; ++c) {
     const pkv_chunk& k = chunks[c];
     if (k.len < 1 || k.seq_begin < 0 || k.seq_begin >= k.seq_end || k.seq_end > num_seqs ||
         k.first_id < 0 || k.first_id + ceil_div(k.len, P) > num_block_ids)
       return PKV_ERR_INVALID_ARG;
     const int64_t cov = k.seq_end - k.seq_begin, nb = ceil_div(k.len, P);
-    n_entries += cov;
     first[c] = tc && cov > thr;
     if (first[c]) {
       where[c] = cf_rows;  // a chunk's rows start a query tile: its stores stay inside
@@ -844,7 +843,7 @@ pkv_status pkv_chunk_tree_plan(const pkv_cache_desc* cache, const pkv_chunk* chu
       pmax = std::max(pmax, nb);
     }
   }
-  if (cf_rows > INT32_MAX || n_entries > INT32_MAX || cf_ids > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  if (cf_rows > INT32_MAX || cf_ids > INT32_MAX) return PKV_ERR_UNSUPPORTED;
   if (n_pseudo > 65535) return PKV_ERR_UNSUPPORTED;
 
   // ---- key split of the chunk-first phase: the fewest 128-key tiles per
@@ -872,6 +871,13 @@ pkv_status pkv_chunk_tree_plan(const pkv_cache_desc* cache, const pkv_chunk* chu
   }
   if (n_items > INT32_MAX) return PKV_ERR_UNSUPPORTED;
   const int64_t split_len = per * pkv::kPrefixKeys;
+  // states each sequence merges: every key split of a chunk-first chunk on
+  // its path, one per other chunk
+  int64_t n_states = 0;
+  for (int32_t c = 0; c < num_chunks; ++c)
+    n_states += (int64_t)(chunks[c].seq_end - chunks[c].seq_begin) *
+                (first[c] ? ceil_div(chunks[c].len, split_len) : 1);
+  if (n_states > INT32_MAX) return PKV_ERR_UNSUPPORTED;
 
   // ---- sizes
   TreePlanHeader h{};
@@ -889,7 +895,7 @@ pkv_status pkv_chunk_tree_plan(const pkv_cache_desc* cache, const pkv_chunk* chu
   h.cf_rows = (int32_t)cf_rows;
   h.n_pseudo = (int32_t)n_pseudo;
   h.pseudo_max_blocks = (int32_t)pmax;
-  h.n_entries = (int32_t)n_entries;
+  h.n_states = (int32_t)n_states;
   h.decode_ctas = n_pseudo > 0 ? decode_ctas(cache, (int32_t)n_pseudo, num_q_heads, (int32_t)pmax, 0)
                                : 0;
   if (h.decode_ctas > INT32_MAX) return PKV_ERR_UNSUPPORTED;
@@ -904,11 +910,11 @@ pkv_status pkv_chunk_tree_plan(const pkv_cache_desc* cache, const pkv_chunk* chu
   section(&h.plen_off, (size_t)n_pseudo * 4);
   section(&h.pq_off, (size_t)n_pseudo * 4);
   section(&h.seqptr_off, (size_t)(num_seqs + 1) * 4);
-  section(&h.entries_off, (size_t)n_entries * 8);
+  section(&h.states_off, (size_t)n_states * 16);
   h.plan_bytes = off;
-  const int64_t n_states = cf_rows * Hq * s_max + n_pseudo * Hq;
-  h.ws_lse_off = align256((size_t)n_states * cache->head_dim * 4);
-  h.ws_dec_off = h.ws_lse_off + align256((size_t)n_states * 4);
+  const int64_t n_ws_states = cf_rows * Hq * s_max + n_pseudo * Hq;  // in the workspace
+  h.ws_lse_off = align256((size_t)n_ws_states * cache->head_dim * 4);
+  h.ws_dec_off = h.ws_lse_off + align256((size_t)n_ws_states * 4);
   DecodeWorkspace dw{};
   if (n_pseudo > 0) dw = decode_workspace(n_pseudo, h.decode_ctas, G, cache->head_dim);
   h.dec_pre_off = dw.pre_off;
@@ -931,7 +937,7 @@ pkv_status pkv_chunk_tree_plan(const pkv_cache_desc* cache, const pkv_chunk* chu
   auto* plen = reinterpret_cast<int32_t*>(base + h.plen_off);
   auto* pq = reinterpret_cast<int32_t*>(base + h.pq_off);
   auto* sptr = reinterpret_cast<int32_t*>(base + h.seqptr_off);
-  auto* ent = reinterpret_cast<int32_t*>(base + h.entries_off);
+  auto* sref = reinterpret_cast<int64_t*>(base + h.states_off);
   int64_t it = 0;
   for (int32_t c = 0; c < num_chunks; ++c) {
     const pkv_chunk& k = chunks[c];
@@ -966,19 +972,25 @@ pkv_status pkv_chunk_tree_plan(const pkv_cache_desc* cache, const pkv_chunk* chu
   });
   // each sequence's states, in tree order: count, then place
   std::vector<int32_t> fill((size_t)num_seqs + 1, 0);
-  for (int32_t c = 0; c < num_chunks; ++c)
-    for (int32_t r = chunks[c].seq_begin; r < chunks[c].seq_end; ++r) ++fill[(size_t)r + 1];
+  for (int32_t c = 0; c < num_chunks; ++c) {
+    const int32_t k = first[c] ? (int32_t)ceil_div(chunks[c].len, split_len) : 1;
+    for (int32_t r = chunks[c].seq_begin; r < chunks[c].seq_end; ++r) fill[(size_t)r + 1] += k;
+  }
   for (int32_t r = 0; r < num_seqs; ++r) fill[(size_t)r + 1] += fill[(size_t)r];
   memcpy(sptr, fill.data(), (size_t)(num_seqs + 1) * 4);
   for (int32_t c = 0; c < num_chunks; ++c) {
     const pkv_chunk& k = chunks[c];
     for (int32_t r = k.seq_begin; r < k.seq_end; ++r) {
-      int32_t* e = ent + 2 * (int64_t)fill[(size_t)r]++;
-      if (first[c]) {
-        e[0] = (int32_t)(where[c] + (r - k.seq_begin));
-        e[1] = (int32_t)ceil_div(k.len, split_len);
-      } else {
-        e[0] = (int32_t)(cf_rows + where[c] + (r - k.seq_begin));
+      if (first[c]) {  // ((row * Hq + h) * s_max + split)
+        const int64_t row = where[c] + (r - k.seq_begin);
+        for (int64_t s = 0; s < ceil_div(k.len, split_len); ++s) {
+          int64_t* e = sref + 2 * (int64_t)fill[(size_t)r]++;
+          e[0] = row * Hq * s_max + s;
+          e[1] = s_max;
+        }
+      } else {  // after every chunk-first state: (segment * Hq + h)
+        int64_t* e = sref + 2 * (int64_t)fill[(size_t)r]++;
+        e[0] = cf_rows * Hq * s_max + (where[c] + (r - k.seq_begin)) * Hq;
         e[1] = 1;
       }
     }
@@ -1077,13 +1089,11 @@ pkv_status pkv_chunk_tree_attention(const pkv_cache_desc* cache, void* out, floa
   m.st_o = st_o;
   m.st_lse = st_lse;
   m.seq_ptr = reinterpret_cast<const int32_t*>(dplan + h.seqptr_off);
-  m.entries = reinterpret_cast<const int2*>(dplan + h.entries_off);
+  m.states = reinterpret_cast<const int64_t*>(dplan + h.states_off);
   m.out = out;
   m.lse_out = lse;
   m.num_seqs = num_seqs;
   m.num_q_heads = num_q_heads;
-  m.cf_rows = h.cf_rows;
-  m.s_max = h.s_max;
   return pkv::launch_tree_merge(cache->dtype, cache->head_dim, m, s) == cudaSuccess ? PKV_OK
                                                                                    : PKV_ERR_CUDA;
 }

@@ -93,6 +93,16 @@ def test_gqa8_tensor_core_decode_one_stage_segments(rep):
     _run_batch(b, check_pool=False)
 
 
+@pytest.mark.parametrize("hq,hkv,batch", [(32, 8, 2500), (64, 8, 1700)])
+def test_batch_past_one_scan_pass(hq, hkv, batch):
+    # more sequences than one pass of the CTAs' length scan covers (1024 for
+    # the CUDA-core decode, 1536 for the tensor-core one): the multi-pass
+    # search for each CTA's first stage
+    lens = np.random.default_rng(batch).integers(0, 48, size=batch, endpoint=True)
+    b = wl.custom_batch(lens, dtype="bf16", hq=hq, hkv=hkv, d=128, p=16, seed=batch, device="cuda")
+    _run_batch(b, check_pool=False)
+
+
 def test_gqa8_tensor_core_decode_long_sampled():
     lens = np.array([40000, 3000, 65536, 1], np.int32)
     b = wl.custom_batch(lens, dtype="bf16", hq=32, hkv=4, d=128, p=16, seed=62, device="cuda")

@@ -18,8 +18,8 @@ from paged_kv_cache_41_gb300 import build, pkv
 
 HDR = struct.Struct("<IIq4i2i6iq8Q3Q4Q")
 FIELDS = ("magic version num_blocks block_size num_kv_heads head_dim dtype num_seqs num_q_heads "
-          "n_items s_max cf_rows n_pseudo pseudo_max_blocks n_entries decode_ctas items_off "
-          "cf_ids_off ptab_off plen_off pq_off seqptr_off entries_off plan_bytes ws_lse_off "
+          "n_items s_max cf_rows n_pseudo pseudo_max_blocks n_states decode_ctas items_off "
+          "cf_ids_off ptab_off plen_off pq_off seqptr_off states_off plan_bytes ws_lse_off "
           "ws_dec_off ws_bytes dec_pre_off dec_lse_off dec_o_off dec_total").split()
 
 
@@ -43,7 +43,7 @@ def _plan(k, chunks, ids, b, hq, threshold=-1):
 
     h["items"] = arr(h["items_off"], 8 * h["n_items"]).reshape(-1, 8)
     h["seq_ptr"] = arr(h["seqptr_off"], b + 1)
-    h["entries"] = arr(h["entries_off"], 2 * h["n_entries"]).reshape(-1, 2)
+    h["states"] = arr(h["states_off"], 2 * h["n_states"], np.int64).reshape(-1, 2)
     h["plen"] = arr(h["plen_off"], h["n_pseudo"])
     h["pq"] = arr(h["pq_off"], h["n_pseudo"])
     h["ptab"] = arr(h["ptab_off"], h["n_pseudo"] * h["pseudo_max_blocks"]).reshape(
@@ -52,6 +52,15 @@ def _plan(k, chunks, ids, b, hq, threshold=-1):
 
 
 LOOP9 = [(2, 0, 4), (1, 0, 2), (2, 2, 4), (2, 0, 1), (1, 1, 2), (1, 2, 3), (1, 3, 4)]
+
+
+def _cf_at(tree, cf, p=16):
+    """(offset among the chunk-first chunks' ids, chunk) for each chunk-first chunk."""
+    out, nxt = [], 0
+    for c in cf:
+        out.append((nxt, c))
+        nxt += -(-tree[c][0] // p)
+    return out
 
 
 def _chunks(tree, p):
@@ -72,15 +81,17 @@ def test_loop9_phases_follow_the_threshold(threshold, cf):
     cov = [e - b for _, b, e in tree]
     assert h["cf_rows"] == 32 * len(cf)  # each chunk-first chunk pads to one query tile
     assert h["n_pseudo"] == sum(c for i, c in enumerate(cov) if i not in cf)
-    # one state list entry per (sequence, chunk on its path): 4 paths of 3
-    assert h["n_entries"] == 12 and h["seq_ptr"].tolist() == [0, 3, 6, 9, 12]
+    # one state per (sequence, chunk on its path), times the chunk-first
+    # chunks' key splits
+    splits = {c: len({it[6] for it in h["items"] if it[0] == off}) for off, c in _cf_at(tree, cf)}
+    per_seq = [sum(splits.get(i, 1) for i, (_, b, e) in enumerate(tree) if b <= r < e)
+               for r in range(4)]
+    assert h["seq_ptr"].tolist() == np.concatenate([[0], np.cumsum(per_seq)]).tolist()
+    assert h["n_states"] == sum(per_seq)
     # every (chunk-first chunk, key) is covered by exactly one item (one pair
     # here); items name a chunk by where its ids start among the chunk-first
     # chunks' ids
-    at, nxt = {}, 0
-    for c in cf:
-        at[nxt] = c
-        nxt += -(-tree[c][0] // 16)
+    at = dict(_cf_at(tree, cf))
     keys = {}
     for it in h["items"]:
         ids_off, key0, nkeys, req0, nreq, st_req0, split = it[:7]
@@ -98,14 +109,17 @@ def test_entries_list_each_path_in_tree_order():
     _, h = _plan(_cache(), ch, ids, 6, 8, 1)
     cf_rows = h["cf_rows"]
     assert cf_rows == 3 * 32 and h["n_pseudo"] == 6
+    S, Hq = h["s_max"], 8
     for r in range(6):
-        ent = h["entries"][h["seq_ptr"][r]:h["seq_ptr"][r + 1]]
-        path = [i for i, (_, b, e) in enumerate(tree) if b <= r < e]
-        assert len(ent) == len(path) == 3
-        # root, group, then the private leaf as one decode segment
-        assert ent[0][0] == r and ent[1][0] == 32 + (r if r < 3 else 32 + r - 3)
-        assert ent[2].tolist() == [cf_rows + r, 1]
-        assert 1 <= ent[1][1] <= ent[0][1] == h["s_max"]
+        refs = h["states"][h["seq_ptr"][r]:h["seq_ptr"][r + 1]].tolist()
+        # root's key splits (row r), the group's (rows 32.. or 64..), then the
+        # private leaf as one decode segment after every chunk-first state
+        grp_row = 32 + r if r < 3 else 64 + r - 3
+        root = [[r * Hq * S + s, S] for s in range(S)]
+        assert refs[:S] == root
+        grp = refs[S:-1]
+        assert 1 <= len(grp) <= S and grp == [[grp_row * Hq * S + s, S] for s in range(len(grp))]
+        assert refs[-1] == [cf_rows * Hq * S + r * Hq, 1]
     # the segments carry their sequence, rows and the chunk's blocks
     assert h["pq"].tolist() == list(range(6)) and h["plen"].tolist() == [5, 6, 7, 8, 9, 10]
     for j in range(6):
