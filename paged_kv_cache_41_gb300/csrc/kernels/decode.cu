@@ -227,6 +227,27 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
   const int n = plan_cta_stages<kDecodeThreads, kStageRows>(
       a, reinterpret_cast<long long*>(scratch), &d0);
   if (n <= 0) return;  // no stages: the whole CTA leaves before any barrier
+  const int hw = lane >> 4, l16 = lane & 15;
+  float2 q2[G][EP2];
+  float2 acc[G][EP2];
+  // q of a piece, scaled, into registers.  Every piece after the CTA's
+  // first starts right after a piece end, whose merge the load overlaps.
+  // The first: where units are stages the plan names its stage, so its q
+  // loads now, under the set-up; otherwise it is the first batch's first
+  // descriptor.
+  auto load_q = [&](int r, int h) {
+    const int64_t qr = a.q_rows ? __ldg(a.q_rows + r) : r;
+    const T* qp = static_cast<const T*>(a.q) + (qr * a.num_q_heads + (int64_t)h * G) * D + l16 * EPL;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float f[EPL];
+      VecLoad<T, EPL>::run(qp + g * D, f);
+#pragma unroll
+      for (int j = 0; j < EP2; ++j) q2[g][j] = make_float2(f[2 * j] * a.qscale, f[2 * j + 1] * a.qscale);
+    }
+  };
+  const bool d0_exact = a.stage_units == 1 && a.piece_units == 0;
+  if (d0_exact) load_q(d0.x, d0.y);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -326,28 +347,17 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
     cT = effective_len(__ldg(a.seq_lens + cr), a.max_blocks, P, a.err, false);
     cpnt = (cT + kStageRows - 1) / kStageRows;
     compute_batch(0);
-    for (int st = 0; st < NS && st < n; ++st) issue_stage(st, st);
+    if (d0_exact)
+      for (int st = 0; st < NS && st < n; ++st) issue_stage(st, st);
+  }
+  if (!d0_exact) {
+    __syncthreads();  // the first batch's descriptors: every warp reads its first piece there
+    if (warp == 0)
+      for (int st = 0; st < NS && st < n; ++st) issue_stage(st, st);
   }
 
   // ------------------------------------------------------------------ consumers
-  const int hw = lane >> 4, l16 = lane & 15;
-  float2 q2[G][EP2];
-  float2 acc[G][EP2];
-  // q of a piece, scaled, into registers.  The CTA's first piece is known
-  // from the plan; every later one starts right after a piece end, whose
-  // merge the load overlaps.
-  auto load_q = [&](int r, int h) {
-    const int64_t qr = a.q_rows ? __ldg(a.q_rows + r) : r;
-    const T* qp = static_cast<const T*>(a.q) + (qr * a.num_q_heads + (int64_t)h * G) * D + l16 * EPL;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float f[EPL];
-      VecLoad<T, EPL>::run(qp + g * D, f);
-#pragma unroll
-      for (int j = 0; j < EP2; ++j) q2[g][j] = make_float2(f[2 * j] * a.qscale, f[2 * j + 1] * a.qscale);
-    }
-  };
-  load_q(d0.x, d0.y);
+  if (!d0_exact) load_q(dB[0].x, dB[0].y);
   // (m_used, l_run): softmax state of head (l16 / (8 / G)) % G of this lane.
   float m_used = -INFINITY, l_run = 0.f;
   float* red = scratch + (warp * 2 + hw) * (2 * G * 16);
@@ -496,19 +506,23 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) 
   const int r = (int)(rh / a.num_q_heads), qh = (int)(rh % a.num_q_heads);
   const int G = a.num_q_heads / a.num_kv_heads, h = qh / G, g = qh % G;
   const int Hkv = a.num_kv_heads, C = a.num_ctas;
+  // the work split of plan.cuh, in units: segment (r, h) starts at unit
+  // seg0, its stage i at seg0 + pu + su i, owned by CTA (start) / w
+  const long long su = a.stage_units, pu = a.piece_units;
   const long long S = a.plan_pre[a.num_seqs] * Hkv;
-  const long long s0 = a.plan_pre[r], nt = a.plan_pre[r + 1] - s0;
+  const long long pre = a.plan_pre[r], u = a.plan_pre[r + 1] - pre;
+  const long long nt = u > 0 ? (u - pu) / su : 0;
   const int n_ext = a.st_o ? a.st_slot : 0;
   // Sources: extra states [0, n_ext), then either the whole-segment state
   // (states mode) or pieces c_first..c_last.
-  const long long wct = stages_per_cta(S, C);
+  const long long w = units_per_cta(S, C, su);
   int c_first = 0, n_pc = 0;  // pieces: CTAs c_first .. c_first + n_pc - 1
   bool whole_state = false;
-  long long seg0 = 0;
+  bool first_is_slot1 = false;
   if (nt > 0) {
-    seg0 = s0 * Hkv + (long long)h * nt;
-    c_first = (int)(seg0 / wct);
-    const int c_last = (int)((seg0 + nt - 1) / wct);
+    const long long seg0 = pre * Hkv + (long long)h * u;
+    c_first = (int)((seg0 + pu) / w);
+    const int c_last = (int)((seg0 + pu + su * (nt - 1)) / w);
     if (c_first == c_last) {
       // written whole by its CTA: to out, or to its state slot, which is
       // already the result when only states are wanted and none merge in
@@ -516,14 +530,15 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) 
       whole_state = true;
     } else {
       n_pc = c_last - c_first + 1;
+      // a cut segment's first piece is in slot 1 of its CTA when that CTA
+      // owns an earlier stage: the stage just before, which starts at
+      // seg0 - su, the last of the previous non-empty segment
+      first_is_slot1 = seg0 > 0 && seg0 - su >= (long long)c_first * w;
     }
   }
   const float* ext_lse = a.st_o ? a.st_lse + rh * a.st_stride : nullptr;
   const float* ext_o = a.st_o ? a.st_o + rh * a.st_stride * D : nullptr;
   const int n_st = n_ext + (whole_state ? 1 : 0);
-  // a cut segment's first piece is in slot 1 of its CTA unless the segment
-  // starts that CTA's range
-  const bool first_is_slot1 = n_pc > 0 && seg0 != (long long)c_first * wct;
   auto piece_rec = [&](int i) -> int64_t {  // record of piece i (CTA c_first + i)
     const int64_t cc = c_first + i;
     return (2 * cc + (i == 0 && first_is_slot1 ? 1 : 0)) * G + g;

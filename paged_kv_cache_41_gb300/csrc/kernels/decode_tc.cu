@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       rsync;
   __shared__ int4 sdesc[kTcStages];
   __shared__ float redm[2][4][kTcN], redl[4][kTcN];
-  __shared__ long long wsum[kTcThreads / 32 + 2];
+  __shared__ long long wsum[2 * (kTcThreads / 32) + 4];
   __shared__ uint32_t tmem_base;
 
   const int c = blockIdx.x;
@@ -146,6 +146,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int r = d0.x, h = d0.y, i = d0.z;
     int len = effective_len(__ldg(a.seq_lens + r), a.max_blocks, P, a.err, false);
     int nt = (len + kTcRows - 1) / kTcRows;
+    while (i >= nt) {  // the plan may name a segment's end: its next non-empty one
+      i -= nt;
+      if (++h == Hkv) {
+        h = 0;
+        do {
+          ++r;
+          len = effective_len(__ldg(a.seq_lens + r), a.max_blocks, P, a.err, false);
+          nt = (len + kTcRows - 1) / kTcRows;
+        } while (nt == 0);
+      }
+    }
     int pieces = 0;
     for (int k = 0; k < n; ++k) {
       const int s = k % kTcStages;

@@ -83,7 +83,7 @@ struct DecodeArgs {
   void* out;                    // [B, Hq, D]
   float* lse_out;               // [B, Hq] natural log, or null
   unsigned int* err;
-  int64_t* plan_pre;            // [B + 1] exclusive prefix of stages per sequence (CTA 0 writes)
+  int64_t* plan_pre;            // [B + 1] exclusive prefix of work units per sequence (CTA 0 writes)
   float* rec_o;                 // [2C, G, D] normalised piece outputs
   float* rec_lse;               // [2C, G] piece LSEs, base 2
   // States mode (shared prefix): a whole segment writes (O, LSE base 2) to
@@ -103,6 +103,8 @@ struct DecodeArgs {
   int32_t block_size;
   int32_t num_ctas;      // C
   int32_t num_stages;    // shared-memory ring depth
+  int32_t stage_units;   // work units of one stage (>= 1) ...
+  int32_t piece_units;   // ... and of a piece's fixed cost (>= 0): the split of plan.cuh
   float qscale;          // softmax scale * log2(e)
 };
 

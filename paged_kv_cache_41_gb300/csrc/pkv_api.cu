@@ -197,7 +197,7 @@ int64_t decode_ctas(const pkv_cache_desc* c, int32_t num_seqs, int32_t num_q_hea
     const int64_t need = (smax + cap - 1) / cap;
     if (need > C) C = need;
   }
-  const int64_t fit = (smax + (1LL << 30) - 1) >> 30;  // stages per CTA fit an int
+  const int64_t fit = (3 * smax + (1LL << 30) - 1) >> 30;  // work units per CTA fit an int
   if (fit > C) C = fit;
   return C < 1 ? 1 : C;
 }
@@ -210,12 +210,24 @@ pkv_status encode_cache_map_sw128(CUtensorMap* map, const pkv_cache_desc* c, con
 // Encode the maps and launch the decode (partial kernel + reduction) on the
 // path use_tc_decode picks.
 pkv_status launch_decode(const pkv_cache_desc* cache, int G, const void* q, const void* k_cache,
-                         const void* v_cache, const pkv::DecodeArgs& a, cudaStream_t stream,
+                         const void* v_cache, const pkv::DecodeArgs& args, cudaStream_t stream,
                          int32_t q_seqs = 0) {
   pkv_status st;
   CUtensorMap tmk, tmv;
   cudaError_t e;
-  if (use_tc_decode(cache, G)) {
+  pkv::DecodeArgs a = args;
+  // Work units of the split (kernels/plan.cuh).  A piece's fixed cost (its
+  // q, merge and record) is about half a 32-row stage of the CUDA-core
+  // decode: where segments are short it decides the balance, so a piece
+  // weighs one unit and a stage two.  Where they may be long the equal
+  // stage split is as good, with a cheaper plan; the tensor-core decode's
+  // 128-row stages dwarf a piece.
+  const bool tc = use_tc_decode(cache, G);
+  const bool short_segments =
+      (int64_t)a.max_blocks * cache->block_size <= 32LL * pkv::kStageRows;
+  a.stage_units = !tc && short_segments ? 2 : 1;
+  a.piece_units = !tc && short_segments ? 1 : 0;
+  if (tc) {
     const int rows = cache->block_size < pkv::decode_tc_rows() ? cache->block_size
                                                                : pkv::decode_tc_rows();
     CUtensorMap tmq;
