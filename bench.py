@@ -32,8 +32,8 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOADS = ("llama", "long_bs16", "long_bs64", "long_bs64_k16", "shared", "churn", "gqa8",
-             "tree")
+WORKLOADS = ("llama", "llama_mxfp8", "long_bs16", "long_bs64", "long_bs64_k16", "shared", "churn",
+             "gqa8", "tree")
 
 
 def parse():
@@ -155,7 +155,7 @@ def barrier(world):
 
 def make_batch(name, device, seed_offset=0, batch=0):
     from paged_kv_cache_41_gb300 import workloads as wl
-    if name == "llama":
+    if name in ("llama", "llama_mxfp8"):
         return wl.llama_batch(device=device, seed=2 + seed_offset, batch=batch or 64)
     if name == "long_bs16":
         return wl.long_batch(device=device, block_size=16, seed=3 + seed_offset, batch=batch or 8)
@@ -241,8 +241,13 @@ def run_pkv(args, rank, world, local):
     B = b.num_seqs
     shape = (b.num_blocks, b.block_size, b.num_kv_heads, b.head_dim)
     dt = b.k_hist.dtype
-    kc = torch.zeros(shape, dtype=dt, device=dev)
-    vc = torch.zeros(shape, dtype=dt, device=dev)
+    mx = args.workload == "llama_mxfp8"  # the same layer over MXFP8 pools
+    if mx:
+        kc = pkv.MxPool(*shape, device=dev)
+        vc = pkv.MxPool(*shape, device=dev)
+    else:
+        kc = torch.zeros(shape, dtype=dt, device=dev)
+        vc = torch.zeros(shape, dtype=dt, device=dev)
     slots = torch.from_numpy(b.slots).to(dev)
     pre = torch.from_numpy(b.prefill_rows()).to(dev)
     pkv.kv_append(kc, vc, b.k_hist[pre], b.v_hist[pre], slots[pre])
@@ -260,7 +265,7 @@ def run_pkv(args, rank, world, local):
     kblock = 16 if args.workload == "long_bs64_k16" else b.block_size
     ratio = b.block_size // kblock
     kview = (b.num_blocks * ratio, kblock, b.num_kv_heads, b.head_dim)
-    kck, vck = kc.view(kview), vc.view(kview)
+    kck, vck = (kc, vc) if mx else (kc.view(kview), vc.view(kview))
     btk = torch.empty(B, b.max_blocks * ratio, dtype=torch.int32, device=dev)
 
     def decode_call(qq, tables, lens):
@@ -282,7 +287,10 @@ def run_pkv(args, rank, world, local):
         pkv.kv_append(kc, vc, new_k, new_v, step_slots)
         decode_call(q, bt, sl)
 
-    kv_bytes = int(b.seq_lens.astype(np.int64).sum()) * kv_row_bytes(b)
+    # algorithmic bytes: K and V of the visible rows; an MXFP8 row is one byte
+    # per element plus one scale byte per 32
+    row_bytes = 2 * b.num_kv_heads * b.head_dim * 33 // 32 if mx else kv_row_bytes(b)
+    kv_bytes = int(b.seq_lens.astype(np.int64).sum()) * row_bytes
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -368,10 +376,11 @@ def run_pkv(args, rank, world, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": b.dtype,
+        "dtype": "mxfp8 K/V, bf16 q/out" if mx else b.dtype,
         "data": "synthetic (seeded N(0,1) q/k/v, seeded lengths and block placement)",
         "config": {
             "workload": {"llama": "llama3-8b-shaped decode layer",
+                         "llama_mxfp8": "llama3-8b-shaped decode layer over MXFP8 K/V pools",
                          "long_bs16": "long-context decode, block size 16",
                          "long_bs64": "long-context decode, block size 64",
                          "long_bs64_k16": "long-context decode, block size 64 read as "

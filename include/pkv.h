@@ -30,9 +30,27 @@
  *     checked by the kernels: an out-of-range item sets a bit of the device
  *     error word and is skipped.  No kernel traps, asserts or waits without a
  *     time limit.
- *   - dtype is PKV_F32 or PKV_BF16; q, k, v, caches and out share it.
- *     Attention arithmetic is fp32 (accumulators, softmax state) whatever the
- *     storage type; bf16 results are rounded to nearest even.
+ *   - dtype is PKV_F32, PKV_BF16 or PKV_MXFP8.  With PKV_F32 or PKV_BF16,
+ *     q, k, v, caches and out share it; with PKV_MXFP8 (quantized pools,
+ *     below) the caches are MXFP8 and q, k, v and out are bf16.  Attention
+ *     arithmetic is fp32 (accumulators, softmax state) whatever the storage
+ *     type; bf16 results are rounded to nearest even.
+ *   - MXFP8 POOLS.  "M5.3 - KV Memory Layout and Exact Reuse" (0x0BB) names
+ *     quantized K/V a cache-ABI field, and TokenSpeed keeps MXFP8 KV scale
+ *     planes beside the element planes; this library's schema: each K (or V)
+ *     cache buffer holds the element plane, OCP FP8 E4M3 codes laid out
+ *     [num_blocks, block_size, num_kv_heads, head_dim] as above, followed at
+ *     byte offset num_blocks * block_size * num_kv_heads * head_dim by the
+ *     scale plane [num_blocks, num_kv_heads, block_size, head_dim / 32] of
+ *     E8M0 bytes s (the value 2^(s - 127)).  Scale byte (b, h, o, j) scales
+ *     elements (b, o, h, 32 j .. 32 j + 31): element = code value * scale.
+ *     kv_append quantizes: each 32-element group takes the smallest power of
+ *     two X with max |x| / X <= 448 (no element saturates), and each element
+ *     the E4M3 code nearest x / X (ties to even).  The scale plane is
+ *     head-major within a block, so an MXFP8 pool cannot be read through
+ *     tables expanded to smaller kernel blocks.  Supported by kv_append,
+ *     kv_block_copy and the CUDA-core decode (head_dim 64 or 128, Hq / Hkv <=
+ *     4); the tensor-core paths (shared prefix, chunk-first) take bf16 only.
  *   - Pointers to the caches, q, k, v and out must be 16-byte aligned.
  */
 #ifndef PKV_H
@@ -54,7 +72,7 @@ typedef enum {
   PKV_ERR_CAPACITY = 5      /* needs more than the fixed static scratch array */
 } pkv_status;
 
-typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_MXFP8 = 2 } pkv_dtype;
 
 /* Bits of the device error word. */
 #define PKV_DEVERR_SLOT 1u     /* a slot id >= num_blocks * block_size          */

@@ -74,6 +74,18 @@ def _load():
         lib.pkv_oracle_row_ledger.argtypes = [vp, i32, vp, i32, i64, i32, p64, p64]
         lib.pkv_oracle_expand_table.restype = i32
         lib.pkv_oracle_expand_table.argtypes = [vp, i64, i32, vp]
+        lib.pkv_oracle_e4m3_decode.restype = dbl
+        lib.pkv_oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.pkv_oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.pkv_oracle_e4m3_encode.argtypes = [dbl]
+        lib.pkv_oracle_e4m3_encode_exhaustive.restype = ctypes.c_uint8
+        lib.pkv_oracle_e4m3_encode_exhaustive.argtypes = [dbl]
+        lib.pkv_oracle_mx_scale.restype = ctypes.c_uint8
+        lib.pkv_oracle_mx_scale.argtypes = [dbl]
+        lib.pkv_oracle_kv_append_mxfp8.restype = i32
+        lib.pkv_oracle_kv_append_mxfp8.argtypes = [i32, vp, vp, i64, i32, i32, i32, vp, vp, vp, i64]
+        lib.pkv_oracle_mxfp8_to_f32.restype = i32
+        lib.pkv_oracle_mxfp8_to_f32.argtypes = [vp, i64, i32, i32, i32, vp]
         lib.pkv_oracle_chunk_tree.restype = i32
         lib.pkv_oracle_chunk_tree.argtypes = [i32, vp, vp, vp, i64, i32, i32, i32, vp, vp, vp, vp,
                                               i32, vp, i64, i32, i32, dbl, vp, vp, i32]
@@ -214,6 +226,57 @@ def chunk_tree(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, chunks,
     if st != OK:
         raise ValueError(f"oracle chunk_tree rejected its inputs (status {st})")
     return out, lse
+
+
+# ------------------------------------------------------------------ MXFP8 pools
+def e4m3_decode(code: int) -> float:
+    """Value of an OCP FP8 E4M3 code."""
+    return _load().pkv_oracle_e4m3_decode(int(code))
+
+
+def e4m3_encode(x: float) -> int:
+    """E4M3 code of x: nearest, ties to even, saturating at 448."""
+    return int(_load().pkv_oracle_e4m3_encode(float(x)))
+
+
+def e4m3_encode_exhaustive(x: float) -> int:
+    """E4M3 code of x by searching every finite code for the nearest value."""
+    return int(_load().pkv_oracle_e4m3_encode_exhaustive(float(x)))
+
+
+def mx_scale(amax: float) -> int:
+    """E8M0 scale byte of a 32-element group: smallest 2^(s - 127) with
+    amax / 2^(s - 127) <= 448."""
+    return int(_load().pkv_oracle_mx_scale(float(amax)))
+
+
+def mxfp8_pool_bytes(num_blocks: int, block_size: int, num_kv_heads: int, head_dim: int) -> int:
+    """Bytes of one MXFP8 cache buffer: the element plane, then the scale plane."""
+    n = num_blocks * block_size * num_kv_heads * head_dim
+    return n + n // 32
+
+
+def kv_append_mxfp8(k_cache: np.ndarray, v_cache: np.ndarray, shape, k: np.ndarray,
+                    v: np.ndarray, slot_mapping) -> int:
+    """Quantize rows k, v ([N, Hkv, D], float32 or bf16 bits) into MXFP8
+    pools (flat uint8 buffers of mxfp8_pool_bytes(*shape))."""
+    nb, p, hkv, d = shape
+    assert k_cache.dtype == np.uint8 and k_cache.size == mxfp8_pool_bytes(nb, p, hkv, d)
+    sl = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    k = np.ascontiguousarray(k)
+    v = np.ascontiguousarray(v)
+    return _load().pkv_oracle_kv_append_mxfp8(_dtype_code(k), _ptr(k_cache), _ptr(v_cache), nb, p,
+                                              hkv, d, _ptr(k), _ptr(v), _ptr(sl), len(sl))
+
+
+def mxfp8_to_f32(cache: np.ndarray, shape) -> np.ndarray:
+    """The fp32 values [NB, P, Hkv, D] an MXFP8 pool holds (exact)."""
+    nb, p, hkv, d = shape
+    out = np.empty((nb, p, hkv, d), np.float32)
+    st = _load().pkv_oracle_mxfp8_to_f32(_ptr(cache), nb, p, hkv, d, _ptr(out))
+    if st != OK:
+        raise ValueError(f"oracle mxfp8_to_f32 rejected its inputs (status {st})")
+    return out
 
 
 def row_ledger(block_tables: np.ndarray, seq_lens: np.ndarray, num_pool_blocks: int,

@@ -313,6 +313,132 @@ int pkv_oracle_chunk_tree(int dtype, const void* q, const void* k_cache,
   return status;
 }
 
+/* ---------------------------------------------------------------- MXFP8 */
+
+double pkv_oracle_e4m3_decode(uint8_t code) {
+  const int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double mag = e == 0 ? ldexp((double)m, -9)               /* m/8 * 2^-6 */
+                            : ldexp(8.0 + m, e - 10);             /* (1 + m/8) * 2^(e-7) */
+  return sign ? -mag : mag;
+}
+
+uint8_t pkv_oracle_e4m3_encode_exhaustive(double x) {
+  const uint8_t sign = x < 0 || (x == 0 && signbit(x)) ? 0x80 : 0;
+  double a = fabs(x);
+  if (a >= 448.0) return sign | 0x7E; /* saturate */
+  /* candidates are the finite codes 0..126 in increasing magnitude: find the
+   * nearest, ties to the even code (even mantissa) */
+  uint8_t best = 0;
+  double best_d = INFINITY;
+  for (int c = 0; c <= 0x7E; ++c) {
+    const double d = fabs(pkv_oracle_e4m3_decode((uint8_t)c) - a);
+    if (d < best_d || (d == best_d && (c & 1) == 0)) {
+      best = (uint8_t)c;
+      best_d = d;
+    }
+  }
+  return sign | best;
+}
+
+uint8_t pkv_oracle_e4m3_encode(double x) {
+  const uint8_t sign = x < 0 || (x == 0 && signbit(x)) ? 0x80 : 0;
+  const double a = fabs(x);
+  if (a >= 448.0) return sign | 0x7E; /* 448 and beyond: the largest finite */
+  if (a < 0.015625) {                 /* below 2^-6: subnormal steps of 2^-9 */
+    /* rint rounds to nearest, ties to even (the default mode); 8 steps of
+     * 2^-9 is 2^-6, the smallest normal, which is code 8 */
+    return sign | (uint8_t)rint(ldexp(a, 9));
+  }
+  int k;
+  frexp(a, &k);                       /* a = f 2^k, f in [0.5, 1) */
+  int E = k - 1;                      /* a = s 2^E, s in [1, 2) */
+  int q = (int)rint((ldexp(a, -E) - 1.0) * 8.0);  /* 3 mantissa bits, ties to even */
+  if (q == 8) {                       /* rounded up to the next power of two */
+    q = 0;
+    ++E;
+  }
+  return sign | (uint8_t)(((E + 7) << 3) | q);
+}
+
+uint8_t pkv_oracle_mx_scale(double amax) {
+  if (!(amax > 0)) return 0;
+  /* the smallest e with amax <= 448 * 2^e: a first guess from the binary
+   * exponent of amax / 448, settled by exact comparisons (448 * 2^e is exact
+   * in binary64) */
+  int k;
+  frexp(amax / 448.0, &k);
+  int e = k;
+  while (e > -127 && amax <= ldexp(448.0, e - 1)) --e;
+  while (e < 127 && amax > ldexp(448.0, e)) ++e;
+  if (e < -127) e = -127;
+  return (uint8_t)(e + 127);
+}
+
+static double load_in(int in_dtype, const void* base, int64_t idx) {
+  return load_elem(in_dtype, base, idx);
+}
+
+int pkv_oracle_kv_append_mxfp8(int in_dtype, uint8_t* k_cache, uint8_t* v_cache,
+                               int64_t num_blocks, int block_size,
+                               int num_kv_heads, int head_dim, const void* k,
+                               const void* v, const int64_t* slots,
+                               int64_t num_tokens) {
+  if (num_tokens < 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      head_dim % 32 != 0)
+    return PKV_ORACLE_BAD_ARG;
+  const int64_t P = block_size, H = num_kv_heads, D = head_dim;
+  const int64_t num_slots = num_blocks * P;
+  const int64_t plane = num_blocks * P * H * D;
+  int status = PKV_ORACLE_OK;
+  for (int64_t i = 0; i < num_tokens; ++i) {
+    const int64_t s = slots[i];
+    if (s < 0) continue;
+    if (s >= num_slots) { status = PKV_ORACLE_BAD_SLOT; continue; }
+    const int64_t blk = s / P, off = s % P;
+    for (int kv = 0; kv < 2; ++kv) {
+      const void* src = kv ? v : k;
+      uint8_t* cache = kv ? v_cache : k_cache;
+      for (int64_t h = 0; h < H; ++h) {
+        for (int64_t g = 0; g < D / 32; ++g) {
+          const int64_t in0 = (i * H + h) * D + g * 32;
+          double amax = 0;
+          for (int j = 0; j < 32; ++j) {
+            const double x = fabs(load_in(in_dtype, src, in0 + j));
+            if (x > amax) amax = x;
+          }
+          const uint8_t sc = pkv_oracle_mx_scale(amax);
+          cache[plane + ((blk * H + h) * P + off) * (D / 32) + g] = sc;
+          for (int j = 0; j < 32; ++j) {
+            const double x = load_in(in_dtype, src, in0 + j);
+            cache[((blk * P + off) * H + h) * D + g * 32 + j] =
+                pkv_oracle_e4m3_encode(ldexp(x, 127 - (int)sc));
+          }
+        }
+      }
+    }
+  }
+  return status;
+}
+
+int pkv_oracle_mxfp8_to_f32(const uint8_t* cache, int64_t num_blocks,
+                            int block_size, int num_kv_heads, int head_dim,
+                            float* out) {
+  if (num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim % 32 != 0)
+    return PKV_ORACLE_BAD_ARG;
+  const int64_t P = block_size, H = num_kv_heads, D = head_dim;
+  const int64_t plane = num_blocks * P * H * D;
+  for (int64_t b = 0; b < num_blocks; ++b)
+    for (int64_t o = 0; o < P; ++o)
+      for (int64_t h = 0; h < H; ++h)
+        for (int64_t c = 0; c < D; ++c) {
+          const int64_t e = ((b * P + o) * H + h) * D + c;
+          const int sc = cache[plane + ((b * H + h) * P + o) * (D / 32) + c / 32];
+          out[e] = (float)ldexp(pkv_oracle_e4m3_decode(cache[e]), sc - 127);
+        }
+  return PKV_ORACLE_OK;
+}
+
 int pkv_oracle_row_ledger(const int32_t* block_tables, int max_blocks,
                           const int32_t* seq_lens, int num_seqs,
                           int64_t num_blocks, int block_size,

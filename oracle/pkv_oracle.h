@@ -146,6 +146,49 @@ int pkv_oracle_chunk_tree(int dtype, const void* q, const void* k_cache,
                           double scale, double* out, double* lse,
                           int nthreads);
 
+/* ------------------------------------------------------------------------
+ * MXFP8 pools: a quantized storage schema ([M5.3] 0x0BB names quantized K/V
+ * a cache-ABI field; TokenSpeed's MXFP8 KV keeps scale planes beside the
+ * element planes).  Elements are OCP FP8 E4M3 (bias 7, 3 mantissa bits,
+ * subnormals, no infinities, 0x7F / 0xFF NaN, largest finite 448); every 32
+ * consecutive head_dim elements of one (token, kv head) row share an E8M0
+ * scale byte s (the value 2^(s - 127)).  A cache buffer holds the element
+ * plane [NB, P, Hkv, D] followed by the scale plane [NB, Hkv, P, D / 32].
+ */
+
+/* E4M3 value of a code (NaN codes return NaN). */
+double pkv_oracle_e4m3_decode(uint8_t code);
+
+/* E4M3 code of x: round to nearest, ties to even, |x| beyond 448 saturating
+ * to 448 (x must not be NaN). */
+uint8_t pkv_oracle_e4m3_encode(double x);
+
+/* The same code by searching all finite codes for the nearest value (ties
+ * to the even code): slow, for checking pkv_oracle_e4m3_encode. */
+uint8_t pkv_oracle_e4m3_encode_exhaustive(double x);
+
+/* Scale byte of a 32-element group with largest magnitude amax: the
+ * smallest power of two X = 2^(s - 127) with amax / X <= 448, so that no
+ * element saturates; clamped to s in [0, 254]; s = 0 for amax = 0. */
+uint8_t pkv_oracle_mx_scale(double amax);
+
+/* Write rows into an MXFP8 pool: for each token i with slot s >= 0, every
+ * kv head's D elements of k[i] / v[i] (bf16 bits, or fp32 when
+ * in_dtype == PKV_ORACLE_F32) are quantized group by group (scale from the
+ * group's largest magnitude, element = E4M3 of x / 2^(s - 127)) into the
+ * element and scale planes at that slot.  Returns as pkv_oracle_kv_append. */
+int pkv_oracle_kv_append_mxfp8(int in_dtype, uint8_t* k_cache, uint8_t* v_cache,
+                               int64_t num_blocks, int block_size,
+                               int num_kv_heads, int head_dim, const void* k,
+                               const void* v, const int64_t* slots,
+                               int64_t num_tokens);
+
+/* Dequantize an MXFP8 pool to fp32 [NB, P, Hkv, D] (exact: an E4M3 value
+ * times a power of two within fp32's range for scales from bf16 data). */
+int pkv_oracle_mxfp8_to_f32(const uint8_t* cache, int64_t num_blocks,
+                            int block_size, int num_kv_heads, int head_dim,
+                            float* out);
+
 /* K/V row ledger of a batch ([M5.3] 0x02D, 0x0BI): logical rows are the sum of
  * the requests' context lengths, unique rows the number of distinct
  * (physical block, offset) slots they reference.  Slots are counted in a

@@ -7,6 +7,8 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -114,6 +116,17 @@ __device__ __forceinline__ void bulk_wait_group_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Bulk copy global -> shared of `bytes` (a multiple of 16; both addresses
+// 16-byte aligned), completing on `bar` (complete_tx).
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Prefetch `bytes` (a multiple of 16) of global memory from a 16-byte
 // aligned address into L2, asynchronously.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
@@ -201,6 +214,42 @@ struct VecLoad<__nv_bfloat16, N> {
     }
   }
 };
+
+// E4M3 codes (the elements of an MXFP8 pool), widened exactly through fp16.
+// The caller applies the group's power-of-two scale.
+template <int N>
+struct VecLoad<__nv_fp8_e4m3, N> {
+  static_assert(N % 4 == 0, "fp8 vectors are loaded four at a time at least");
+  __device__ __forceinline__ static void run(const __nv_fp8_e4m3* p, float (&f)[N]) {
+    if constexpr (N % 8 == 0) {
+#pragma unroll
+      for (int i = 0; i < N / 8; ++i) {
+        const uint2 x = reinterpret_cast<const uint2*>(p)[i];
+        widen4(x.x, f + 8 * i);
+        widen4(x.y, f + 8 * i + 4);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < N / 4; ++i) widen4(reinterpret_cast<const uint32_t*>(p)[i], f + 4 * i);
+    }
+  }
+  __device__ __forceinline__ static void widen4(uint32_t w, float* f) {
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+    f[0] = a.x;
+    f[1] = a.y;
+    f[2] = b.x;
+    f[3] = b.y;
+  }
+};
+
+// 2^(s - 127) for an E8M0 scale byte s in [0, 254] (s = 0 is the fp32
+// subnormal 2^-127).
+__device__ __forceinline__ float e8m0_value(uint32_t s) {
+  return __uint_as_float(s ? s << 23 : 0x00400000u);
+}
 
 __device__ __forceinline__ void store_out(float* p, float v) { *p = v; }
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }

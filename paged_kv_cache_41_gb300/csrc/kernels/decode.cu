@@ -58,6 +58,21 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Sources a merging warp loads at once (their latencies overlap).
 constexpr int kMergeBatch = 8;
 
+// The element storage of the pool -> the type of q and out (bf16 beside an
+// MXFP8 pool, whose stages also carry their rows' E8M0 scales).
+template <typename T>
+struct IoOf {
+  using type = T;
+};
+template <>
+struct IoOf<__nv_fp8_e4m3> {
+  using type = __nv_bfloat16;
+};
+template <typename T>
+constexpr bool kIsMx = false;
+template <>
+constexpr bool kIsMx<__nv_fp8_e4m3> = true;
+
 // Stage descriptor flags.
 constexpr int kPieceStart = 1;   // first stage of a piece: reset the state, load q
 constexpr int kPieceEnd = 2;     // last stage of a piece: merge the warps and write
@@ -67,19 +82,22 @@ constexpr int kSlot1 = 8;        // a cut piece that is not the CTA's first: rec
 struct DecodeSmem {
   int tile_elems;   // rows * head_dim of one K (or V) tile
   int stages;
-  size_t tiles_bytes, bar_off, ok_off, desc_off, ring_off, scratch_off, total;
+  size_t tiles_bytes, scale_off, bar_off, ok_off, desc_off, ring_off, scratch_off, total;
 };
 
 // Stage s holds its K tile then its V tile; both together also hold the
 // [4][G][D] fp32 merge of a piece's end (16 G D bytes <= 2 * 32 * D * b for
-// G <= 8).
+// G <= 8 with 2- and 4-byte elements, G <= 4 with 1-byte ones).
 __host__ __device__ inline DecodeSmem decode_smem_layout(int head_dim, int elem_bytes, int group,
                                                          int stages) {
   DecodeSmem s;
   s.tile_elems = kStageRows * head_dim;
   s.stages = stages;
   s.tiles_bytes = ((size_t)2 * stages * s.tile_elems * elem_bytes + 127) & ~(size_t)127;
-  s.bar_off = s.tiles_bytes;                        // full[stages], empty[stages], merge
+  // MXFP8 (1-byte elements): each stage's K then V scale rows [rows][D / 32]
+  s.scale_off = s.tiles_bytes;
+  const size_t scale_bytes = elem_bytes == 1 ? (size_t)2 * stages * kStageRows * (head_dim / 32) : 0;
+  s.bar_off = s.scale_off + ((scale_bytes + 127) & ~(size_t)127);  // full[stages], empty[stages], merge
   s.ok_off = s.bar_off + (size_t)(2 * stages + 1) * 8;
   s.desc_off = (s.ok_off + (size_t)stages * 4 + 15) & ~(size_t)15;
   s.ring_off = s.desc_off + (size_t)stages * 16;
@@ -110,14 +128,27 @@ int decode_num_stages(int head_dim, int elem_bytes) {
 // up holding value j = l16 / (8/G): row tk = l16 >> 3, head g = j % G.
 template <typename T, int D, int G, bool kTail>
 __device__ __forceinline__ void decode_chunk(const T* __restrict__ kt, const T* __restrict__ vt,
-                                             int row0, int nvalid,
-                                             const float2 (&q2)[G][D / 32],
+                                             const uint8_t* __restrict__ ksc,
+                                             const uint8_t* __restrict__ vsc, int row0,
+                                             int nvalid, const float2 (&q2)[G][D / 32],
                                              float2 (&acc)[G][D / 32], float& m_used,
                                              float& l_run, float* __restrict__ red, int l16) {
   constexpr int EPL = D / 16;
   constexpr int EP2 = EPL / 2;
   constexpr int NV = 2 * G;    // values per half-warp and chunk
   constexpr int LPV = 16 / NV; // lanes summing one value
+  // MXFP8: this lane's EPL elements lie in one 32-element scale group; its
+  // K scale multiplies the lane's partial dot product, its V scale the
+  // weights (both powers of two)
+  float kscale[2] = {1.f, 1.f}, vscale[2] = {1.f, 1.f};
+  if constexpr (kIsMx<T>) {
+    const int grp = l16 * EPL / 32;
+#pragma unroll
+    for (int tk = 0; tk < 2; ++tk) {
+      kscale[tk] = e8m0_value(ksc[(row0 + tk) * (D / 32) + grp]);
+      vscale[tk] = e8m0_value(vsc[(row0 + tk) * (D / 32) + grp]);
+    }
+  }
   // ---- q . k partial sums for rows row0, row0 + 1 and the G heads
   float v[NV];
 #pragma unroll
@@ -129,7 +160,7 @@ __device__ __forceinline__ void decode_chunk(const T* __restrict__ kt, const T* 
       float2 d2 = __fmul2_rn(q2[g][0], make_float2(kf[0], kf[1]));
 #pragma unroll
       for (int j = 1; j < EP2; ++j) d2 = __ffma2_rn(q2[g][j], make_float2(kf[2 * j], kf[2 * j + 1]), d2);
-      v[tk * G + g] = d2.x + d2.y;
+      v[tk * G + g] = kIsMx<T> ? (d2.x + d2.y) * kscale[tk] : d2.x + d2.y;
     }
   }
   // ---- sum each value over the 16 lanes of the half-warp
@@ -181,7 +212,8 @@ __device__ __forceinline__ void decode_chunk(const T* __restrict__ kt, const T* 
       VecLoad<T, EPL>::run(vt + (row0 + tk) * D + l16 * EPL, vf);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float2 p2 = make_float2(pg[tk][g], pg[tk][g]);
+        const float pv = kIsMx<T> ? pg[tk][g] * vscale[tk] : pg[tk][g];
+        const float2 p2 = make_float2(pv, pv);
 #pragma unroll
         for (int e = 0; e < EP2; ++e)
           acc[g][e] = __ffma2_rn(p2, make_float2(vf[2 * e], vf[2 * e + 1]), acc[g][e]);
@@ -194,10 +226,13 @@ template <typename T, int D, int G>
 __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
     decode_partial_kernel(const __grid_constant__ CUtensorMap tmk,
                           const __grid_constant__ CUtensorMap tmv, const DecodeArgs a) {
+  using TQ = typename IoOf<T>::type;  // q and out
   constexpr int EPL = D / 16;  // head_dim elements per lane
   constexpr int EP2 = EPL / 2;
   constexpr int NV = 2 * G;    // (row, head) partial sums per lane per chunk
   static_assert(NV <= 16 && (NV & (NV - 1)) == 0, "group must be 1, 2, 4 or 8");
+  static_assert(!kIsMx<T> || G <= 4, "an MXFP8 stage tile holds the merge of up to 4 heads");
+  constexpr int kScaleRow = D / 32;  // MXFP8 scale bytes per row
 
   const int c = blockIdx.x;
   const int Hkv = a.num_kv_heads, P = a.block_size;
@@ -237,11 +272,11 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
   // descriptor.
   auto load_q = [&](int r, int h) {
     const int64_t qr = a.q_rows ? __ldg(a.q_rows + r) : r;
-    const T* qp = static_cast<const T*>(a.q) + (qr * a.num_q_heads + (int64_t)h * G) * D + l16 * EPL;
+    const TQ* qp = static_cast<const TQ*>(a.q) + (qr * a.num_q_heads + (int64_t)h * G) * D + l16 * EPL;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       float f[EPL];
-      VecLoad<T, EPL>::run(qp + g * D, f);
+      VecLoad<TQ, EPL>::run(qp + g * D, f);
 #pragma unroll
       for (int j = 0; j < EP2; ++j) q2[g][j] = make_float2(f[2 * j] * a.qscale, f[2 * j + 1] * a.qscale);
     }
@@ -268,6 +303,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
   // batch's first stage, cpnt / cT the stages and length of sequence cr.
   int cr = d0.x, ch = d0.y, ci = d0.z, cpnt = 0, cT = 0;
   const uint32_t box_bytes = (uint32_t)(TB * D * sizeof(T));
+  const uint32_t scale_box = (uint32_t)(TB * kScaleRow);  // MXFP8 scale bytes of one box
   auto compute_batch = [&](int kb) {
     int r = cr, h = ch, i = ci + lane, pnt = cpnt, len = cT;
     const bool act = kb + lane < n;
@@ -295,8 +331,8 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
                         (end && i == pnt - 1 && dseg >= 0 ? kWhole : 0) | (dseg > 0 ? kSlot1 : 0);
       if (flags & kPieceStart) {  // the piece's q rows, into L2 long before they are read
         const int64_t qr = a.q_rows ? __ldg(a.q_rows + r) : r;
-        prefetch_l2_bulk(static_cast<const T*>(a.q) + (qr * a.num_q_heads + (int64_t)h * G) * D,
-                         (uint32_t)(G * D * sizeof(T)));
+        prefetch_l2_bulk(static_cast<const TQ*>(a.q) + (qr * a.num_q_heads + (int64_t)h * G) * D,
+                         (uint32_t)(G * D * sizeof(TQ)));
       }
       dA[k & 63] = make_int4(id0, id1, row0 - b0 * P, nbox);
       dB[k & 63] = make_int4(r, h, nvalid, flags);
@@ -326,15 +362,29 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
     } else {
       if (lane == 0) {
         stage_ok[st] = 1;
-        mbar_arrive_expect_tx(&full[st], 2u * box_bytes * (uint32_t)nbox);
+        mbar_arrive_expect_tx(&full[st], 2u * (box_bytes + (kIsMx<T> ? scale_box : 0u)) * (uint32_t)nbox);
       }
       __syncwarp();
-      // one box per lane: lanes 0..nbox-1 load K, lanes 16..16+nbox-1 load V
+      // one box per lane: lanes 0..nbox-1 load K, lanes 16..16+nbox-1 load V;
+      // MXFP8: lanes 8.. and 24.. copy the same boxes' scale rows, which lie
+      // contiguously in the head-major scale plane
       const int j = lane & 15;
       if (j < nbox) {
         T* dst = tiles + (size_t)st * 2 * L.tile_elems + (lane < 16 ? 0 : L.tile_elems) + j * TB * D;
         tma_load_4d(dst, lane < 16 ? &tmk : &tmv, 0, db.y, j == 0 ? da.z : 0, j == 0 ? da.x : da.y,
                     &full[st]);
+      }
+      if constexpr (kIsMx<T>) {
+        const int js = j - 8;
+        if (js >= 0 && js < nbox) {
+          const int64_t blk = js == 0 ? da.x : da.y;
+          const int row = js == 0 ? da.z : 0;
+          const uint8_t* src = (lane < 16 ? a.k_scales : a.v_scales) +
+                               ((blk * Hkv + db.y) * P + row) * kScaleRow;
+          uint8_t* sdst = smem + L.scale_off + (size_t)st * 2 * kStageRows * kScaleRow +
+                          (lane < 16 ? 0 : kStageRows * kScaleRow) + js * TB * kScaleRow;
+          bulk_load(sdst, src, scale_box, &full[st]);
+        }
       }
     }
     if ((k & 31) == 0 && k + 32 < n) compute_batch(k + 32);
@@ -382,6 +432,8 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
     const int nvalid = dsc.z, flags = dsc.w;
     const T* kt = tiles + (size_t)s * 2 * L.tile_elems;
     const T* vt = kt + L.tile_elems;
+    const uint8_t* ksc = smem + L.scale_off + (size_t)s * 2 * kStageRows * kScaleRow;
+    const uint8_t* vsc = ksc + kStageRows * kScaleRow;
     if (flags & kPieceStart) {  // q2 already holds this piece's q
 #pragma unroll
       for (int g = 0; g < G; ++g)
@@ -394,11 +446,11 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
       if (nvalid == kStageRows) {
 #pragma unroll 1
         for (int cc = 0; cc < kStageRows / kChunk; ++cc)
-          decode_chunk<T, D, G, false>(kt, vt, cc * kChunk + rbase, kStageRows, q2, acc, m_used,
+          decode_chunk<T, D, G, false>(kt, vt, ksc, vsc, cc * kChunk + rbase, kStageRows, q2, acc, m_used,
                                        l_run, red, l16);
       } else {
         for (int cc = 0; cc * kChunk < nvalid; ++cc)
-          decode_chunk<T, D, G, true>(kt, vt, cc * kChunk + rbase, nvalid, q2, acc, m_used, l_run,
+          decode_chunk<T, D, G, true>(kt, vt, ksc, vsc, cc * kChunk + rbase, nvalid, q2, acc, m_used, l_run,
                                       red, l16);
       }
     }
@@ -461,7 +513,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
           a.st_o[slot * D + e] = o;
           if (e == 0) a.st_lse[slot] = lse2;
         } else {
-          store_out(static_cast<T*>(a.out) + rh * D + e, o);
+          store_out(static_cast<TQ*>(a.out) + rh * D + e, o);
           if (e == 0 && a.lse_out) a.lse_out[rh] = lse2 * kLn2;
         }
       }
@@ -649,12 +701,19 @@ static int resident_for_group(int group) {
     case 1: return resident_ctas<T, D, 1>();
     case 2: return resident_ctas<T, D, 2>();
     case 4: return resident_ctas<T, D, 4>();
-    case 8: return resident_ctas<T, D, 8>();
+    case 8:
+      if constexpr (!kIsMx<T>) return resident_ctas<T, D, 8>();
+      return 0;
     default: return 0;
   }
 }
 
 int decode_resident_ctas(int dtype, int head_dim, int group) {
+  if (dtype == PKV_MXFP8) {
+    if (group > 4) return 0;
+    return head_dim == 128 ? resident_for_group<__nv_fp8_e4m3, 128>(group)
+                           : resident_for_group<__nv_fp8_e4m3, 64>(group);
+  }
   if (dtype == PKV_BF16)
     return head_dim == 128 ? resident_for_group<__nv_bfloat16, 128>(group)
                            : resident_for_group<__nv_bfloat16, 64>(group);
@@ -669,7 +728,9 @@ static cudaError_t dispatch_group(int group, const CUtensorMap& tmk, const CUten
     case 1: return launch_partial<T, D, 1>(tmk, tmv, a, stream);
     case 2: return launch_partial<T, D, 2>(tmk, tmv, a, stream);
     case 4: return launch_partial<T, D, 4>(tmk, tmv, a, stream);
-    case 8: return launch_partial<T, D, 8>(tmk, tmv, a, stream);
+    case 8:
+      if constexpr (!kIsMx<T>) return launch_partial<T, D, 8>(tmk, tmv, a, stream);
+      return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
 }
@@ -683,7 +744,7 @@ static cudaError_t launch_reduce_t(const DecodeArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_decode_reduce(int dtype, int head_dim, const DecodeArgs& a,
                                  cudaStream_t stream) {
-  if (dtype == PKV_BF16)
+  if (dtype == PKV_BF16 || dtype == PKV_MXFP8)  // out is bf16 beside an MXFP8 pool
     return head_dim == 128 ? launch_reduce_t<__nv_bfloat16, 128>(a, stream)
                            : launch_reduce_t<__nv_bfloat16, 64>(a, stream);
   return head_dim == 128 ? launch_reduce_t<float, 128>(a, stream)
@@ -694,7 +755,10 @@ cudaError_t launch_paged_decode(int dtype, int head_dim, int group, const CUtens
                                 const CUtensorMap& tmv, const DecodeArgs& a,
                                 cudaStream_t stream) {
   cudaError_t e;
-  if (dtype == PKV_BF16)
+  if (dtype == PKV_MXFP8)
+    e = head_dim == 128 ? dispatch_group<__nv_fp8_e4m3, 128>(group, tmk, tmv, a, stream)
+                        : dispatch_group<__nv_fp8_e4m3, 64>(group, tmk, tmv, a, stream);
+  else if (dtype == PKV_BF16)
     e = head_dim == 128 ? dispatch_group<__nv_bfloat16, 128>(group, tmk, tmv, a, stream)
                         : dispatch_group<__nv_bfloat16, 64>(group, tmk, tmv, a, stream);
   else

@@ -55,6 +55,12 @@ cudaError_t launch_kv_append(void* k_cache, void* v_cache, const void* k, const 
 cudaError_t launch_expand_block_tables(const int32_t* in, int64_t n_in, int32_t q, int32_t* out,
                                        unsigned int* err, cudaStream_t stream);
 
+// MXFP8 pools (include/pkv.h): quantize bf16 rows into the element and
+// scale planes; plane_bytes = NB * P * Hkv * D, head_dim 64 or 128.
+cudaError_t launch_kv_append_mxfp8(void* k_cache, void* v_cache, const void* k, const void* v,
+                                   const int64_t* slots, int64_t num_tokens, int num_kv_heads,
+                                   int head_dim, int block_size, int64_t num_slots,
+                                   int64_t plane_bytes, unsigned int* err, cudaStream_t stream);
 cudaError_t launch_kv_block_copy(void* k_cache, void* v_cache, const int64_t* pairs,
                                  int64_t num_pairs, int64_t num_blocks, int64_t block_bytes,
                                  unsigned int* err, cudaStream_t stream);
@@ -76,7 +82,9 @@ __host__ __device__ constexpr int box_rows_for(int block_size) {
 // record per piece, slot 0 of its CTA for the piece holding the CTA's first
 // stage and slot 1 for a last piece that is not also the first.
 struct DecodeArgs {
-  const void* q;                // [B_q, Hq, D]
+  const void* q;                // [B_q, Hq, D] (bf16 beside an MXFP8 pool)
+  const uint8_t* k_scales;      // MXFP8 pools: the scale planes [NB, Hkv, P, D / 32]
+  const uint8_t* v_scales;
   const int32_t* q_rows;        // [B] query row of each sequence, or null: row r
   const int32_t* block_tables;  // [B, max_blocks]
   const int32_t* seq_lens;      // [B]

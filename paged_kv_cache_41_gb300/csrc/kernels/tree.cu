@@ -109,7 +109,7 @@ static cudaError_t launch_merge_t(const TreeMergeArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_tree_merge(int dtype, int head_dim, const TreeMergeArgs& a,
                               cudaStream_t stream) {
-  if (dtype == PKV_BF16)
+  if (dtype == PKV_BF16 || dtype == PKV_MXFP8)  // out is bf16 beside an MXFP8 pool
     return head_dim == 128 ? launch_merge_t<__nv_bfloat16, 128>(a, stream)
                            : launch_merge_t<__nv_bfloat16, 64>(a, stream);
   return head_dim == 128 ? launch_merge_t<float, 128>(a, stream)

@@ -108,7 +108,14 @@ CUresult encode_tiled_cached(CUtensorMap* map, CUtensorMapDataType dtype, cuuint
   return r;
 }
 
-int elem_bytes(int dtype) { return dtype == PKV_BF16 ? 2 : 4; }
+// Bytes of one element of the cache's element plane.
+int elem_bytes(int dtype) { return dtype == PKV_MXFP8 ? 1 : dtype == PKV_BF16 ? 2 : 4; }
+// Bytes of q, k, v and out: bf16 beside an MXFP8 pool.
+int io_bytes(int dtype) { return dtype == PKV_F32 ? 4 : 2; }
+// Byte offset of an MXFP8 pool's scale plane (the element plane's size).
+int64_t mx_plane_bytes(const pkv_cache_desc* c) {
+  return c->num_blocks * c->block_size * c->num_kv_heads * c->head_dim;
+}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -116,7 +123,8 @@ pkv_status check_cache(const pkv_cache_desc* c) {
   if (!c) return PKV_ERR_INVALID_ARG;
   if (c->num_blocks <= 0 || c->block_size <= 0 || c->num_kv_heads <= 0 || c->head_dim <= 0)
     return PKV_ERR_INVALID_ARG;
-  if (c->dtype != PKV_F32 && c->dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  if (c->dtype != PKV_F32 && c->dtype != PKV_BF16 && c->dtype != PKV_MXFP8)
+    return PKV_ERR_INVALID_ARG;
   return PKV_OK;
 }
 
@@ -131,6 +139,7 @@ pkv_status check_attention_shape(const pkv_cache_desc* c, int32_t num_q_heads) {
   if (num_q_heads <= 0 || num_q_heads % c->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   const int G = num_q_heads / c->num_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return PKV_ERR_UNSUPPORTED;
+  if (c->dtype == PKV_MXFP8 && G > 4) return PKV_ERR_UNSUPPORTED;  // the CUDA-core decode only
   if (c->num_kv_heads > 65535 || c->num_blocks > INT32_MAX) return PKV_ERR_UNSUPPORTED;
   return PKV_OK;
 }
@@ -144,8 +153,10 @@ pkv_status encode_cache_map(CUtensorMap* map, const pkv_cache_desc* c, const voi
                         (cuuint64_t)c->block_size, (cuuint64_t)c->num_blocks};
   cuuint64_t strides[3] = {dims[0] * es, dims[0] * dims[1] * es, dims[0] * dims[1] * dims[2] * es};
   cuuint32_t box[4] = {(cuuint32_t)c->head_dim, 1, (cuuint32_t)rows, 1};
-  CUresult r = encode_tiled_cached(map, c->dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+  const CUtensorMapDataType dt = c->dtype == PKV_BF16    ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                : c->dtype == PKV_MXFP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  CUresult r = encode_tiled_cached(map, dt,
                                    4, const_cast<void*>(base), dims, strides, box,
                                    CU_TENSOR_MAP_SWIZZLE_NONE);
   if (r == CUDA_ERROR_NOT_INITIALIZED) return PKV_ERR_CUDA;
@@ -223,6 +234,10 @@ pkv_status launch_decode(const pkv_cache_desc* cache, int G, const void* q, cons
   // stage split is as good, with a cheaper plan; the tensor-core decode's
   // 128-row stages dwarf a piece.
   const bool tc = use_tc_decode(cache, G);
+  if (cache->dtype == PKV_MXFP8) {  // the scale planes follow the element planes
+    a.k_scales = static_cast<const uint8_t*>(k_cache) + mx_plane_bytes(cache);
+    a.v_scales = static_cast<const uint8_t*>(v_cache) + mx_plane_bytes(cache);
+  }
   const bool short_segments =
       (int64_t)a.max_blocks * cache->block_size <= 32LL * pkv::kStageRows;
   a.stage_units = !tc && short_segments ? 2 : 1;
@@ -388,12 +403,21 @@ pkv_status pkv_kv_append(const pkv_cache_desc* cache, void* k_cache, void* v_cac
   if (row_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
   if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k) || !aligned16(v))
     return PKV_ERR_INVALID_ARG;
-  if ((num_tokens + 7) / 8 > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  if ((num_tokens * cache->num_kv_heads + 7) / 8 > INT32_MAX) return PKV_ERR_UNSUPPORTED;
   unsigned int* err = device_error_word();
   if (!err) return PKV_ERR_CUDA;
-  cudaError_t e = pkv::launch_kv_append(k_cache, v_cache, k, v, slot_mapping, num_tokens,
-                                        cache->num_blocks * cache->block_size, row_bytes, err,
-                                        as_stream(stream));
+  cudaError_t e;
+  if (cache->dtype == PKV_MXFP8) {  // quantize bf16 rows into the two planes
+    if (cache->head_dim != 64 && cache->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    e = pkv::launch_kv_append_mxfp8(k_cache, v_cache, k, v, slot_mapping, num_tokens,
+                                    cache->num_kv_heads, cache->head_dim, cache->block_size,
+                                    cache->num_blocks * cache->block_size, mx_plane_bytes(cache),
+                                    err, as_stream(stream));
+  } else {
+    e = pkv::launch_kv_append(k_cache, v_cache, k, v, slot_mapping, num_tokens,
+                              cache->num_blocks * cache->block_size, row_bytes, err,
+                              as_stream(stream));
+  }
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -407,12 +431,22 @@ pkv_status pkv_kv_block_copy(const pkv_cache_desc* cache, void* k_cache, void* v
   const int64_t block_bytes = (int64_t)cache->block_size * cache->num_kv_heads * cache->head_dim *
                               elem_bytes(cache->dtype);
   if (block_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
+  if (cache->dtype == PKV_MXFP8 && (cache->head_dim % 32 != 0 || (block_bytes / 32) % 16 != 0))
+    return PKV_ERR_UNSUPPORTED;
   if (!aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_INVALID_ARG;
   if (num_pairs > INT32_MAX || block_bytes / 16 / 1024 + 1 > 65535) return PKV_ERR_UNSUPPORTED;
   unsigned int* err = device_error_word();
   if (!err) return PKV_ERR_CUDA;
   cudaError_t e = pkv::launch_kv_block_copy(k_cache, v_cache, src_dst_pairs, num_pairs,
                                             cache->num_blocks, block_bytes, err, as_stream(stream));
+  if (e == cudaSuccess && cache->dtype == PKV_MXFP8) {
+    // the scale plane holds a block's scales contiguously too: copy them alike
+    const int64_t plane = mx_plane_bytes(cache);
+    e = pkv::launch_kv_block_copy(static_cast<unsigned char*>(k_cache) + plane,
+                                  static_cast<unsigned char*>(v_cache) + plane, src_dst_pairs,
+                                  num_pairs, cache->num_blocks, block_bytes / 32, err,
+                                  as_stream(stream));
+  }
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

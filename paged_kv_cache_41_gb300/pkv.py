@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libpkv.so")
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA, PKV_ERR_DEVICE, PKV_ERR_CAPACITY = range(6)
 # PKV_STATIC_SCRATCH_BYTES of include/pkv.h: the library-owned scratch array
 STATIC_SCRATCH_BYTES = 16 << 20
-PKV_F32, PKV_BF16 = 0, 1
+PKV_F32, PKV_BF16, PKV_MXFP8 = 0, 1, 2
 DEVERR_SLOT, DEVERR_BLOCK, DEVERR_LENGTH, DEVERR_TIMEOUT = 1, 2, 4, 8
 
 EXPORTED = [
@@ -126,8 +126,43 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
 
-def cache_desc(k_cache: torch.Tensor) -> CacheDesc:
-    """Descriptor of a [num_blocks, block_size, num_kv_heads, head_dim] pool."""
+class MxPool:
+    """An MXFP8 K (or V) pool (include/pkv.h): one uint8 device buffer holding
+    the E4M3 element plane [num_blocks, block_size, num_kv_heads, head_dim]
+    followed by the E8M0 scale plane [num_blocks, num_kv_heads, block_size,
+    head_dim / 32].  q, k, v and out beside it are bf16."""
+
+    def __init__(self, num_blocks, block_size, num_kv_heads, head_dim, device="cuda", fill=0):
+        self.shape = (int(num_blocks), int(block_size), int(num_kv_heads), int(head_dim))
+        n = num_blocks * block_size * num_kv_heads * head_dim
+        self.plane_bytes = n
+        self.buf = torch.full((n + n // 32,), fill, dtype=torch.uint8, device=device)
+
+    @property
+    def device(self):
+        return self.buf.device
+
+    def data_ptr(self) -> int:
+        return self.buf.data_ptr()
+
+    @property
+    def elements(self) -> torch.Tensor:
+        """The element plane as raw E4M3 codes (uint8)."""
+        return self.buf[:self.plane_bytes].view(self.shape)
+
+    @property
+    def scales(self) -> torch.Tensor:
+        """The scale plane (E8M0 bytes)."""
+        nb, p, hkv, d = self.shape
+        return self.buf[self.plane_bytes:].view(nb, hkv, p, d // 32)
+
+
+def cache_desc(k_cache) -> CacheDesc:
+    """Descriptor of a [num_blocks, block_size, num_kv_heads, head_dim] pool
+    (a bf16 or fp32 tensor, or an MxPool)."""
+    if isinstance(k_cache, MxPool):
+        nb, p, hkv, d = k_cache.shape
+        return CacheDesc(nb, p, hkv, d, PKV_MXFP8)
     if k_cache.dim() != 4 or not k_cache.is_contiguous():
         raise ValueError("cache must be a contiguous [NB, P, Hkv, D] tensor")
     if k_cache.dtype == torch.bfloat16:

@@ -647,3 +647,108 @@ def test_loop10_shared_work_ledger():
         bt = np.array([t + [-1] * (width - len(t)) for t in tables], np.int32)
         lo, un = oracle.row_ledger(bt, np.array(lens, np.int32), nxt, p)
         assert (lo, un, lo - un) == (logical, unique, saved)
+
+
+# ------------------------------------------------------------------ MXFP8 pools
+def test_e4m3_decode_table():
+    # every code against torch's float8_e4m3fn, and the format's closed forms
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).double().numpy()
+    got = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(got[~np.isnan(got)], ref[~np.isnan(ref)])
+    assert oracle.e4m3_decode(0x38) == 1.0 and oracle.e4m3_decode(0x7E) == 448.0
+    assert oracle.e4m3_decode(0x01) == 2.0 ** -9 and oracle.e4m3_decode(0x08) == 2.0 ** -6
+    assert oracle.e4m3_decode(0x07) == 7 * 2.0 ** -9 and oracle.e4m3_decode(0xB8) == -1.0
+    assert math.isnan(oracle.e4m3_decode(0x7F)) and math.isnan(oracle.e4m3_decode(0xFF))
+
+
+def test_e4m3_encode_matches_search_and_library():
+    # nearest code, ties to even: the arithmetic encoder against a search over
+    # every finite code, and against torch's conversion (which overflows to NaN
+    # past 464, where the encoder saturates instead)
+    bits = (np.arange(0, 0x7F80, 5, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+    x = np.concatenate([bits, -bits[::3]])
+    fast = np.array([oracle.e4m3_encode(v) for v in x])
+    search = np.array([oracle.e4m3_encode_exhaustive(v) for v in x[::4]])
+    assert np.array_equal(fast[::4], search)
+    m = np.abs(x) <= 464
+    lib = torch.tensor(x[m]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(fast[m], lib)
+
+
+def test_e4m3_ties_and_saturation():
+    vals = [oracle.e4m3_decode(c) for c in range(0x7F)]
+    for c in range(0x7E):  # the midpoint of neighbours goes to the even code
+        mid = (vals[c] + vals[c + 1]) / 2
+        assert oracle.e4m3_encode(mid) == (c if c % 2 == 0 else c + 1)
+    for big in (448.0, 463.99, 464.0, 465.0, 1e9):
+        assert oracle.e4m3_encode(big) == 0x7E and oracle.e4m3_encode(-big) == 0xFE
+    assert oracle.e4m3_encode(2.0 ** -10) == 0 and oracle.e4m3_encode(3 * 2.0 ** -10) == 2
+
+
+def test_mx_scale_is_the_smallest_power_that_fits():
+    rng = np.random.default_rng(3)
+    amax = np.concatenate([np.exp(rng.uniform(-80, 80, 500)), 448.0 * 2.0 ** np.arange(-60, 60)])
+    for a in amax:
+        s = oracle.mx_scale(a)
+        assert 0 < s <= 254
+        assert a <= 448.0 * 2.0 ** (s - 127) and a > 448.0 * 2.0 ** (s - 128)
+    assert oracle.mx_scale(0.0) == 0
+
+
+def _mx_shape():
+    return (6, 16, 2, 64)
+
+
+def test_mxfp8_append_layout_and_roundtrip():
+    shape = _mx_shape()
+    nb, p, hkv, d = shape
+    rng = np.random.default_rng(9)
+    n = 5
+    # group g of every row: E4M3 values times 2^k with the group's largest
+    # magnitude 448 * 2^k, so the scale is 2^k and the round trip is exact
+    codes = rng.integers(0, 0x7E, size=(n, hkv, d))
+    codes[:, :, ::32] = 0x7E
+    vals = np.array([[[oracle.e4m3_decode(c) for c in row] for row in head] for head in codes])
+    ks = rng.integers(-20, 20, size=(n, hkv, d // 32))
+    x = (vals * np.repeat(2.0 ** ks, 32, axis=2)).astype(np.float32)
+    kc = np.full(oracle.mxfp8_pool_bytes(*shape), 0xFF, np.uint8)
+    vc = kc.copy()
+    slots = np.array([0, 17, 33, -1, 95], np.int64)
+    assert oracle.kv_append_mxfp8(kc, vc, shape, x, x, slots) == oracle.OK
+    plane = nb * p * hkv * d
+    for i, s in enumerate(slots):
+        if s < 0:
+            continue
+        b, o = divmod(int(s), p)
+        for h in range(hkv):
+            el = kc[((b * p + o) * hkv + h) * d:((b * p + o) * hkv + h + 1) * d]
+            assert np.array_equal(el, codes[i, h].astype(np.uint8))
+            sc = kc[plane + ((b * hkv + h) * p + o) * (d // 32):][:d // 32]
+            assert np.array_equal(sc.astype(int) - 127, ks[i, h])
+    deq = oracle.mxfp8_to_f32(kc, shape).reshape(nb * p, hkv, d)
+    for i, s in enumerate(slots):
+        if s >= 0:
+            assert np.array_equal(deq[s], x[i])
+    # untouched slots keep their bytes (0xFF: NaN codes)
+    assert np.isnan(deq[1]).all()
+
+
+def test_mxfp8_append_error_bound_and_no_saturation():
+    shape = (4, 16, 1, 128)
+    rng = np.random.default_rng(4)
+    x = (rng.standard_normal((10, 1, 128)) * np.exp(rng.uniform(-5, 5, (10, 1, 1)))).astype(np.float32)
+    kc = np.zeros(oracle.mxfp8_pool_bytes(*shape), np.uint8)
+    vc = kc.copy()
+    assert oracle.kv_append_mxfp8(kc, vc, shape, x, x, np.arange(10)) == oracle.OK
+    deq = oracle.mxfp8_to_f32(kc, shape).reshape(-1, 1, 128)[:10]
+    g = x.reshape(10, 4, 32).astype(np.float64)
+    q = deq.reshape(10, 4, 32).astype(np.float64)
+    X = 2.0 ** (kc[4 * 16 * 128:][:40].reshape(10, 4).astype(int) - 127)
+    scaled = np.abs(g) / X[:, :, None]
+    assert scaled.max() <= 448 and (scaled.max(axis=2) > 224).all()  # fits, and the smallest scale
+    # nearest-code error: at most half a step of 2^(floor(log2|v|) - 3), or of 2^-9 below 2^-6
+    step = np.where(scaled >= 2.0 ** -6, 2.0 ** (np.floor(np.log2(np.maximum(scaled, 1e-300))) - 3),
+                    2.0 ** -9)
+    assert (np.abs(q / X[:, :, None] - g / X[:, :, None]) <= step / 2 + 1e-12).all()
