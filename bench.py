@@ -33,7 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOADS = ("llama", "llama_mxfp8", "long_bs16", "long_bs64", "long_bs64_k16", "shared", "churn",
-             "gqa8", "tree")
+             "gqa8", "gqa8_mxfp8", "tree")
 
 
 def parse():
@@ -161,7 +161,7 @@ def make_batch(name, device, seed_offset=0, batch=0):
         return wl.long_batch(device=device, block_size=16, seed=3 + seed_offset, batch=batch or 8)
     if name in ("long_bs64", "long_bs64_k16"):
         return wl.long_batch(device=device, block_size=64, seed=3 + seed_offset, batch=batch or 8)
-    if name == "gqa8":
+    if name in ("gqa8", "gqa8_mxfp8"):
         # the Llama-shaped lengths with eight query heads per kv head (64 / 8)
         rng = np.random.default_rng(2 + seed_offset)
         lens = rng.integers(512, 8192, size=batch or 64, endpoint=True)
@@ -241,7 +241,7 @@ def run_pkv(args, rank, world, local):
     B = b.num_seqs
     shape = (b.num_blocks, b.block_size, b.num_kv_heads, b.head_dim)
     dt = b.k_hist.dtype
-    mx = args.workload == "llama_mxfp8"  # the same layer over MXFP8 pools
+    mx = args.workload.endswith("_mxfp8")  # the same layer over MXFP8 pools
     if mx:
         kc = pkv.MxPool(*shape, device=dev)
         vc = pkv.MxPool(*shape, device=dev)
@@ -385,7 +385,9 @@ def run_pkv(args, rank, world, local):
                          "long_bs64": "long-context decode, block size 64",
                          "long_bs64_k16": "long-context decode, block size 64 read as "
                                           "16-row kernel blocks (tables expanded per step)",
-                         "gqa8": "decode layer with 8 query heads per kv head (64/8)"
+                         "gqa8": "decode layer with 8 query heads per kv head (64/8)",
+                         "gqa8_mxfp8": "decode layer with 8 query heads per kv head (64/8) over "
+                                       "MXFP8 K/V pools",
                          }[args.workload],
             "batch": B, "num_q_heads": b.num_q_heads, "num_kv_heads": b.num_kv_heads,
             "head_dim": b.head_dim, "block_size": b.block_size, "kernel_block_size": kblock,
@@ -401,8 +403,9 @@ def run_pkv(args, rank, world, local):
         "decode_ms": decode_ms,
         "append_ms": append_ms,
         "roofline": {"bound": "hbm",
-                     "kernel": ("decode_tc_kernel" if args.workload == "gqa8"
-                                else "decode_partial_kernel") + " + decode_reduce_kernel",
+                     "kernel": {"gqa8": "decode_tc_kernel",
+                                "gqa8_mxfp8": "decode_tc_mx_kernel"}.get(
+                                    args.workload, "decode_partial_kernel") + " + decode_reduce_kernel",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs (copy)",
                      "traffic": traffic,

@@ -49,8 +49,12 @@
  *     the E4M3 code nearest x / X (ties to even).  The scale plane is
  *     head-major within a block, so an MXFP8 pool cannot be read through
  *     tables expanded to smaller kernel blocks.  Supported by kv_append,
- *     kv_block_copy and the CUDA-core decode (head_dim 64 or 128, Hq / Hkv <=
- *     4); the tensor-core paths (shared prefix, chunk-first) take bf16 only.
+ *     kv_block_copy and the decode: on the CUDA cores for head_dim 64 or 128
+ *     and Hq / Hkv <= 4, on the tensor cores (tiles widened to bf16 in shared
+ *     memory) for head_dim 128 and Hq / Hkv = 8 with block_size 16, 32, 64,
+ *     128 or 256; other group sizes return PKV_ERR_UNSUPPORTED.  The
+ *     shared-prefix kernel and the chunk-first phase take bf16 only (a tree
+ *     over MXFP8 pools runs sequence-first).
  *   - Pointers to the caches, q, k, v and out must be 16-byte aligned.
  */
 #ifndef PKV_H

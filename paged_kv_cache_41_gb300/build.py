@@ -25,6 +25,7 @@ CUDA_SOURCES = [
     "kernels/append_copy.cu",
     "kernels/decode.cu",
     "kernels/decode_tc.cu",
+    "kernels/decode_tc_mx.cu",
     "kernels/prefix_tc.cu",
     "kernels/tree.cu",
 ]
@@ -33,6 +34,7 @@ CUDA_SOURCES = [
 PER_SOURCE_FLAGS = {
     "kernels/decode.cu": ["--use_fast_math"],
     "kernels/decode_tc.cu": ["--use_fast_math"],
+    "kernels/decode_tc_mx.cu": ["--use_fast_math"],
     "kernels/prefix_tc.cu": ["--use_fast_math"],
     "kernels/tree.cu": ["--use_fast_math"],
 }

@@ -135,6 +135,14 @@ cudaError_t launch_decode_reduce(int dtype, int head_dim, const DecodeArgs& args
 // 128-byte-swizzled map over q [B, Hq, D] whose box is 64 columns x 8 heads
 // x 1 request.  Launches the reduction too.
 bool decode_tc_supported(int dtype, int head_dim, int group, int block_size);
+// The tensor-core decode over MXFP8 pools (decode_tc_mx.cu): tmk / tmv are
+// 4-D uint8 maps over the element planes whose box is 128-byte rows x
+// min(P, 128) rows; the scale planes come in args.  Launches the reduction.
+bool decode_tc_mx_supported(int dtype, int head_dim, int group, int block_size);
+int decode_tc_mx_resident_ctas();
+cudaError_t launch_paged_decode_tc_mx(int group, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                                      const CUtensorMap& tmq, const DecodeArgs& args,
+                                      cudaStream_t stream);
 int decode_tc_rows();
 int decode_tc_resident_ctas();
 cudaError_t launch_paged_decode_tc(const CUtensorMap& tmk, const CUtensorMap& tmv,

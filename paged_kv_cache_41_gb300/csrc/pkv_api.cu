@@ -139,7 +139,10 @@ pkv_status check_attention_shape(const pkv_cache_desc* c, int32_t num_q_heads) {
   if (num_q_heads <= 0 || num_q_heads % c->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   const int G = num_q_heads / c->num_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return PKV_ERR_UNSUPPORTED;
-  if (c->dtype == PKV_MXFP8 && G > 4) return PKV_ERR_UNSUPPORTED;  // the CUDA-core decode only
+  // MXFP8 with more than 4 query heads per kv head: the tensor-core decode only
+  if (c->dtype == PKV_MXFP8 && G > 4 &&
+      !pkv::decode_tc_mx_supported(c->dtype, c->head_dim, G, c->block_size))
+    return PKV_ERR_UNSUPPORTED;
   if (c->num_kv_heads > 65535 || c->num_blocks > INT32_MAX) return PKV_ERR_UNSUPPORTED;
   return PKV_OK;
 }
@@ -173,8 +176,14 @@ int sm_count() {
 
 // Whether the decode runs on the tensor cores (eight query heads per kv
 // head) or on the CUDA cores, and the rows of one stage of its work list.
+// Eight query heads per kv head run on the tensor cores (bf16, and MXFP8
+// through the widening kernel); fewer on the CUDA cores, which for MXFP8
+// pools measure faster than widening to bf16 in shared memory (266 vs
+// 377 us for the Llama-shaped layer: the widening, not HBM, bounds the
+// tensor-core kernel).
 bool use_tc_decode(const pkv_cache_desc* c, int group) {
-  return pkv::decode_tc_supported(c->dtype, c->head_dim, group, c->block_size);
+  return pkv::decode_tc_supported(c->dtype, c->head_dim, group, c->block_size) ||
+         pkv::decode_tc_mx_supported(c->dtype, c->head_dim, group, c->block_size);
 }
 
 int decode_stage_rows(const pkv_cache_desc* c, int group) {
@@ -197,8 +206,9 @@ int64_t decode_ctas(const pkv_cache_desc* c, int32_t num_seqs, int32_t num_q_hea
                     int32_t max_blocks, int32_t partition_size) {
   const int G = num_q_heads / c->num_kv_heads;
   const bool tc = use_tc_decode(c, G);
-  int64_t resident = tc ? pkv::decode_tc_resident_ctas()
-                        : pkv::decode_resident_ctas(c->dtype, c->head_dim, G);
+  int64_t resident = !tc ? pkv::decode_resident_ctas(c->dtype, c->head_dim, G)
+                     : c->dtype == PKV_MXFP8 ? pkv::decode_tc_mx_resident_ctas()
+                                             : pkv::decode_tc_resident_ctas();
   if (resident <= 0) resident = (tc ? 1LL : 4LL) * sm_count();
   const int64_t smax = max_decode_stages(c, G, num_seqs, max_blocks);
   int64_t C = resident < smax ? resident : smax;
@@ -246,6 +256,15 @@ pkv_status launch_decode(const pkv_cache_desc* cache, int G, const void* q, cons
     const int rows = cache->block_size < pkv::decode_tc_rows() ? cache->block_size
                                                                : pkv::decode_tc_rows();
     CUtensorMap tmq;
+    if (cache->dtype == PKV_MXFP8) {  // 128-byte E4M3 rows, widened in the kernel
+      if ((st = encode_cache_map(&tmk, cache, k_cache, rows)) != PKV_OK) return st;
+      if ((st = encode_cache_map(&tmv, cache, v_cache, rows)) != PKV_OK) return st;
+      if ((st = encode_q_map_sw128(&tmq, q, q_seqs > 0 ? q_seqs : a.num_seqs, a.num_q_heads,
+                                   cache->head_dim, G, 1)) != PKV_OK)
+        return st;
+      e = pkv::launch_paged_decode_tc_mx(G, tmk, tmv, tmq, a, stream);
+      return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    }
     if ((st = encode_cache_map_sw128(&tmk, cache, k_cache, rows)) != PKV_OK) return st;
     if ((st = encode_cache_map_sw128(&tmv, cache, v_cache, rows)) != PKV_OK) return st;
     if ((st = encode_q_map_sw128(&tmq, q, q_seqs > 0 ? q_seqs : a.num_seqs, a.num_q_heads,

@@ -162,8 +162,46 @@ def test_tree_attention_over_mxfp8_pools():
     pu.assert_close(lse.cpu().numpy(), ref_lse, "tree lse")
 
 
-def test_eight_heads_per_kv_head_is_rejected():
-    b = wl.custom_batch([10], dtype="bf16", hq=16, hkv=2, d=128, p=16, seed=1, device="cuda")
+@pytest.mark.parametrize("p", [16, 128, 256])
+def test_eight_heads_per_kv_head_tensor_cores(p):
+    # G = 8 over MXFP8 runs only on the tensor cores (E4M3 tiles widened to bf16)
+    lens = [1, 127, 128, 129, 300, 0, 1000, 33]
+    b = wl.custom_batch(lens, dtype="bf16", hq=64, hkv=8, d=128, p=p, seed=17 + p, device="cuda")
+    kc, vc, hk, hv = _pools(b)
+    _decode_and_check(b, kc, vc, hk, hv)
+
+
+@pytest.mark.parametrize("rep", range(2))
+def test_tensor_core_one_stage_segments(rep):
+    # every segment one 128-row stage: pieces change every stage, and the
+    # widening runs one stage ahead of the MMAs
+    lens = np.random.default_rng(40 + rep).integers(1, 128, size=300, endpoint=True)
+    b = wl.custom_batch(lens, dtype="bf16", hq=64, hkv=8, d=128, p=16, seed=40 + rep, device="cuda")
+    kc, vc, hk, hv = _pools(b)
+    _decode_and_check(b, kc, vc, hk, hv)
+
+
+def test_tensor_core_extreme_scales():
+    # scales past 2^7 (the widening's second multiply), tiny scales and
+    # all-zero groups on the tensor-core path: V rows times 1e30 and 1e-30,
+    # K rows times 1e5 in one sequence (its softmax turns one-hot) and 1e-30
+    lens = [300, 200, 129]
+    b = wl.custom_batch(lens, dtype="bf16", hq=64, hkv=8, d=128, p=16, seed=23, device="cuda")
+    n = b.v_hist.shape[0]
+    rows = torch.arange(n, device="cuda")
+    b.v_hist[rows % 5 == 1] *= 1e30
+    b.v_hist[rows % 7 == 2] *= 1e-30
+    b.v_hist[rows % 11 == 3, :, 32:64] = 0
+    b.k_hist[rows % 13 == 4] *= 1e-30
+    k0 = rows[int(b.hist_offsets[0]):int(b.hist_offsets[1])]  # sequence 0's rows
+    b.k_hist[k0[k0 % 9 == 5]] *= 1e5
+    kc, vc, hk, hv = _pools(b)
+    assert kc.scales.max().item() > 134 and vc.scales.max().item() > 134
+    _decode_and_check(b, kc, vc, hk, hv)
+
+
+def test_eight_heads_per_kv_head_at_head_dim_64_is_rejected():
+    b = wl.custom_batch([10], dtype="bf16", hq=16, hkv=2, d=64, p=16, seed=1, device="cuda")
     kc = pkv.MxPool(*_shape(b), device="cuda")
     vc = pkv.MxPool(*_shape(b), device="cuda")
     with pytest.raises(pkv.PkvError) as e:
