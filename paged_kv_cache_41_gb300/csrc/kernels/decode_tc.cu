@@ -157,9 +157,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         } while (nt == 0);
       }
     }
+    // block id of this lane's box in the stage at row i * kTcRows of
+    // sequence r (0 where the lane has no box), loaded one stage ahead: the
+    // table read then overlaps the wait for a free slot
+    const int j = lane & 15;
+    auto box_block = [&](int r_, int i_, int len_) -> int {
+      const int row = i_ * kTcRows + (j >> 1) * TB;
+      return row < len_ && (j >> 1) * TB < kTcRows
+                 ? __ldg(a.block_tables + (int64_t)r_ * a.max_blocks + row / P)
+                 : 0;
+    };
+    int blk_next = box_block(r, i, len);
     int pieces = 0;
     for (int k = 0; k < n; ++k) {
       const int s = k % kTcStages;
+      int blk = blk_next;
       if (k >= kTcStages) {
         int ok = 1;
         if (lane == 0 && !mbar_wait(&kvfree[s], ((k / kTcStages) - 1) & 1)) {
@@ -179,14 +191,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         (end && i == nt - 1 && dseg >= 0 ? kWholeSeg : 0) |
                         (dseg > 0 ? kSlotOne : 0) | (qb << 4);
       const int nbox = 2 * ((nvalid + TB - 1) / TB);  // per tensor
-      const int j = lane & 15;
-      int blk = 0, brow = 0;
-      if (j < nbox) {
-        const int row = t0 + (j >> 1) * TB;
-        const int bi = row / P;
-        brow = row - bi * P;
-        blk = __ldg(a.block_tables + (int64_t)r * a.max_blocks + bi);
-      }
+      int brow = (t0 + (j >> 1) * TB) % P;
       const bool bad = j < nbox && (blk < 0 || (int64_t)blk >= a.num_blocks);
       if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.err, PKV_DEVERR_BLOCK);
       if (bad) {
@@ -221,6 +226,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           } while (nt == 0);
         }
       }
+      if (k + 1 < n) blk_next = box_block(r, i, len);
     }
   } else if (warp == 1) {
     // ============================================================ MMA issue
