@@ -362,9 +362,12 @@ def run_pkv(args, rank, world, local):
 
     peak, peak_kind = load_peaks()
     achieved = kv_bytes / (decode_ms * 1e-3) / 1e9
-    traffic = (kernel_traffic("decode.cu", "decode_partial_llama.md") if args.workload == "llama"
-               else kernel_traffic("decode_tc.cu", "decode_tc_gqa8.md")
-               if args.workload == "gqa8" else None)
+    summaries = {"llama": ("decode.cu", "decode_partial_llama.md"),
+                 "llama_mxfp8": ("decode.cu", "decode_partial_mxfp8.md"),
+                 "gqa8": ("decode_tc.cu", "decode_tc_gqa8.md"),
+                 "gqa8_mxfp8": ("decode_tc_mx.cu", "decode_tc_mx_gqa8.md")}
+    traffic = (kernel_traffic(*summaries[args.workload]) if args.workload in summaries and
+               not args.batch else None)
     res = {
         "metric": "paged-decode KV GB/s (% of HBM peak) and decode rows/s at 1 GB300",
         "value": world * kv_bytes / (ms_step * 1e-3) / 1e9,
