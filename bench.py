@@ -33,7 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOADS = ("llama", "llama_mxfp8", "long_bs16", "long_bs64", "long_bs64_k16", "shared", "churn",
-             "gqa8", "gqa8_mxfp8", "tree")
+             "gqa8", "gqa8_mxfp8", "tree", "append", "block_copy")
 
 
 def parse():
@@ -680,6 +680,180 @@ def run_tree(args, rank, world, local):
     return res, tb
 
 
+# ------------------------------------------------------------------ append / block copy
+COPY_PAIRS = 16384  # copy-on-write (src, dst) block pairs per block_copy call
+
+
+def cache_ops_inputs(args, dev, seed_offset):
+    """The Llama-shaped batch's pool and rows; for block_copy also a filled
+    pool and COPY_PAIRS (src, dst) pairs over disjoint blocks."""
+    b = make_batch("llama", dev, seed_offset=seed_offset, batch=args.batch)
+    pairs = None
+    if args.workload == "block_copy":
+        rng = np.random.default_rng(7 + seed_offset)
+        n = min(COPY_PAIRS, b.num_blocks // 2)
+        perm = rng.permutation(b.num_blocks)
+        pairs = np.stack([perm[:n], perm[n:2 * n]], axis=1).astype(np.int64)
+    return b, pairs
+
+
+def run_cache_ops(args, rank, world, local):
+    """kv_append of every history row of the Llama-shaped batch (a prefill's
+    scatter, 294k rows), or kv_block_copy of COPY_PAIRS whole blocks (K and
+    V): byte copies, bound by HBM read + write."""
+    import torch
+    from paged_kv_cache_41_gb300 import pkv
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    pkv.load_library()
+    b, pairs = cache_ops_inputs(args, dev, rank)
+    shape = (b.num_blocks, b.block_size, b.num_kv_heads, b.head_dim)
+    kc = torch.zeros(shape, dtype=b.k_hist.dtype, device=dev)
+    vc = torch.zeros_like(kc)
+    slots = torch.from_numpy(b.slots).to(dev)
+    row = b.num_kv_heads * b.head_dim * b.k_hist.element_size()  # bytes of one K (or V) row
+    stream = torch.cuda.current_stream()
+    append = args.workload == "append"
+    if append:
+        nbytes = 2 * 2 * b.k_hist.shape[0] * row  # K and V, read + written
+
+        def call():
+            pkv.kv_append(kc, vc, b.k_hist, b.v_hist, slots)
+    else:
+        pkv.kv_append(kc, vc, b.k_hist, b.v_hist, slots)
+        d_pairs = torch.from_numpy(pairs).to(dev)
+        nbytes = 2 * 2 * len(pairs) * b.block_size * row
+
+        def call():
+            pkv.kv_block_copy(kc, vc, d_pairs)
+
+    def timed(fn, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for a, e in evs:
+            a.record(stream)
+            fn()
+            e.record(stream)
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(e) for a, e in evs]))
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = ClockSampler(local)
+    clocks.start()
+    n = max(args.steps, 20)
+    ms = all_max(timed(call, n), world)
+    clk = clocks.stop()
+    assert pkv.get_device_error() == 0
+
+    # end to end: the step's inputs from pinned host memory (the rows and
+    # their slots, or the pairs), the call, and a read of the device error
+    # word as the step's result
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    h_err = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    if append:
+        h_k, h_v = b.k_hist.cpu().pin_memory(), b.v_hist.cpu().pin_memory()
+        h_s = slots.cpu().pin_memory()
+        d_k, d_v, d_s = torch.empty_like(b.k_hist), torch.empty_like(b.v_hist), torch.empty_like(slots)
+        h2d = h_k.numel() * h_k.element_size() * 2 + h_s.numel() * 8
+
+        def e2e():
+            d_k.copy_(h_k, non_blocking=True)
+            d_v.copy_(h_v, non_blocking=True)
+            d_s.copy_(h_s, non_blocking=True)
+            pkv.kv_append(kc, vc, d_k, d_v, d_s)
+            h_err.copy_(err, non_blocking=True)
+    else:
+        h_p = torch.from_numpy(pairs).pin_memory()
+        d_p = torch.empty_like(d_pairs)
+        h2d = h_p.numel() * 8
+
+        def e2e():
+            d_p.copy_(h_p, non_blocking=True)
+            pkv.kv_block_copy(kc, vc, d_p)
+            h_err.copy_(err, non_blocking=True)
+
+    for _ in range(3):
+        e2e()
+    e2e_ms = timed(e2e, n)
+    assert pkv.get_device_error() == 0
+
+    hbm, kind = load_peaks()
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    kname = "kv_append_kernel" if append else "kv_block_copy_kernel"
+    summary = "kv_append_prefill.md" if append else "kv_block_copy.md"
+    traffic = kernel_traffic("append_copy.cu", summary) if not args.batch else None
+    res = {
+        "metric": ("kv_append" if append else "kv_block_copy") +
+                  " GB/s (K/V bytes read + written per call / call time)",
+        "value": world * achieved, "unit": "GB/s", "n_gpus": world, "steps": n,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": b.dtype,
+        "data": "synthetic (seeded N(0,1) k/v rows, seeded block placement)",
+        "config": {"workload": ("prefill-scale append: every history row of the "
+                                "llama3-8b-shaped batch" if append else
+                                f"copy-on-write of {len(pairs)} whole blocks (K and V) of the "
+                                "llama3-8b-shaped pool"),
+                   "rows": int(b.k_hist.shape[0]), "num_kv_heads": b.num_kv_heads,
+                   "head_dim": b.head_dim, "block_size": b.block_size,
+                   "pool_blocks": b.num_blocks, "bytes_per_call": nbytes,
+                   "l2": f"inputs larger than L2 ({nbytes / 2e9:.2f} GB read per call)",
+                   "parallelism": f"replicas x{world} (no collective)"},
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": achieved / hbm,
+                     "peak_kind": f"{kind} hbm_gbs (copy: read + write bytes)",
+                     "traffic": traffic, "algorithmic_bytes_per_launch": nbytes},
+        "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},
+        "gpu_launches": n,
+        "clocks": clk,
+    }
+    return res, (b, pairs)
+
+
+def cache_ops_cpu_sample(b, pairs, workload, seconds):
+    """The oracle's kv_append (or kv_block_copy) on samples of the same rows
+    (or pairs) until about `seconds` of CPU work: (bytes, elapsed, sample)."""
+    import oracle
+    from paged_kv_cache_41_gb300 import workloads as wl
+    kh_all, vh_all = wl.to_numpy_storage(b.k_hist.cpu()), wl.to_numpy_storage(b.v_hist.cpu())
+    row = kh_all[0].nbytes
+    done = 0
+    elapsed = 0.0
+    calls = 0
+    if workload == "append":
+        n = min(16384, kh_all.shape[0])
+        kc = np.zeros((n // b.block_size + 1, b.block_size) + kh_all.shape[1:], kh_all.dtype)
+        vc = np.zeros_like(kc)
+        slots = np.random.default_rng(0).permutation(n).astype(np.int64)
+        while elapsed < seconds:
+            lo = (calls * n) % max(1, kh_all.shape[0] - n)
+            k, v = kh_all[lo:lo + n], vh_all[lo:lo + n]
+            t0 = time.perf_counter()
+            oracle.kv_append(kc, vc, k, v, slots)
+            elapsed += time.perf_counter() - t0
+            done += 4 * n * row
+            calls += 1
+        desc = f"{calls} calls of {n} rows into a private pool"
+    else:
+        nb = 2 * min(1024, len(pairs))
+        shape = (nb, b.block_size) + kh_all.shape[1:]
+        kc = np.zeros(shape, kh_all.dtype)
+        kc.reshape(-1)[:] = kh_all.reshape(-1)[:kc.size]
+        vc = kc.copy()
+        pp = np.stack([np.arange(nb // 2), np.arange(nb // 2, nb)], axis=1).astype(np.int64)
+        while elapsed < seconds:
+            t0 = time.perf_counter()
+            oracle.kv_block_copy(kc, vc, pp)
+            elapsed += time.perf_counter() - t0
+            done += 4 * len(pp) * b.block_size * row
+            calls += 1
+        desc = f"{calls} calls of {len(pp)} block pairs in a private pool"
+    return done, elapsed, desc + ", single-threaded C oracle"
+
+
 def tree_cpu_baseline(tb, seconds):
     """The oracle's definition on whole requests of the tree batch."""
     import oracle
@@ -885,6 +1059,12 @@ def main():
         res, tb = run_tree(args, rank, world, local)
         if rank == 0 and not args.no_cpu_baseline and world == 1:
             res["cpu_baseline"] = tree_cpu_baseline(tb, args.cpu_sample_seconds)
+    elif args.workload in ("append", "block_copy"):
+        res, (b, pairs) = run_cache_ops(args, rank, world, local)
+        if rank == 0 and not args.no_cpu_baseline and world == 1:
+            nb_, el, desc = cache_ops_cpu_sample(b, pairs, args.workload, args.cpu_sample_seconds)
+            res["cpu_baseline"] = {"value": nb_ / el / 1e9, "unit": "GB/s", "cores": 1,
+                                   "kind": "oracle", "sample": desc}
     elif args.workload == "churn":
         res, b = run_churn(args, rank, world, local)
         if rank == 0 and not args.no_cpu_baseline and world == 1:
@@ -902,6 +1082,28 @@ def main():
 
 def run_reference(args):
     """The CPU oracle, as it stands, on bounded samples of the same workload."""
+    if args.workload in ("append", "block_copy"):
+        b, pairs = cache_ops_inputs(args, "cpu", 0)
+        per_step = max(1.0, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
+        cache_ops_cpu_sample(b, pairs, args.workload, per_step / 4)
+        nb_ = el = 0.0
+        for _ in range(args.steps):
+            x, y, desc = cache_ops_cpu_sample(b, pairs, args.workload, per_step)
+            nb_ += x
+            el += y
+        v = nb_ / el / 1e9
+        return {"impl": "reference",
+                "metric": ("kv_append" if args.workload == "append" else "kv_block_copy") +
+                          " GB/s (K/V bytes read + written per call / call time)",
+                "value": v, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16 (byte copies)", "data": "synthetic",
+                "config": {"workload": args.workload},
+                "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                 "sample": f"per step: {desc}"},
+                "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
     b = make_batch(args.workload, "cpu", batch=args.batch)
     nthreads = len(os.sched_getaffinity(0))
     per_step = max(1.0, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
