@@ -256,11 +256,12 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---------------------------------------------------------------- plan
-  pdl_wait();                // inputs written by earlier kernels are visible
+  if (!a.plan_before_wait) pdl_wait();  // inputs written by earlier kernels are visible
   pdl_launch_dependents();   // the reduction may be scheduled as CTAs retire
   int4 d0;
   const int n = plan_cta_stages<kDecodeThreads, kStageRows>(
       a, reinterpret_cast<long long*>(scratch), &d0);
+  if (a.plan_before_wait) pdl_wait();
   if (n <= 0) return;  // no stages: the whole CTA leaves before any barrier
   const int hw = lane >> 4, l16 = lane & 15;
   float2 q2[G][EP2];

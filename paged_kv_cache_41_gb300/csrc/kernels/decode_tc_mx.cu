@@ -135,10 +135,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   __shared__ uint32_t tmem_base;
 
   const int c = blockIdx.x;
-  pdl_wait();               // inputs written by earlier kernels are visible
+  if (!a.plan_before_wait) pdl_wait();  // inputs written by earlier kernels are visible
   pdl_launch_dependents();  // the reduction may be scheduled as CTAs retire
   int4 d0;
   const int n = plan_cta_stages<kMxThreads, kMxRows>(a, wsum, &d0);
+  if (a.plan_before_wait) pdl_wait();
   if (n <= 0) return;  // no stages: the whole CTA leaves before any barrier
   const int Hkv = a.num_kv_heads, P = a.block_size;
   const int TB = P < kMxRows ? P : kMxRows;  // rows per TMA box

@@ -680,6 +680,7 @@ pkv_status pkv_shared_prefix_attention(
   a.num_ctas = (int32_t)w.ctas;
   a.num_stages = pkv::decode_num_stages(cache->head_dim, elem_bytes(cache->dtype));
   a.qscale = qscale;
+  a.plan_before_wait = w.prefix_parts > 0;  // right after the prefix kernel
   return launch_decode(cache, G, q, k_cache, v_cache, a, s);
 }
 
@@ -1148,6 +1149,7 @@ pkv_status pkv_chunk_tree_attention(const pkv_cache_desc* cache, void* out, floa
     a.num_ctas = (int32_t)h.decode_ctas;
     a.num_stages = pkv::decode_num_stages(cache->head_dim, elem_bytes(cache->dtype));
     a.qscale = qscale;
+    a.plan_before_wait = h.n_items > 0;  // right after the chunk-first prefix kernel
     if ((st = launch_decode(cache, G, q, k_cache, v_cache, a, s, num_seqs)) != PKV_OK) return st;
   }
   pkv::TreeMergeArgs m{};
