@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--batch", type=int, default=0,
                     help="override the batch size (small cases for profiling)")
+    ap.add_argument("--prefix-len", type=int, default=0,
+                    help="shared workload: prefix tokens (default 2048)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -433,7 +435,8 @@ def run_shared(args, rank, world, local):
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     pkv.load_library()
-    sp = wl.shared_prefix_batch(device=dev, seed=5 + rank, batch=args.batch or 128)
+    sp = wl.shared_prefix_batch(device=dev, seed=5 + rank, batch=args.batch or 128,
+                                **({"prefix_len": args.prefix_len} if args.prefix_len else {}))
     shape = (sp.num_blocks, sp.block_size, sp.num_kv_heads, sp.head_dim)
     kc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
     vc = torch.zeros_like(kc)
