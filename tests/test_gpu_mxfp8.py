@@ -162,7 +162,7 @@ def test_tree_attention_over_mxfp8_pools():
     pu.assert_close(lse.cpu().numpy(), ref_lse, "tree lse")
 
 
-@pytest.mark.parametrize("p", [16, 128, 256])
+@pytest.mark.parametrize("p", [16, 32, 64, 128, 256])
 def test_eight_heads_per_kv_head_tensor_cores(p):
     # G = 8 over MXFP8 runs only on the tensor cores (E4M3 tiles widened to bf16)
     lens = [1, 127, 128, 129, 300, 0, 1000, 33]
@@ -179,6 +179,44 @@ def test_tensor_core_one_stage_segments(rep):
     b = wl.custom_batch(lens, dtype="bf16", hq=64, hkv=8, d=128, p=16, seed=40 + rep, device="cuda")
     kc, vc, hk, hv = _pools(b)
     _decode_and_check(b, kc, vc, hk, hv)
+
+
+@pytest.mark.parametrize("partition_size", [128, 512])
+def test_tensor_core_split_k(partition_size):
+    # pieces cut at CTA boundaries every few stages: records and the reduction
+    rng = np.random.default_rng(partition_size + 1)
+    lens = rng.integers(1, 3000, size=24)
+    b = wl.custom_batch(lens, dtype="bf16", hq=64, hkv=8, d=128, p=16, seed=9, device="cuda")
+    kc, vc, hk, hv = _pools(b)
+    _decode_and_check(b, kc, vc, hk, hv, partition_size=partition_size)
+
+
+def test_tree_with_eight_heads_over_mxfp8_pools():
+    # sequence-first through the tensor-core MXFP8 decode: q_rows indirection
+    # and states-only output
+    tree = [(300, 0, 6), (70, 0, 3), (45, 3, 6)] + [(r * 9 + 1, r, r + 1) for r in range(6)]
+    tb = wl.prefix_tree_batch(tree, device="cuda", seed=14, hq=64, hkv=8, d=128)
+    shape = (tb.num_blocks, tb.block_size, tb.num_kv_heads, tb.head_dim)
+    kc = pkv.MxPool(*shape, device="cuda", fill=0xFF)
+    vc = pkv.MxPool(*shape, device="cuda", fill=0xFF)
+    pkv.kv_append(kc, vc, tb.k_rows, tb.v_rows, torch.from_numpy(tb.slots).cuda())
+    hk = np.full(oracle.mxfp8_pool_bytes(*shape), 0xFF, np.uint8)
+    hv = hk.copy()
+    slots = np.concatenate([
+        np.array([oracle.slot_for_position(tb.block_ids[f:], tb.block_size, t) for t in range(int(n))],
+                 np.int64) for f, n, _, _ in tb.chunks])
+    assert oracle.kv_append_mxfp8(hk, hv, shape, wl.to_numpy_storage(tb.k_rows),
+                                  wl.to_numpy_storage(tb.v_rows), slots) == oracle.OK
+    plan = pkv.chunk_tree_plan(kc, tb.chunks, tb.block_ids, tb.num_seqs, tb.num_q_heads, 0)
+    lse = torch.empty(tb.num_seqs, tb.num_q_heads, dtype=torch.float32, device="cuda")
+    out = pkv.chunk_tree_attention(tb.q, kc, vc, plan, tb.scale, lse=lse)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
+    ref, ref_lse = oracle.chunk_tree(wl.to_numpy_storage(tb.q.float()), oracle.mxfp8_to_f32(hk, shape),
+                                     oracle.mxfp8_to_f32(hv, shape), tb.chunks, tb.block_ids,
+                                     tb.scale)
+    pu.assert_close(out.float().cpu().numpy(), ref, "tree out")
+    pu.assert_close(lse.cpu().numpy(), ref_lse, "tree lse")
 
 
 def test_tensor_core_extreme_scales():
