@@ -844,7 +844,7 @@ def cache_ops_cpu_sample(b, pairs, workload, seconds):
         nb = 2 * min(1024, len(pairs))
         shape = (nb, b.block_size) + kh_all.shape[1:]
         kc = np.zeros(shape, kh_all.dtype)
-        kc.reshape(-1)[:] = kh_all.reshape(-1)[:kc.size]
+        kc.reshape(-1)[:] = np.resize(kh_all.reshape(-1), kc.size)  # rows repeated as needed
         vc = kc.copy()
         pp = np.stack([np.arange(nb // 2), np.arange(nb // 2, nb)], axis=1).astype(np.int64)
         while elapsed < seconds:
