@@ -85,6 +85,30 @@ struct DecodeSmem {
   size_t tiles_bytes, scale_off, bar_off, ok_off, desc_off, ring_off, scratch_off, total;
 };
 
+// Cross-lane sum scratch of one consumer warp, in floats: row i of half-warp
+// hw (the 16 lanes' partial sums of value i) starts at red_row<G, kMx>(hw, i).
+// Rows are placed so that neither the 32-lane store of a value nor an 8-lane
+// phase of the 16-byte reads meets a bank conflict: for G = 4 each phase
+// reads four rows whose bank offsets are {0, 4, 16, 20} (half-warp 1 at +16),
+// packed into 260 floats; G = 8 takes rows 20 floats apart; G = 1, 2 only
+// offset half-warp 1 by 16 banks.  MXFP8 with G = 4 keeps the plain
+// 256-float layout (two-way conflicts): the four extra floats per warp would
+// cost its six-stage ring a CTA per SM.
+__host__ __device__ constexpr int red_warp_floats(int g, int elem_bytes) {
+  return g == 4 ? (elem_bytes == 1 ? 256 : 260) : g == 8 ? 672 : 2 * (32 * g + 16);
+}
+template <int G, bool kMx>
+__device__ __forceinline__ int red_row(int hw, int i) {
+  if constexpr (G == 4 && kMx)
+    return hw * 128 + i * 16;
+  else if constexpr (G == 4)
+    return ((i & 1) ? 132 : 0) + 16 * (2 * (i >> 2) + (hw ? 5 - ((i >> 1) & 1) : ((i >> 1) & 1)));
+  else if constexpr (G == 8)
+    return hw * 336 + i * 20;
+  else
+    return hw * (32 * G + 16) + i * 16;
+}
+
 // Stage s holds its K tile then its V tile; both together also hold the
 // [4][G][D] fp32 merge of a piece's end (16 G D bytes <= 2 * 32 * D * b for
 // G <= 8 with 2- and 4-byte elements, G <= 4 with 1-byte ones).
@@ -102,9 +126,9 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int head_dim, int elem_
   s.desc_off = (s.ok_off + (size_t)stages * 4 + 15) & ~(size_t)15;
   s.ring_off = s.desc_off + (size_t)stages * 16;
   s.scratch_off = s.ring_off + (size_t)2 * 64 * 16;  // two 64-entry stage descriptor rings
-  // scratch: the half-warps' cross-lane sums [4][2][2G][16], then the merge's
-  // per-warp maxima and sums [2][4][G]
-  s.total = s.scratch_off + (size_t)kConsumerWarps * 2 * (2 * group * 16) * 4 +
+  // scratch: the warps' cross-lane sums (red_warp_floats each), then the
+  // merge's per-warp maxima and sums [2][4][G]
+  s.total = s.scratch_off + (size_t)kConsumerWarps * red_warp_floats(group, elem_bytes) * 4 +
             (size_t)2 * kConsumerWarps * group * 4 + 128;  // +128: base alignment
   return s;
 }
@@ -121,9 +145,10 @@ int decode_num_stages(int head_dim, int elem_bytes) {
 // of this half-warp.  kTail = false is the full-stage fast path (every row
 // valid, no masking); kTail = true masks rows >= nvalid.
 //
-// Cross-lane sums go through `red`, this half-warp's [2G][16] scratch: lane
-// l16 stores its partial dot product of value i = (row tk, head g) = tk*G + g
-// at red[i][l16]; then each value is summed by 8/G lanes that read 2G
+// Cross-lane sums go through `red`, this warp's scratch: lane l16 of
+// half-warp hw stores its partial dot product of value i = (row tk, head g) =
+// tk*G + g at red[red_row(hw, i) + l16]; then each value is summed by 8/G
+// lanes that read 2G
 // consecutive partials each and combine with 8/G - 1 shuffles.  Lane l16 ends
 // up holding value j = l16 / (8/G): row tk = l16 >> 3, head g = j % G.
 template <typename T, int D, int G, bool kTail>
@@ -132,7 +157,7 @@ __device__ __forceinline__ void decode_chunk(const T* __restrict__ kt, const T* 
                                              const uint8_t* __restrict__ vsc, int row0,
                                              int nvalid, const float2 (&q2)[G][D / 32],
                                              float2 (&acc)[G][D / 32], float& m_used,
-                                             float& l_run, float* __restrict__ red, int l16) {
+                                             float& l_run, float* __restrict__ red, int hw, int l16) {
   constexpr int EPL = D / 16;
   constexpr int EP2 = EPL / 2;
   constexpr int NV = 2 * G;    // values per half-warp and chunk
@@ -165,11 +190,11 @@ __device__ __forceinline__ void decode_chunk(const T* __restrict__ kt, const T* 
   }
   // ---- sum each value over the 16 lanes of the half-warp
 #pragma unroll
-  for (int i = 0; i < NV; ++i) red[i * 16 + l16] = v[i];
+  for (int i = 0; i < NV; ++i) red[red_row<G, kIsMx<T>>(hw, i) + l16] = v[i];
   __syncwarp();
   const int j = l16 / LPV, sub = l16 % LPV;
   float part[NV];
-  VecLoad<float, NV>::run(red + j * 16 + sub * NV, part);
+  VecLoad<float, NV>::run(red + red_row<G, kIsMx<T>>(hw, j) + sub * NV, part);
   __syncwarp();  // the next chunk rewrites red
   float s2 = part[0];
 #pragma unroll
@@ -388,7 +413,14 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
         }
       }
     }
-    if ((k & 31) == 0 && k + 32 < n) compute_batch(k + 32);
+    // The next batch (stages kb + 32 ..) overwrites the ring entries of
+    // stages kb - 32 .. kb - 1, which a consumer still reads at a piece end
+    // (the next stage's q) until it has released stage kb - 1.  So it is
+    // worked out with the refill of stage kb + NS - 1, which warp 0 issues
+    // only after every warp released stage kb - 1, and still before stage
+    // kb + 32 (NS <= 8) is issued.
+    const int kb = k - (NS - 1);
+    if (kb >= 0 && (kb & 31) == 0 && kb + 32 < n) compute_batch(kb + 32);
   };
   if (warp == 0) {
     if (lane == 0) {
@@ -411,7 +443,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
   if (!d0_exact) load_q(dB[0].x, dB[0].y);
   // (m_used, l_run): softmax state of head (l16 / (8 / G)) % G of this lane.
   float m_used = -INFINITY, l_run = 0.f;
-  float* red = scratch + (warp * 2 + hw) * (2 * G * 16);
+  float* red = scratch + warp * red_warp_floats(G, (int)sizeof(T));
   const int rbase = warp * 4 + hw * 2;
   int s = 0, round = 0;
   uint32_t mrg_phase = 0;
@@ -448,11 +480,11 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
 #pragma unroll 1
         for (int cc = 0; cc < kStageRows / kChunk; ++cc)
           decode_chunk<T, D, G, false>(kt, vt, ksc, vsc, cc * kChunk + rbase, kStageRows, q2, acc, m_used,
-                                       l_run, red, l16);
+                                       l_run, red, hw, l16);
       } else {
         for (int cc = 0; cc * kChunk < nvalid; ++cc)
           decode_chunk<T, D, G, true>(kt, vt, ksc, vsc, cc * kChunk + rbase, nvalid, q2, acc, m_used, l_run,
-                                      red, l16);
+                                      red, hw, l16);
       }
     }
     if (flags & kPieceEnd) {
@@ -466,7 +498,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
       // ---- merge the four warps through this stage's tile, then write
       if (!merge_sync()) break;  // every warp is done with the tile
       float* macc = reinterpret_cast<float*>(const_cast<T*>(kt));  // [4][G][D]
-      float* mm = scratch + kConsumerWarps * 2 * (2 * G * 16);        // [4][G], after the sums
+      float* mm = scratch + kConsumerWarps * red_warp_floats(G, (int)sizeof(T));  // [4][G]
       float* ml = mm + kConsumerWarps * G;                          // [4][G]
 #pragma unroll
       for (int g = 0; g < G; ++g)

@@ -219,6 +219,18 @@ def test_tree_with_eight_heads_over_mxfp8_pools():
     pu.assert_close(lse.cpu().numpy(), ref_lse, "tree lse")
 
 
+@pytest.mark.parametrize("d", [128, 64])
+def test_short_segments_past_the_descriptor_batches(d):
+    # more than 64 stages per CTA and a piece end at nearly every stage: the
+    # consumers read the next stage's descriptor (its q) at each piece end
+    # while warp 0 refills the 64-entry descriptor ring with later batches;
+    # every output is checked
+    lens = np.random.default_rng(d + 5).integers(1, 190, size=2000, endpoint=True)
+    b = wl.custom_batch(lens, dtype="bf16", hq=32, hkv=8, d=d, p=16, seed=d + 6, device="cuda")
+    kc, vc, hk, hv = _pools(b)
+    _decode_and_check(b, kc, vc, hk, hv)
+
+
 def test_tensor_core_extreme_scales():
     # scales past 2^7 (the widening's second multiply), tiny scales and
     # all-zero groups on the tensor-core path: V rows times 1e30 and 1e-30,

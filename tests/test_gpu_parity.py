@@ -103,6 +103,17 @@ def test_batch_past_one_scan_pass(hq, hkv, batch):
     _run_batch(b, check_pool=False)
 
 
+@pytest.mark.parametrize("d,p", [(64, 16), (128, 32)])
+def test_short_segments_past_the_descriptor_batches(d, p):
+    # more than 64 stages per CTA and a piece end at nearly every stage: the
+    # consumers read the next stage's descriptor (its q) at each piece end
+    # while warp 0 refills the 64-entry descriptor ring with later batches
+    # (head_dim 64: a six-stage ring); every output is checked
+    lens = np.random.default_rng(d + p).integers(1, 190, size=2000, endpoint=True)
+    b = wl.custom_batch(lens, dtype="bf16", hq=32, hkv=8, d=d, p=p, seed=d + p, device="cuda")
+    _run_batch(b, check_pool=False)
+
+
 def test_gqa8_tensor_core_decode_long_sampled():
     lens = np.array([40000, 3000, 65536, 1], np.int32)
     b = wl.custom_batch(lens, dtype="bf16", hq=32, hkv=4, d=128, p=16, seed=62, device="cuda")
