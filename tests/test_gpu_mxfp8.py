@@ -231,6 +231,15 @@ def test_short_segments_past_the_descriptor_batches(d):
     _decode_and_check(b, kc, vc, hk, hv)
 
 
+def test_tensor_core_many_short_pieces():
+    # as the bf16 test: about 150 one- or two-stage pieces per CTA through
+    # the widening kernel's raw slots, bf16 buffers and descriptor ring
+    lens = np.random.default_rng(78).integers(1, 190, size=2000, endpoint=True)
+    b = wl.custom_batch(lens, dtype="bf16", hq=64, hkv=8, d=128, p=16, seed=78, device="cuda")
+    kc, vc, hk, hv = _pools(b)
+    _decode_and_check(b, kc, vc, hk, hv)
+
+
 def test_tensor_core_extreme_scales():
     # scales past 2^7 (the widening's second multiply), tiny scales and
     # all-zero groups on the tensor-core path: V rows times 1e30 and 1e-30,

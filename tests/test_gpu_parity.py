@@ -114,6 +114,15 @@ def test_short_segments_past_the_descriptor_batches(d, p):
     _run_batch(b, check_pool=False)
 
 
+def test_tensor_core_many_short_pieces():
+    # eight heads per kv head over 2,000 short segments: about 150 one- or
+    # two-stage pieces per CTA, so every Q buffer, descriptor slot and record
+    # slot is reused many times; every output is checked
+    lens = np.random.default_rng(77).integers(1, 190, size=2000, endpoint=True)
+    b = wl.custom_batch(lens, dtype="bf16", hq=64, hkv=8, d=128, p=16, seed=77, device="cuda")
+    _run_batch(b, check_pool=False)
+
+
 def test_gqa8_tensor_core_decode_long_sampled():
     lens = np.array([40000, 3000, 65536, 1], np.int32)
     b = wl.custom_batch(lens, dtype="bf16", hq=32, hkv=4, d=128, p=16, seed=62, device="cuda")
