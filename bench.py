@@ -184,9 +184,11 @@ def kv_row_bytes(b):
 
 
 # ------------------------------------------------------------------ CPU oracle timing
-def oracle_sample(b, seconds, nthreads):
+def oracle_sample(b, seconds, nthreads, mx=False):
     """Time the CPU oracle decoding whole sequences of the batch until about
-    `seconds` of CPU work; returns (kv_bytes, rows, elapsed, sample description)."""
+    `seconds` of CPU work; returns (kv_bytes, rows, elapsed, sample description).
+    mx: the sequences are quantized into MXFP8 pools and the oracle decodes
+    their exact values (the time includes reading them out of the pool)."""
     import oracle
     from paged_kv_cache_41_gb300 import workloads as wl
     order = np.random.default_rng(0).permutation(b.num_seqs)
@@ -204,29 +206,38 @@ def oracle_sample(b, seconds, nthreads):
         table = np.arange(nblk, dtype=np.int32)
         kh = wl.to_numpy_storage(kh_all[lo:hi])
         vh = wl.to_numpy_storage(vh_all[lo:hi])
-        kc = np.zeros((nblk,) + shape_blk, dtype=kh.dtype)
-        vc = np.zeros_like(kc)
         slots = np.array([oracle.slot_for_position(table, b.block_size, i) for i in range(t)],
                          np.int64)
-        oracle.kv_append(kc, vc, kh, vh, slots)
         q = np.ascontiguousarray(q_all[r:r + 1])
-        t0 = time.perf_counter()
+        if mx:
+            shape = (nblk,) + shape_blk
+            kq = np.zeros(oracle.mxfp8_pool_bytes(*shape), np.uint8)
+            vq = kq.copy()
+            oracle.kv_append_mxfp8(kq, vq, shape, kh, vh, slots)
+            q = np.ascontiguousarray(wl.to_numpy_storage(b.q[r:r + 1].float()))
+            t0 = time.perf_counter()
+            kc, vc = oracle.mxfp8_to_f32(kq, shape), oracle.mxfp8_to_f32(vq, shape)
+        else:
+            kc = np.zeros((nblk,) + shape_blk, dtype=kh.dtype)
+            vc = np.zeros_like(kc)
+            oracle.kv_append(kc, vc, kh, vh, slots)
+            t0 = time.perf_counter()
         oracle.paged_decode(q, kc, vc, table.reshape(1, -1), np.array([t], np.int32), b.scale,
                             nthreads=nthreads)
         elapsed += time.perf_counter() - t0
-        done_bytes += t * kv_row_bytes(b)
+        done_bytes += t * (2 * b.num_kv_heads * b.head_dim * 33 // 32 if mx else kv_row_bytes(b))
         done_rows += 1
         used.append(int(r))
         if elapsed >= seconds:
             break
-    desc = (f"{done_rows} of {b.num_seqs} sequences ({done_bytes / 1e6:.1f} MB of K/V), "
-            f"all {b.num_q_heads} heads, fp64 oracle")
+    desc = (f"{done_rows} of {b.num_seqs} sequences ({done_bytes / 1e6:.1f} MB of "
+            f"{'MXFP8 ' if mx else ''}K/V), all {b.num_q_heads} heads, fp64 oracle")
     return done_bytes, done_rows, elapsed, desc
 
 
-def cpu_baseline(b, seconds):
+def cpu_baseline(b, seconds, mx=False):
     nthreads = len(os.sched_getaffinity(0))
-    nbytes, rows, el, desc = oracle_sample(b, seconds, nthreads)
+    nbytes, rows, el, desc = oracle_sample(b, seconds, nthreads, mx)
     return {"value": nbytes / el / 1e9, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
             "sample": desc, "rows_per_s": rows / el}
 
@@ -883,7 +894,7 @@ def tree_cpu_baseline(tb, seconds):
         nbytes += sum(int(n) for _, n, _, _ in mine) * row
         done += 1
     return {"value": nbytes / el / 1e9, "unit": "GB/s (logical K/V)", "cores": nthreads,
-            "kind": "oracle",
+            "kind": "oracle", "seconds": el,
             "sample": f"{done} of {tb.num_seqs} requests, all heads, whole path, fp64 oracle"}
 
 
@@ -1038,7 +1049,7 @@ def shared_cpu_baseline(sp, seconds):
         flops += 4.0 * sp.num_q_heads * sp.prefix_len * sp.head_dim
         done += 1
     return {"value": flops / el / 1e12, "unit": "TFLOP/s (prefix part)", "cores": nthreads,
-            "kind": "oracle",
+            "kind": "oracle", "seconds": el,
             "sample": f"{done} of {sp.num_seqs} requests, all heads, prefix + suffix, fp64 oracle"}
 
 
@@ -1075,7 +1086,8 @@ def main():
     else:
         res, b = run_pkv(args, rank, world, local)
         if rank == 0 and not args.no_cpu_baseline and world == 1:
-            res["cpu_baseline"] = cpu_baseline(b, args.cpu_sample_seconds)
+            res["cpu_baseline"] = cpu_baseline(b, args.cpu_sample_seconds,
+                                               args.workload.endswith("_mxfp8"))
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
@@ -1107,15 +1119,37 @@ def run_reference(args):
                                  "sample": f"per step: {desc}"},
                 "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
-    b = make_batch(args.workload, "cpu", batch=args.batch)
-    nthreads = len(os.sched_getaffinity(0))
     per_step = max(1.0, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
+    if args.workload in ("shared", "tree"):
+        # the oracle's whole-request definition, as the GPU arm's cpu_baseline
+        from paged_kv_cache_41_gb300 import workloads as wl
+        if args.workload == "shared":
+            sp = wl.shared_prefix_batch(device="cpu", seed=5, batch=args.batch or 128,
+                                        **({"prefix_len": args.prefix_len} if args.prefix_len else {}))
+            cb = shared_cpu_baseline(sp, per_step * args.steps)
+            metric, unit = ("shared-prefix TFLOP/s (prefix contraction on tensor cores, % of "
+                            "dense bf16 peak)"), "TFLOP/s"
+        else:
+            cb = tree_cpu_baseline(tree_batch("cpu", 6, args.batch or 128), per_step * args.steps)
+            metric, unit = ("prefix-tree attention: logical KV GB/s (K/V bytes per-request "
+                            "decode would read / call time)"), "GB/s"
+        v = cb["value"]
+        return {"impl": "reference", "metric": metric, "value": v, "unit": unit, "n_gpus": 1,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * cb["seconds"] / max(1, args.steps),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic", "config": {"workload": args.workload},
+                "cpu_baseline": cb,
+                "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    b = make_batch(args.workload, "cpu", batch=args.batch)
+    mx = args.workload.endswith("_mxfp8")
+    nthreads = len(os.sched_getaffinity(0))
     for _ in range(args.warmup):
-        oracle_sample(b, per_step / 4, nthreads)
+        oracle_sample(b, per_step / 4, nthreads, mx)
     tot_b = tot_r = tot_t = 0.0
     desc = ""
     for _ in range(args.steps):
-        nb_, nr_, el, desc = oracle_sample(b, per_step, nthreads)
+        nb_, nr_, el, desc = oracle_sample(b, per_step, nthreads, mx)
         tot_b += nb_
         tot_r += nr_
         tot_t += el
