@@ -259,6 +259,27 @@ def test_tensor_core_extreme_scales():
     _decode_and_check(b, kc, vc, hk, hv)
 
 
+@pytest.mark.parametrize("hq", [8, 16])  # 16 / 2: eight heads per kv head, the tensor cores
+def test_bad_block_and_length_set_errors(hq):
+    # a block id past the pool: its rows are skipped (CUDA cores) or read as
+    # zero-filled boxes (tensor cores) and the error bit is set; a length past
+    # the table sets its own bit
+    b = wl.custom_batch([200, 20], dtype="bf16", hq=hq, hkv=2, d=128, p=16, seed=63, device="cuda")
+    kc, vc, _, _ = _pools(b)
+    bt = torch.from_numpy(b.block_tables).cuda()
+    sl = torch.from_numpy(b.seq_lens).cuda()
+    bad = bt.clone()
+    bad[0, 1] = b.num_blocks + 3
+    pkv.paged_attention_decode(b.q, kc, vc, bad, sl, b.scale)
+    assert pkv.get_device_error() & pkv.DEVERR_BLOCK
+    pkv.paged_attention_decode(b.q, kc, vc, bt, torch.tensor([200, 10_000], dtype=torch.int32,
+                                                             device="cuda"), b.scale)
+    assert pkv.get_device_error() & pkv.DEVERR_LENGTH
+    pkv.kv_block_copy(kc, vc, torch.tensor([[0, -5]], dtype=torch.int64, device="cuda"))
+    assert pkv.get_device_error() == pkv.DEVERR_BLOCK
+    assert pkv.get_device_error() == 0  # read and cleared
+
+
 def test_eight_heads_per_kv_head_at_head_dim_64_is_rejected():
     b = wl.custom_batch([10], dtype="bf16", hq=16, hkv=2, d=64, p=16, seed=1, device="cuda")
     kc = pkv.MxPool(*_shape(b), device="cuda")
