@@ -110,8 +110,6 @@ CUresult encode_tiled_cached(CUtensorMap* map, CUtensorMapDataType dtype, cuuint
 
 // Bytes of one element of the cache's element plane.
 int elem_bytes(int dtype) { return dtype == PKV_MXFP8 ? 1 : dtype == PKV_BF16 ? 2 : 4; }
-// Bytes of q, k, v and out: bf16 beside an MXFP8 pool.
-int io_bytes(int dtype) { return dtype == PKV_F32 ? 4 : 2; }
 // Byte offset of an MXFP8 pool's scale plane (the element plane's size).
 int64_t mx_plane_bytes(const pkv_cache_desc* c) {
   return c->num_blocks * c->block_size * c->num_kv_heads * c->head_dim;
