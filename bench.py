@@ -235,11 +235,31 @@ def oracle_sample(b, seconds, nthreads, mx=False):
     return done_bytes, done_rows, elapsed, desc
 
 
+def cpu_model():
+    """The host CPU's model name, as /proc/cpuinfo gives it (or its part
+    number on Arm), for the baseline's record."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+    except OSError:
+        return None
+    for key in ("model name", "CPU part"):
+        m = re.search(rf"^{key}\s*:\s*(.+)$", info, re.M)
+        if m:
+            return m.group(1).strip() if key == "model name" else f"Arm CPU part {m.group(1).strip()}"
+    return None
+
+
 def cpu_baseline(b, seconds, mx=False):
+    """The oracle on all host cores of the affinity mask, then on one core
+    (a shorter sample)."""
     nthreads = len(os.sched_getaffinity(0))
     nbytes, rows, el, desc = oracle_sample(b, seconds, nthreads, mx)
+    nb1, rows1, el1, desc1 = oracle_sample(b, max(2.0, seconds / 4), 1, mx)
     return {"value": nbytes / el / 1e9, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
-            "sample": desc, "rows_per_s": rows / el}
+            "sample": desc, "rows_per_s": rows / el,
+            "single_thread": {"value": nb1 / el1 / 1e9, "unit": "GB/s", "sample": desc1},
+            "cpu_model": cpu_model()}
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -413,6 +433,8 @@ def run_pkv(args, rank, world, local):
     achieved = kv_bytes / (decode_ms * 1e-3) / 1e9
     summaries = {"llama": ("decode.cu", "decode_partial_llama.md"),
                  "llama_mxfp8": ("decode.cu", "decode_partial_mxfp8.md"),
+                 "long_bs16": ("decode.cu", "decode_partial_long_bs16.md"),
+                 "long_bs64": ("decode.cu", "decode_partial_long_bs64.md"),
                  "gqa8": ("decode_tc.cu", "decode_tc_gqa8.md"),
                  "gqa8_mxfp8": ("decode_tc_mx.cu", "decode_tc_mx_gqa8.md")}
     traffic = (kernel_traffic(*summaries[args.workload]) if args.workload in summaries and
