@@ -185,11 +185,12 @@ int32_t pkv_decode_num_ctas(const pkv_cache_desc* cache, int32_t num_seqs,
  *                  bytes, 256-byte aligned.  Nothing in it needs to be
  *                  initialised.
  * Supported: block_size 16 or a multiple of 32 up to 256; head_dim 64 or 128;
- * Hq / Hkv in {1, 2, 4, 8}; num_seqs <= 65535.  Eight query heads per kv
- * head with bf16, head_dim 128 and a block size dividing 128 (or a multiple
- * of it) run q.k and P.V on the tcgen05 tensor cores (128-row stages);
- * everything else on the CUDA cores.  Same results within the attention
- * tolerance either way. */
+ * Hq / Hkv in {1, 2, 4, 8} (MXFP8 pools: see the top of this file);
+ * num_seqs <= 65535.  Eight query heads per kv head with head_dim 128 and a
+ * block size dividing 128 (or a multiple of it) run q.k and P.V on the
+ * tcgen05 tensor cores (128-row stages; an MXFP8 pool's tiles are widened
+ * to bf16 in shared memory first); everything else on the CUDA cores.  Same
+ * results within the attention tolerance either way. */
 pkv_status pkv_paged_attention_decode(
     const pkv_cache_desc* cache, void* out, float* lse, const void* q,
     const void* k_cache, const void* v_cache, const int32_t* block_tables,
