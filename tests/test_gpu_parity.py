@@ -57,6 +57,9 @@ EDGE_LENS = [1, 15, 16, 17, 31, 32, 33, 100, 257, 0, 1000, 64, 2]
     ("f32", 64, 4, 2, 16), ("bf16", 128, 32, 8, 64), ("bf16", 128, 32, 8, 32),
     ("bf16", 128, 32, 8, 128), ("bf16", 64, 16, 4, 256), ("f32", 128, 16, 2, 192),
     ("bf16", 128, 16, 4, 96),
+    # eight query heads per kv head on the CUDA cores: fp32 pools, and bf16
+    # at head_dim 64 (the tensor cores take bf16 at 128 only)
+    ("f32", 128, 16, 2, 16), ("bf16", 64, 16, 2, 16), ("f32", 64, 16, 2, 32),
 ])
 @pytest.mark.parametrize("partition_size", [0, "one_block", "three_blocks", "whole"])
 def test_edge_lengths(dtype, d, hq, hkv, p, partition_size):
@@ -111,6 +114,14 @@ def test_short_segments_past_the_descriptor_batches(d, p):
     # (head_dim 64: a six-stage ring); every output is checked
     lens = np.random.default_rng(d + p).integers(1, 190, size=2000, endpoint=True)
     b = wl.custom_batch(lens, dtype="bf16", hq=32, hkv=8, d=d, p=p, seed=d + p, device="cuda")
+    _run_batch(b, check_pool=False)
+
+
+def test_eight_heads_cuda_cores_short_segments_past_the_descriptor_batches():
+    # fp32 pools at eight heads per kv head (two CTAs per SM) with more than
+    # 64 stages per CTA and a piece end at nearly every stage
+    lens = np.random.default_rng(91).integers(1, 190, size=1200, endpoint=True)
+    b = wl.custom_batch(lens, dtype="f32", hq=64, hkv=8, d=64, p=16, seed=91, device="cuda")
     _run_batch(b, check_pool=False)
 
 
