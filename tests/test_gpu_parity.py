@@ -382,20 +382,30 @@ def _churn(tr, hq, hkv, d, check_pools):
 
 
 # ------------------------------------------------------------------ shared prefix
-def _shared_prefix_run(sp, rows=None, suffix_lens=None, partition_size=0):
+def _shared_prefix_run(sp, rows=None, suffix_lens=None, partition_size=0, block_offset=0):
     """Device: append parent rows, CoW copies, child rows, then the shared-prefix
-    call.  Oracle: its own pool (own slots) and the concatenated-table decode."""
+    call.  Oracle: its own pool (own slots) and the concatenated-table decode.
+    With block_offset, the device side alone relabels every block id i as
+    i + block_offset in a pool that much larger (blocks below stay unused)."""
     shape = (sp.num_blocks, sp.block_size, sp.num_kv_heads, sp.head_dim)
-    kc = torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    off, P = block_offset, sp.block_size
+
+    def ids(x):
+        return torch.from_numpy(np.where(x >= 0, x + off, x).astype(x.dtype)).cuda()
+
+    def slots(x):
+        return torch.from_numpy(np.where(x >= 0, x + off * P, x).astype(np.int64)).cuda()
+
+    kc = torch.full((off + shape[0],) + shape[1:], float("nan"), dtype=torch.bfloat16, device="cuda")
     vc = torch.full_like(kc, float("nan"))
-    pkv.kv_append(kc, vc, sp.parent_k, sp.parent_v, torch.from_numpy(sp.parent_slots).cuda())
-    pkv.kv_block_copy(kc, vc, torch.from_numpy(sp.cow_pairs).cuda())
-    pkv.kv_append(kc, vc, sp.child_k, sp.child_v, torch.from_numpy(sp.child_slots).cuda())
+    pkv.kv_append(kc, vc, sp.parent_k, sp.parent_v, slots(sp.parent_slots))
+    pkv.kv_block_copy(kc, vc, ids(sp.cow_pairs))
+    pkv.kv_append(kc, vc, sp.child_k, sp.child_v, slots(sp.child_slots))
     lens = sp.suffix_lens if suffix_lens is None else np.asarray(suffix_lens, np.int32)
     lse = torch.empty(sp.num_seqs, sp.num_q_heads, dtype=torch.float32, device="cuda")
     out = pkv.shared_prefix_attention(
-        sp.q, kc, vc, torch.from_numpy(sp.prefix_block_ids).cuda(), sp.prefix_len,
-        torch.from_numpy(sp.suffix_tables).cuda(), torch.from_numpy(lens).cuda(), sp.scale,
+        sp.q, kc, vc, ids(sp.prefix_block_ids), sp.prefix_len,
+        ids(sp.suffix_tables), torch.from_numpy(lens).cuda(), sp.scale,
         lse=lse, partition_size=partition_size)
     torch.cuda.synchronize()
     assert pkv.get_device_error() == 0
@@ -437,6 +447,17 @@ def test_shared_prefix_small(batch, prefix, hq, hkv, d):
     sp = wl.shared_prefix_batch(device="cuda", batch=batch, prefix_len=prefix, shared_tail=8,
                                 suffix_lo=8, suffix_hi=200, hq=hq, hkv=hkv, d=d, seed=81 + batch)
     _shared_prefix_run(sp)
+
+
+@pytest.mark.parametrize("hq", [32, 64])  # 64 / 8: the suffixes decode on the tensor cores
+def test_shared_prefix_pool_past_2_31_elements(hq):
+    """Every block the batch uses lies past element 2^31 of the pool: the
+    prefix kernel's and the decode's block coordinates, and the CoW copy's
+    and the appends' 64-bit offsets."""
+    sp = wl.shared_prefix_batch(device="cuda", batch=24, prefix_len=512, shared_tail=8,
+                                suffix_lo=8, suffix_hi=200, hq=hq, hkv=8, d=128, seed=211 + hq)
+    off = 2**31 // (sp.block_size * sp.num_kv_heads * sp.head_dim) + 5
+    _shared_prefix_run(sp, block_offset=off)
 
 
 def test_shared_prefix_with_empty_suffixes():
