@@ -18,13 +18,17 @@ import parity_util as pu
 pytestmark = pytest.mark.gpu
 
 
-def _pools(tb):
+def _pools(tb, block_offset=0):
+    """Device pools filled through kv_append and the oracle's own.  With
+    block_offset, the device side alone relabels every block id i as
+    i + block_offset in a pool that much larger (blocks below stay unused)."""
     shape = (tb.num_blocks, tb.block_size, tb.num_kv_heads, tb.head_dim)
     dt = wl.DTYPES[tb.dtype]
-    kc = torch.full(shape, float("nan"), dtype=dt, device="cuda")
+    kc = torch.full((block_offset + shape[0],) + shape[1:], float("nan"), dtype=dt, device="cuda")
     vc = torch.full_like(kc, float("nan"))
     if tb.slots.size:
-        pkv.kv_append(kc, vc, tb.k_rows, tb.v_rows, torch.from_numpy(tb.slots).cuda())
+        dev_slots = np.where(tb.slots >= 0, tb.slots + block_offset * tb.block_size, tb.slots)
+        pkv.kv_append(kc, vc, tb.k_rows, tb.v_rows, torch.from_numpy(dev_slots.astype(np.int64)).cuda())
     hk, hv = pu.host_pool(tb)
     slots = np.empty(int(tb.row_offsets[-1]), np.int64)
     for c, (first, n, _, _) in enumerate(tb.chunks):
@@ -36,11 +40,11 @@ def _pools(tb):
     return kc, vc, hk, hv
 
 
-def _run(tb, threshold=-1, q=None, pools=None):
-    kc, vc, hk, hv = pools or _pools(tb)
+def _run(tb, threshold=-1, q=None, pools=None, block_offset=0):
+    kc, vc, hk, hv = pools or _pools(tb, block_offset)
     q = tb.q if q is None else q
-    plan = pkv.chunk_tree_plan(kc, tb.chunks, tb.block_ids, tb.num_seqs, tb.num_q_heads,
-                               threshold)
+    plan = pkv.chunk_tree_plan(kc, tb.chunks, (tb.block_ids + block_offset).astype(np.int32),
+                               tb.num_seqs, tb.num_q_heads, threshold)
     lse = torch.empty(tb.num_seqs, tb.num_q_heads, dtype=torch.float32, device="cuda")
     out = pkv.chunk_tree_attention(q, kc, vc, plan, tb.scale, lse=lse)
     torch.cuda.synchronize()
@@ -72,6 +76,16 @@ def test_multi_level_tree(hq, hkv, d, p):
                                leaf_hi=150, seed=hq + p)
     tb = wl.prefix_tree_batch(tree, device="cuda", seed=hq * 3 + p, hq=hq, hkv=hkv, d=d, p=p)
     _run(tb)
+
+
+@pytest.mark.parametrize("threshold", [-1, 4])  # shared chunks chunk-first / all sequence-first
+def test_tree_pool_past_2_31_elements(threshold):
+    """Every block the tree uses lies past element 2^31 of the pool: the
+    chunk-first items' block ids and the sequence-first decode's tables."""
+    tree = wl.multi_level_tree(batch=40, root_len=300, groups=3, group_len=200, leaf_lo=1,
+                               leaf_hi=150, seed=223)
+    tb = wl.prefix_tree_batch(tree, device="cuda", seed=227, hq=32, hkv=8, d=128, p=16)
+    _run(tb, threshold, block_offset=2**31 // (16 * 8 * 128) + 3)
 
 
 def test_long_shared_chunk_splits_and_many_pairs():
