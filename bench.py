@@ -2,15 +2,21 @@
 
 A step is one pass of the decode hot path over one batch: kv_append of each
 sequence's newest K/V row, then paged_attention_decode (split-K partial kernel
-plus log-sum-exp reduction).  Default workload: the Llama-3-8B-shaped decode
-layer (bf16, batch 64, 32/8 heads, head_dim 128, block size 16, lengths
-uniform in [512, 8192], 1.25x pool from a shuffled free FIFO).
+plus log-sum-exp reduction).  Default workload: the long-context decode
+(bf16, batch 8, lengths uniform in [32768, 65536], 32/8 heads, head_dim 128,
+block size 16, random physical placement, split-K over blocks), the largest
+steady decode configuration.
 
 Prints one JSON line (rank 0).  `value` is decode KV GB/s: algorithmic K/V
 bytes of the visible rows (4096 B per token row for this layer) per step over
 the device-timed step time.  `e2e` is the same metric through the C ABI with
 the per-step inputs copied from pinned host memory and the output read back
-inside the timed region.
+inside the timed region.  On one GPU the default run also measures, as extra
+keys of the same line, a read-only HBM streaming peak and the other
+configured workloads (the Llama-shaped layer, long context at block size 64,
+the 200-step churn trace, the shared-prefix batch, the prefix tree, eight
+query heads per kv head, and both over MXFP8 pools), each with its own
+roofline.
 
 --impl reference times the CPU oracle on bounded samples of the same workload.
 """
@@ -42,13 +48,15 @@ def parse():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
-    ap.add_argument("--workload", default="llama", choices=WORKLOADS)
+    ap.add_argument("--workload", default="long_bs16", choices=WORKLOADS)
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--batch", type=int, default=0,
                     help="override the batch size (small cases for profiling)")
     ap.add_argument("--prefix-len", type=int, default=0,
                     help="shared workload: prefix tokens (default 2048)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the read peak and the other workloads of the default run")
     ap.add_argument("--cpu-sample-seconds", type=float, default=12.0)
     return ap.parse_args()
 
@@ -177,6 +185,37 @@ def make_batch(name, device, seed_offset=0, batch=0):
         return wl.custom_batch(step.seq_lens, dtype="bf16", hq=32, hkv=8, d=128, p=16,
                                seed=4 + seed_offset, device=device)
     raise ValueError(name)
+
+
+DECODE_WORKLOAD_NAMES = {
+    "llama": "llama3-8b-shaped decode layer",
+    "llama_mxfp8": "llama3-8b-shaped decode layer over MXFP8 K/V pools",
+    "long_bs16": "long-context decode, block size 16",
+    "long_bs64": "long-context decode, block size 64",
+    "long_bs64_k16": "long-context decode, block size 64 read as 16-row kernel blocks "
+                     "(tables expanded per step)",
+    "gqa8": "decode layer with 8 query heads per kv head (64/8)",
+    "gqa8_mxfp8": "decode layer with 8 query heads per kv head (64/8) over MXFP8 K/V pools",
+    "churn": "churn trace decode",
+}
+
+
+def decode_config(workload, b, partition_size, world):
+    """The config of a decode workload, the same for both arms."""
+    kblock = 16 if workload == "long_bs64_k16" else b.block_size
+    mx = workload.endswith("_mxfp8")
+    row_bytes = 2 * b.num_kv_heads * b.head_dim * 33 // 32 if mx else kv_row_bytes(b)
+    return {
+        "workload": DECODE_WORKLOAD_NAMES[workload],
+        "batch": b.num_seqs, "num_q_heads": b.num_q_heads, "num_kv_heads": b.num_kv_heads,
+        "head_dim": b.head_dim, "block_size": b.block_size, "kernel_block_size": kblock,
+        "seq_len_min": int(b.seq_lens.min()), "seq_len_max": int(b.seq_lens.max()),
+        "total_tokens": int(b.seq_lens.sum()), "pool_blocks": b.num_blocks,
+        "partition_size": partition_size,
+        "kv_bytes_per_step": int(b.seq_lens.astype(np.int64).sum()) * row_bytes,
+        "l2": "inputs larger than L2 (K/V read per step >> 129 MB)",
+        "parallelism": f"replicas x{world} (sequences shard, no collective)",
+    }
 
 
 def kv_row_bytes(b):
@@ -470,26 +509,8 @@ def run_pkv(args, rank, world, local):
         "vs_baseline": None,
         "dtype": "mxfp8 K/V, bf16 q/out" if mx else b.dtype,
         "data": "synthetic (seeded N(0,1) q/k/v, seeded lengths and block placement)",
-        "config": {
-            "workload": {"llama": "llama3-8b-shaped decode layer",
-                         "llama_mxfp8": "llama3-8b-shaped decode layer over MXFP8 K/V pools",
-                         "long_bs16": "long-context decode, block size 16",
-                         "long_bs64": "long-context decode, block size 64",
-                         "long_bs64_k16": "long-context decode, block size 64 read as "
-                                          "16-row kernel blocks (tables expanded per step)",
-                         "gqa8": "decode layer with 8 query heads per kv head (64/8)",
-                         "gqa8_mxfp8": "decode layer with 8 query heads per kv head (64/8) over "
-                                       "MXFP8 K/V pools",
-                         }[args.workload],
-            "batch": B, "num_q_heads": b.num_q_heads, "num_kv_heads": b.num_kv_heads,
-            "head_dim": b.head_dim, "block_size": b.block_size, "kernel_block_size": kblock,
-            "seq_len_min": int(b.seq_lens.min()), "seq_len_max": int(b.seq_lens.max()),
-            "total_tokens": int(b.seq_lens.sum()), "pool_blocks": b.num_blocks,
-            "partition_size": psize, "decode_ctas": ctas,
-            "kv_bytes_per_step": kv_bytes,
-            "l2": "inputs larger than L2 (K/V read per step >> 129 MB)",
-            "parallelism": f"replicas x{world} (sequences shard, no collective)",
-        },
+        "config": decode_config(args.workload, b, psize, world),
+        "decode_ctas": ctas,
         "rows_per_s": world * B / (ms_step * 1e-3),
         "pct_of_hbm_peak": 100.0 * (kv_bytes / (ms_step * 1e-3) / 1e9) / peak,
         "decode_ms": decode_ms,
@@ -977,7 +998,7 @@ def tree_cpu_baseline(tb, seconds):
 
 
 # ------------------------------------------------------------------ churn trace
-def run_churn(args, rank, world, local):
+def run_churn(args, rank, world, local, want_batch=True):
     """256 concurrent requests; each step appends one row per request, then
     decodes.  Requests finish (geometric output lengths) and are replaced by
     arrivals whose whole prompt is appended first (untimed, as prefill).  The
@@ -1085,7 +1106,7 @@ def run_churn(args, rank, world, local):
         "gpu_launches": n_timed * 3,  # append, partial, reduce
         "clocks": clk,
     }
-    return res, make_batch("churn", "cpu", seed_offset=rank)
+    return res, (make_batch("churn", "cpu", seed_offset=rank) if want_batch else None)
 
 
 def kv_row_bytes_dims(hkv, d, elem):
@@ -1132,6 +1153,99 @@ def shared_cpu_baseline(sp, seconds):
 
 
 
+# ------------------------------------------------------------------ read peak, extras
+def hbm_read_peak(dev, reps=10):
+    """Read-only HBM streaming peak of this GPU: the better of the two probes
+    of libpkv_probe (16-byte loads that skip L1; 32 KiB bulk copies into
+    shared memory), each streaming a ~4 GB buffer (>> L2) once per launch,
+    best of `reps` launches timed with CUDA events on the launching stream."""
+    import ctypes
+    import torch
+    from paged_kv_cache_41_gb300 import build as pkv_build
+    lib = ctypes.CDLL(pkv_build.build_probe())
+    for fn in (lib.pkv_probe_hbm_read_lsu, lib.pkv_probe_hbm_read_bulk):
+        fn.restype = ctypes.c_int
+        fn.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p,
+                       ctypes.c_void_p]
+    lib.pkv_probe_error.restype = ctypes.c_int
+    lib.pkv_probe_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    nbytes = sms * 32768 * 800
+    buf = torch.ones(nbytes // 4, dtype=torch.int32, device=dev)
+    sink = torch.zeros(sms * 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    res = {}
+    for name, fn, ctas in (("lsu", lib.pkv_probe_hbm_read_lsu, sms * 4),
+                           ("bulk", lib.pkv_probe_hbm_read_bulk, sms)):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps + 2)]
+        for a, b in evs:
+            a.record(stream)
+            rc = fn(buf.data_ptr(), nbytes, ctas, sink.data_ptr(), stream.cuda_stream)
+            b.record(stream)
+            assert rc == 0, f"read probe {name} failed to launch"
+        torch.cuda.synchronize()
+        ms = min(a.elapsed_time(b) for a, b in evs[2:])
+        res[name] = nbytes / (ms * 1e-3) / 1e9
+    err = ctypes.c_uint(0)
+    assert lib.pkv_probe_error(ctypes.byref(err)) == 0 and err.value == 0
+    del buf
+    torch.cuda.empty_cache()
+    best = max(res.values())
+    return {"value": best, "unit": "GB/s", "lsu": res["lsu"], "bulk": res["bulk"],
+            "bytes_per_launch": nbytes,
+            "how": "read-only streaming of a buffer >> L2 once per launch, writing nothing "
+                   f"but one word per CTA; best of {reps} launches (CUDA events); the better "
+                   "of 16-byte L1-bypassing loads (4 CTAs x 512 threads per SM) and 32 KiB "
+                   "cp.async.bulk copies into a 4-slot shared-memory ring (1 CTA per SM)"}
+
+
+def _compact(r, read_peak=None):
+    """The keys of a workload's result that an extra entry keeps."""
+    keep = ("value", "unit", "ms_per_step", "steps", "warmup", "rows_per_s", "decode_ms",
+            "append_ms", "pct_of_hbm_peak", "prefix_ms", "shared_prefix_call_ms", "tree_call_ms",
+            "effective_kv_gbps", "unique_kv_bytes", "roofline", "clocks", "gpu_launches",
+            "decode_ctas", "config")
+    d = {k: r[k] for k in keep if k in r}
+    d["e2e"] = {k: r["e2e"][k] for k in ("value", "unit", "ms_per_step") if k in r["e2e"]}
+    if read_peak and d.get("roofline", {}).get("bound") == "hbm":
+        d["roofline"] = dict(d["roofline"], read_peak=read_peak,
+                             frac_of_read_peak=d["roofline"]["achieved"] / read_peak)
+    return d
+
+
+def run_extras(args, local):
+    """The other configured workloads, measured in the same run (one GPU):
+    each keeps its own timing rules (L2 flushed or inputs larger than L2) and
+    its own roofline."""
+    import torch
+
+    def sub(**kw):
+        d = dict(vars(args))
+        d.update(kw)
+        return argparse.Namespace(**d)
+
+    out = {}
+    peak = hbm_read_peak(torch.device(f"cuda:{local}"))
+    out["hbm_read_peak"] = peak
+    rp = peak["value"]
+    for name in ("llama", "long_bs64", "gqa8", "llama_mxfp8", "gqa8_mxfp8"):
+        r, _ = run_pkv(sub(workload=name, batch=0, partition_size=0), 0, 1, local)
+        out[name] = _compact(r, rp)
+        torch.cuda.empty_cache()
+    # the churn trace as configured: 200 decode steps, the first 5 untimed
+    r, _ = run_churn(sub(workload="churn", warmup=5, steps=195), 0, 1, local, want_batch=False)
+    out["churn"] = _compact(r, rp)
+    torch.cuda.empty_cache()
+    r, _ = run_shared(sub(workload="shared", batch=0, prefix_len=0), 0, 1, local)
+    out["shared"] = _compact(r, rp)
+    torch.cuda.empty_cache()
+    r, _ = run_tree(sub(workload="tree", batch=0), 0, 1, local)
+    out["tree"] = _compact(r, rp)
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     args = parse()
     if args.warmup < 3:
@@ -1166,6 +1280,15 @@ def main():
         if rank == 0 and not args.no_cpu_baseline and world == 1:
             res["cpu_baseline"] = cpu_baseline(b, args.cpu_sample_seconds,
                                                args.workload.endswith("_mxfp8"))
+        del b
+        if (world == 1 and args.workload == "long_bs16" and not args.batch
+                and not args.no_extras):
+            extras = run_extras(args, local)
+            rp = extras["hbm_read_peak"]["value"]
+            res["roofline"]["read_peak"] = rp
+            res["roofline"]["frac_of_read_peak"] = res["roofline"]["achieved"] / rp
+            res["hbm_read_peak"] = extras.pop("hbm_read_peak")
+            res["also_measured"] = extras
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
@@ -1241,7 +1364,8 @@ def run_reference(args):
         "value": v, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload},
+        "config": decode_config(args.workload, b, args.partition_size,
+                                int(os.environ.get("WORLD_SIZE", "1"))),
         "rows_per_s": tot_r / tot_t,
         "cpu_baseline": {"value": v, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
                          "sample": f"per step: {desc}"},

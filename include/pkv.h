@@ -20,8 +20,13 @@
  * CONVENTIONS (every call).
  *   - Every pointer argument is a DEVICE pointer unless stated otherwise; the
  *     caller allocates and owns all device memory.  The library allocates
- *     nothing and keeps no state between calls except one device error word
- *     per device (see pkv_get_device_error).
+ *     no device memory at run time.  Its state between calls: one device
+ *     error word per device (see pkv_get_device_error); the fixed scratch
+ *     array that pkv_paged_attention_decode_static alone uses (a static
+ *     device array, PKV_STATIC_SCRATCH_BYTES on every device that loads the
+ *     library); and a host-side cache of up to 64 encoded TMA tensor maps,
+ *     keyed by every argument of the encoding (base address, shape, strides,
+ *     box, swizzle), so a hit returns the map a fresh encoding would give.
  *   - Every call is asynchronous on `stream` (a cudaStream_t, NULL = legacy
  *     default stream) and returns after enqueuing its kernels.
  *   - Arguments are validated on the host before any launch; a rejected call

@@ -60,6 +60,8 @@ def _load():
         lib.pkv_oracle_resolve.argtypes = [vp, i64, i64, i64, i64, i64, p64, p64]
         lib.pkv_oracle_slot_for_position.restype = i64
         lib.pkv_oracle_slot_for_position.argtypes = [vp, i64, i64]
+        lib.pkv_oracle_slots_for_positions.restype = i32
+        lib.pkv_oracle_slots_for_positions.argtypes = [vp, i64, vp, vp, i64, i64, vp]
         lib.pkv_oracle_kv_append.restype = i32
         lib.pkv_oracle_kv_append.argtypes = [i32, vp, vp, i64, i32, i32, i32, vp, vp, vp, i64]
         lib.pkv_oracle_kv_block_copy.restype = i32
@@ -138,6 +140,22 @@ def resolve(table, context_len: int, block_size: int, num_pool_blocks: int, toke
 def slot_for_position(table, block_size: int, pos: int) -> int:
     t = np.ascontiguousarray(table, dtype=np.int32)
     return _load().pkv_oracle_slot_for_position(_ptr(t), block_size, pos)
+
+
+def slots_for_positions(tables, block_size: int, rows, positions) -> np.ndarray:
+    """slot_for_position for many (request, position) pairs: request rows[i]
+    (a row of the 2-D int32 tables), position positions[i]."""
+    t = np.ascontiguousarray(tables, dtype=np.int32)
+    assert t.ndim == 2
+    r = np.ascontiguousarray(rows, dtype=np.int32)
+    p = np.ascontiguousarray(positions, dtype=np.int64)
+    assert r.shape == p.shape
+    out = np.empty(p.shape, np.int64)
+    st = _load().pkv_oracle_slots_for_positions(_ptr(t), t.shape[1], _ptr(r), _ptr(p), p.size,
+                                                block_size, _ptr(out))
+    if st != OK:
+        raise ValueError("slots_for_positions: a row, position or table bound is out of range")
+    return out
 
 
 # ---------------------------------------------------------------- data ops

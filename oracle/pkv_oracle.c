@@ -92,6 +92,19 @@ int64_t pkv_oracle_slot_for_position(const int32_t* table, int64_t block_size,
   return physical * block_size + pos % block_size;
 }
 
+int pkv_oracle_slots_for_positions(const int32_t* tables, int64_t table_stride,
+                                   const int32_t* rows, const int64_t* positions, int64_t n,
+                                   int64_t block_size, int64_t* out) {
+  if (n < 0 || table_stride <= 0 || block_size <= 0) return PKV_ORACLE_BAD_ARG;
+  for (int64_t i = 0; i < n; ++i) {
+    if (rows[i] < 0 || positions[i] < 0 || positions[i] / block_size >= table_stride)
+      return PKV_ORACLE_BAD_ARG;
+    out[i] = pkv_oracle_slot_for_position(tables + (int64_t)rows[i] * table_stride, block_size,
+                                          positions[i]);
+  }
+  return PKV_ORACLE_OK;
+}
+
 int pkv_oracle_kv_append(int dtype, void* k_cache, void* v_cache,
                          int64_t num_blocks, int block_size, int num_kv_heads,
                          int head_dim, const void* k, const void* v,

@@ -75,6 +75,14 @@ int pkv_oracle_resolve(const int32_t* table, int64_t table_len,
 int64_t pkv_oracle_slot_for_position(const int32_t* table, int64_t block_size,
                                      int64_t pos);
 
+/* The same slot for n (request, position) pairs at once: out[i] is the slot
+ * of position positions[i] of the request whose table is row rows[i] of
+ * `tables` ([*, table_stride] int32).  A negative row or position, or a
+ * position past the table, returns PKV_ORACLE_BAD_ARG. */
+int pkv_oracle_slots_for_positions(const int32_t* tables, int64_t table_stride,
+                                   const int32_t* rows, const int64_t* positions, int64_t n,
+                                   int64_t block_size, int64_t* out);
+
 /* Write new token rows.  Row i (num_kv_heads * head_dim elements of k and of
  * v) goes to slot slots[i]; a negative slot is skipped ([Cache] -1 sentinel).
  * Returns PKV_ORACLE_BAD_SLOT (after writing every valid row) if any slot is

@@ -2,8 +2,12 @@
 
 * ``libpkv.so``      -- the CUDA kernels and their C ABI (nvcc, sm_103a only).
 * ``libpkv_pool.so`` -- the host block pool (gcc, plain C99).
+* ``libpkv_probe.so`` -- read-only HBM streaming probes (bench.py's
+  read-bandwidth denominator).
+* ``tests/libpkv_wait_probe.so`` -- a test-only kernel for the bounded
+  mbarrier wait (not part of libpkv).
 
-Both land next to this file.  Sources compile in parallel; nothing here uses
+The first three land next to this file.  Sources compile in parallel; nothing here uses
 cmake or setuptools.
 """
 from __future__ import annotations
@@ -103,9 +107,47 @@ def build_cuda(force=False, extra_flags=()) -> str:
     return LIB
 
 
+PROBE_SRC = os.path.join(CSRC, "probe", "hbm_read.cu")
+PROBE_LIB = os.path.join(HERE, "libpkv_probe.so")
+
+
+def build_probe(force=False) -> str:
+    """The read-only HBM streaming probes that bench.py measures its
+    read-bandwidth denominator with (csrc/probe/hbm_read.cu)."""
+    deps = [PROBE_SRC, os.path.join(CSRC, "kernels", "common.cuh"), os.path.join(INCLUDE, "pkv.h")]
+    if not force and _newer(PROBE_LIB, deps):
+        return PROBE_LIB
+    tmp = PROBE_LIB + ".tmp"
+    subprocess.check_call([NVCC, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+                           "-shared", "-I", INCLUDE, "-I", CSRC, "-o", tmp, PROBE_SRC])
+    os.replace(tmp, PROBE_LIB)
+    return PROBE_LIB
+
+
+WAIT_PROBE_SRC = os.path.join(ROOT, "tests", "csrc", "wait_probe.cu")
+WAIT_PROBE_LIB = os.path.join(ROOT, "tests", "libpkv_wait_probe.so")
+
+
+def build_wait_probe(force=False) -> str:
+    """The test suite's bounded-wait probe (tests/csrc/wait_probe.cu): its own
+    small library over the kernels' common.cuh, not part of libpkv."""
+    deps = [WAIT_PROBE_SRC, os.path.join(CSRC, "kernels", "common.cuh"),
+            os.path.join(INCLUDE, "pkv.h")]
+    if not force and _newer(WAIT_PROBE_LIB, deps):
+        return WAIT_PROBE_LIB
+    tmp = WAIT_PROBE_LIB + ".tmp"
+    subprocess.check_call([NVCC, *ARCH, "-O2", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+                           "-shared", "-I", INCLUDE, "-I", CSRC, "-o", tmp, WAIT_PROBE_SRC])
+    os.replace(tmp, WAIT_PROBE_LIB)
+    return WAIT_PROBE_LIB
+
+
 def build_all(force=False) -> None:
     build_pool(force)
     build_cuda(force)
+    build_probe(force)
+    if os.path.exists(WAIT_PROBE_SRC):
+        build_wait_probe(force)
 
 
 if __name__ == "__main__":

@@ -11,9 +11,10 @@
 //
 // Design (GB300):
 //   * persistent, balanced CTAs: the work is the list of 32-row stages of
-//     every (sequence, kv head) segment, sequence-major; a one-CTA planning
-//     kernel scans the lengths, and CTA c of C (one wave: four per SM) streams
-//     stages [c S / C, (c + 1) S / C) of the S in the list.  Every CTA moves
+//     every (sequence, kv head) segment, sequence-major; every CTA scans the
+//     lengths itself (a block-wide prefix sum, no planning launch), and CTA c
+//     of C (one wave: four per SM) streams stages [c S / C, (c + 1) S / C) of
+//     the S in the list.  Every CTA moves
 //     the same bytes whatever the length mix, there is no tail wave, and a
 //     CTA crosses segment boundaries without draining its pipeline;
 //   * a segment a CTA covers whole is finished there (output written

@@ -36,12 +36,11 @@ def assert_close(gpu, ref, what=""):
 
 
 def oracle_batch_slots(b: wl.PagedBatch) -> np.ndarray:
-    out = np.empty(int(b.hist_offsets[-1]), np.int64)
-    for r in range(b.num_seqs):
-        lo = int(b.hist_offsets[r])
-        for t in range(int(b.seq_lens[r])):
-            out[lo + t] = oracle.slot_for_position(b.block_tables[r], b.block_size, t)
-    return out
+    """The oracle's slot for every history row, in history order."""
+    lens = b.seq_lens.astype(np.int64)
+    rows = np.repeat(np.arange(b.num_seqs, dtype=np.int32), lens)
+    pos = np.arange(int(lens.sum()), dtype=np.int64) - np.repeat(b.hist_offsets[:-1], lens)
+    return oracle.slots_for_positions(b.block_tables, b.block_size, rows, pos)
 
 
 def device_pool(b, device="cuda"):

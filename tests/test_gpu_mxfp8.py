@@ -290,7 +290,7 @@ def test_eight_heads_per_kv_head_at_head_dim_64_is_rejected():
     assert e.value.status == pkv.PKV_ERR_UNSUPPORTED
 
 
-def test_llama_shaped_full_size_sampled():
+def test_llama_shaped_full_size():
     b = wl.llama_batch(device="cuda")
     shape = _shape(b)
     kc = pkv.MxPool(*shape, device="cuda", fill=0xFF)
@@ -302,8 +302,8 @@ def test_llama_shaped_full_size_sampled():
                                      torch.from_numpy(b.seq_lens).to(dev), b.scale, lse=lse)
     torch.cuda.synchronize()
     assert pkv.get_device_error() == 0
-    # the oracle quantizes the sampled sequences into a pool of its own
-    rows = np.unique(np.concatenate([np.argsort(b.seq_lens)[[0, -1]], np.arange(0, 64, 13)]))
+    # the oracle quantizes every sequence into a pool of its own
+    rows = np.arange(b.num_seqs)
     P = b.block_size
     tables, lens, kh, vh, slots, nxt = [], [], [], [], [], 0
     kall, vall = wl.to_numpy_storage(b.k_hist), wl.to_numpy_storage(b.v_hist)
@@ -317,7 +317,8 @@ def test_llama_shaped_full_size_sampled():
         lo = int(b.hist_offsets[r])
         kh.append(kall[lo:lo + t])
         vh.append(vall[lo:lo + t])
-        slots.append(np.array([oracle.slot_for_position(own, P, i) for i in range(t)], np.int64))
+        slots.append(oracle.slots_for_positions(own[None, :], P, np.zeros(t, np.int32),
+                                                np.arange(t, dtype=np.int64)))
     width = max(len(t) for t in tables)
     tb = np.full((len(rows), width), -1, np.int32)
     for i, t in enumerate(tables):
@@ -331,5 +332,5 @@ def test_llama_shaped_full_size_sampled():
     ref, ref_lse = oracle.paged_decode(np.ascontiguousarray(q), oracle.mxfp8_to_f32(hk, oshape),
                                        oracle.mxfp8_to_f32(hv, oshape), tb,
                                        np.array(lens, np.int32), b.scale, nthreads=pu.NTHREADS)
-    pu.assert_close(out.float().cpu().numpy()[rows], ref, "llama mxfp8 out")
-    pu.assert_close(lse.cpu().numpy()[rows], ref_lse, "llama mxfp8 lse")
+    pu.assert_close(out.float().cpu().numpy(), ref, "llama mxfp8 out")
+    pu.assert_close(lse.cpu().numpy(), ref_lse, "llama mxfp8 lse")

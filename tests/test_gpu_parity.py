@@ -134,10 +134,10 @@ def test_tensor_core_many_short_pieces():
     _run_batch(b, check_pool=False)
 
 
-def test_gqa8_tensor_core_decode_long_sampled():
+def test_gqa8_tensor_core_decode_long():
     lens = np.array([40000, 3000, 65536, 1], np.int32)
     b = wl.custom_batch(lens, dtype="bf16", hq=32, hkv=4, d=128, p=16, seed=62, device="cuda")
-    _run_batch(b, rows=np.array([0, 2, 3]))
+    _run_batch(b)
 
 
 def test_empty_batch_rows_and_all_empty():
@@ -150,17 +150,20 @@ def test_empty_batch_rows_and_all_empty():
     assert not out.any() and np.isneginf(lse).all()
 
 
-def test_llama_shaped_full_size_sampled():
+def test_llama_shaped_full_size():
+    # the Llama-shaped decode layer at full size (64 sequences, 32/8 heads,
+    # lengths 512..8192): whole pools bit for bit after the appends, every
+    # row and head of the decode against the oracle
     b = wl.llama_batch(device="cuda")
-    rows = np.unique(np.concatenate([np.argsort(b.seq_lens)[[0, 1, -2, -1]], np.arange(0, 64, 9)]))
-    _run_batch(b, rows=rows)
+    _run_batch(b)
 
 
 @pytest.mark.parametrize("block_size", [16, 64])
-def test_long_context_full_size_sampled(block_size):
+def test_long_context_full_size(block_size):
+    # the long-context decode at full size (8 sequences of 32k..64k rows):
+    # whole pools, every row and head
     b = wl.long_batch(device="cuda", block_size=block_size)
-    rows = np.array([int(np.argmax(b.seq_lens)), int(np.argmin(b.seq_lens))])
-    _run_batch(b, rows=rows)
+    _run_batch(b)
 
 
 def test_block_copy_bit_exact():
@@ -332,9 +335,28 @@ def test_churn_trace_config_shapes():
     assert _churn(tr, hq=32, hkv=8, d=128, check_pools=False) >= 3
 
 
-def _churn(tr, hq, hkv, d, check_pools):
+def test_churn_trace_as_configured():
+    """The churn trace exactly as configured: 256 concurrent requests over 200
+    decode steps, prompts lognormal (median 1024, sigma 1.0, capped at 16384),
+    outputs geometric with mean 200, 32/8 heads, head_dim 128, block size 16,
+    pool 1.25 x the dry run's peak.  Every step runs the arrivals' prompt
+    appends, the step's append and the decode on the device, and the same
+    appends in the oracle's own pool.  At ten evenly spaced steps the whole
+    pools are compared bit for bit (every row appended since the last check,
+    arrival prompts included, and every stale row of a freed block) and every
+    row and head of that step's decode against the oracle."""
+    tr = wl.ChurnTrace()  # the defaults are the configured trace
+    assert (tr.concurrency, tr.steps, tr.block_size) == (256, 200, 16)
+    checks = set(np.linspace(0, tr.steps - 1, 10).round().astype(int).tolist())
+    assert len(checks) == 10
+    assert _churn(tr, hq=32, hkv=8, d=128, check_pools=True, check_steps=checks,
+                  fresh_q=True) >= 100
+
+
+def _churn(tr, hq, hkv, d, check_pools, check_steps=None, fresh_q=False):
     """Run the trace on the device and in the oracle; returns the number of
-    steps that saw arrivals."""
+    steps that saw arrivals.  check_steps: the steps whose pools and decode
+    are compared (None: every step).  fresh_q: draw a new q every step."""
     p = tr.block_size
     B = tr.concurrency
     shape = (tr.num_blocks, p, hkv, d)
@@ -344,40 +366,44 @@ def _churn(tr, hq, hkv, d, check_pools):
     hv = np.full(shape, 0x7FC0, np.uint16)
     gen = wl.make_generator(44, "cuda")
     q = wl.randn((B, hq, d), "bf16", gen, "cuda")
-    qh = wl.to_numpy_storage(q)
     scale = 1.0 / np.sqrt(d)
     arrivals = 0
-    for step in tr.run():
+    for i_step, step in enumerate(tr.run()):
         if step.arrival_rows:
             arrivals += 1
             ak = wl.randn((step.arrival_rows, hkv, d), "bf16", gen, "cuda")
             av = wl.randn((step.arrival_rows, hkv, d), "bf16", gen, "cuda")
             pkv.kv_append(kc, vc, ak, av, torch.from_numpy(step.arrival_slots).cuda())
-            slots = np.array([oracle.slot_for_position(step.block_tables[i], p, int(pos))
-                              for i, pos in zip(step.arrival_seq_index, step.arrival_positions)],
-                             np.int64)
+            slots = oracle.slots_for_positions(step.block_tables, p, step.arrival_seq_index,
+                                               step.arrival_positions)
             assert oracle.kv_append(hk, hv, wl.to_numpy_storage(ak), wl.to_numpy_storage(av),
                                     slots) == oracle.OK
         nk = wl.randn((B, hkv, d), "bf16", gen, "cuda")
         nv = wl.randn((B, hkv, d), "bf16", gen, "cuda")
         pkv.kv_append(kc, vc, nk, nv, torch.from_numpy(step.step_slots).cuda())
-        slots = np.array([oracle.slot_for_position(step.block_tables[i], p,
-                                                   int(step.seq_lens[i]) - 1)
-                          for i in range(B)], np.int64)
+        slots = oracle.slots_for_positions(step.block_tables, p, np.arange(B, dtype=np.int32),
+                                           step.seq_lens.astype(np.int64) - 1)
         assert oracle.kv_append(hk, hv, wl.to_numpy_storage(nk), wl.to_numpy_storage(nv),
                                 slots) == oracle.OK
+        if fresh_q:
+            q = wl.randn((B, hq, d), "bf16", gen, "cuda")
         bt = torch.from_numpy(step.block_tables).cuda()
         sl = torch.from_numpy(step.seq_lens).cuda()
         lse = torch.empty(B, hq, dtype=torch.float32, device="cuda")
         out = pkv.paged_attention_decode(q, kc, vc, bt, sl, scale, lse=lse)
+        if check_steps is not None and i_step not in check_steps:
+            continue
         torch.cuda.synchronize()
         assert pkv.get_device_error() == 0
         if check_pools:
-            assert pu.pools_equal_bytes(kc, hk) and pu.pools_equal_bytes(vc, hv)
-        ref, ref_lse = oracle.paged_decode(qh, hk, hv, step.block_tables, step.seq_lens, scale,
-                                           nthreads=pu.NTHREADS)
-        pu.assert_close(out.float().cpu().numpy(), ref, "churn out")
-        pu.assert_close(lse.cpu().numpy(), ref_lse, "churn lse")
+            assert pu.pools_equal_bytes(kc, hk), f"K pool differs from the oracle's at step {i_step}"
+            assert pu.pools_equal_bytes(vc, hv), f"V pool differs from the oracle's at step {i_step}"
+        ref, ref_lse = oracle.paged_decode(wl.to_numpy_storage(q), hk, hv, step.block_tables,
+                                           step.seq_lens, scale, nthreads=pu.NTHREADS)
+        pu.assert_close(out.float().cpu().numpy(), ref, f"churn out, step {i_step}")
+        pu.assert_close(lse.cpu().numpy(), ref_lse, f"churn lse, step {i_step}")
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 0
     return arrivals
 
 
@@ -440,7 +466,8 @@ def _shared_prefix_run(sp, rows=None, suffix_lens=None, partition_size=0, block_
 @pytest.mark.parametrize("batch,prefix,hq,hkv,d", [
     (16, 256, 32, 8, 128), (5, 384, 8, 2, 128), (40, 128, 16, 16, 64), (3, 512, 16, 2, 128),
     (24, 256, 64, 8, 128),  # eight heads per kv head: the suffixes decode on the tensor cores
-    # 2, 3 (padded to 4) and 5 (padded to 8) query tiles: clusters of 2 and 4 CTAs
+    # 2, 3 and 5 query tiles of 128 rows: odd tile counts leave a CTA's second
+    # tile (B) partly or wholly past the last request
     (50, 256, 32, 8, 128), (80, 384, 32, 8, 128), (150, 256, 32, 8, 64),
 ])
 def test_shared_prefix_small(batch, prefix, hq, hkv, d):
@@ -468,10 +495,10 @@ def test_shared_prefix_with_empty_suffixes():
     _shared_prefix_run(sp, suffix_lens=lens)
 
 
-def test_shared_prefix_full_size_sampled():
-    sp = wl.shared_prefix_batch(device="cuda")  # 128 requests, 2048-token prefix
-    rows = np.array([0, 1, 31, 32, 63, 64, 100, 127])
-    _shared_prefix_run(sp, rows=rows)
+def test_shared_prefix_full_size():
+    # 128 requests on one 2048-token prefix, every request and head
+    sp = wl.shared_prefix_batch(device="cuda")
+    _shared_prefix_run(sp)
 
 
 @pytest.mark.parametrize("split_len", [0, 128, 384])

@@ -90,14 +90,43 @@ def test_resolve_rejection_order():
     assert oracle.resolve([3, 5], 40, 16, 8, 20)[:2] == (oracle.OK, 5)
 
 
-def test_slot_mapping_of_the_35_token_example():
-    # "7. Memory Management and Local Model State": logical blocks 0, 1, 2 of a
-    # 35-token sequence sit in physical blocks 7, 2, 19.  Enumerate the slots as
-    # whole physical row ranges and compare position by position.
-    table = [7, 2, 19]
-    expect = list(range(7 * 16, 8 * 16)) + list(range(2 * 16, 3 * 16)) + list(range(19 * 16, 19 * 16 + 3))
+@pytest.mark.parametrize("table", [[3, 8, 1], [7, 2, 19]])
+def test_slot_mapping_of_the_35_token_example(table):
+    # "7. Memory Management and Local Model State", section "Logical tokens,
+    # physical blocks", draws the 35-token sequence twice with different
+    # placements: its flowchart maps logical blocks 0, 1, 2 to physical blocks
+    # 3, 8, 1, and the position ruler below it to 7, 2, 19.  Either table must
+    # give the same slots: whole physical row ranges for the two full blocks
+    # and the first three rows of the third.
+    a, b, c = table
+    expect = (list(range(a * 16, (a + 1) * 16)) + list(range(b * 16, (b + 1) * 16))
+              + list(range(c * 16, c * 16 + 3)))
     got = [oracle.slot_for_position(table, 16, t) for t in range(35)]
     assert got == expect
+
+
+def test_batched_slots_equal_enumerated_row_ranges():
+    # the batched form against the slots enumerated as whole physical row
+    # ranges of each request's blocks, for a ragged, shuffled batch
+    rng = np.random.default_rng(7)
+    p = 16
+    ids = rng.permutation(200).astype(np.int32)
+    lens = [35, 1, 16, 100, 0, 47]
+    tables = np.full((len(lens), 8), -1, np.int32)
+    expect, rows, pos, nxt = [], [], [], 0
+    for r, t in enumerate(lens):
+        n = -(-t // p)
+        tables[r, :n] = ids[nxt:nxt + n]
+        nxt += n
+        slots = np.concatenate([np.arange(b * p, (b + 1) * p) for b in tables[r, :n]] or [[]])
+        expect.extend(slots[:t].tolist())
+        rows += [r] * t
+        pos += list(range(t))
+    order = rng.permutation(len(pos))
+    got = oracle.slots_for_positions(tables, p, np.array(rows)[order], np.array(pos)[order])
+    assert got.tolist() == np.array(expect, np.int64)[order].tolist()
+    with pytest.raises(ValueError):
+        oracle.slots_for_positions(tables, p, [0], [8 * p])  # past the table
 
 
 def test_slot_ids_widen_to_int64():

@@ -77,3 +77,31 @@ def test_static_scratch_refuses_oversized_requests():
     with pytest.raises(pkv.PkvError) as ei:
         pkv.paged_attention_decode_static(q, kc, kc, bt, sl, 1.0, partition_size=256)
     assert ei.value.status == pkv.PKV_ERR_CAPACITY
+
+
+def test_static_calls_allocate_no_device_memory():
+    # out and lse are the caller's; the first call on the device looks up the
+    # scratch array's address (and loads the kernels), so it comes first.
+    # After it, several calls must leave both torch's allocator and the
+    # device's free memory exactly as they were.
+    b = wl.custom_batch([1000, 37, 4096, 0, 513, 2000], dtype="bf16", hq=32, hkv=8, d=128, p=16,
+                        seed=74, device="cuda")
+    kc, vc = _pool(b)
+    bt = torch.from_numpy(b.block_tables).cuda()
+    sl = torch.from_numpy(b.seq_lens).cuda()
+    out = torch.empty_like(b.q)
+    lse = torch.empty(b.num_seqs, b.num_q_heads, dtype=torch.float32, device="cuda")
+    ref_lse = torch.empty_like(lse)
+    ref = pkv.paged_attention_decode(b.q, kc, vc, bt, sl, b.scale, lse=ref_lse)
+    pkv.paged_attention_decode_static(b.q, kc, vc, bt, sl, b.scale, out=out, lse=lse)
+    torch.cuda.synchronize()
+    alloc0 = torch.cuda.memory_allocated()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(5):
+        got = pkv.paged_attention_decode_static(b.q, kc, vc, bt, sl, b.scale, out=out, lse=lse)
+        assert got.data_ptr() == out.data_ptr()
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == alloc0
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert pkv.get_device_error() == 0
+    assert _close(out, ref) and _close(lse, ref_lse)
