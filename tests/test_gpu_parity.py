@@ -501,9 +501,11 @@ def test_shared_prefix_full_size():
     _shared_prefix_run(sp)
 
 
-@pytest.mark.parametrize("split_len", [0, 128, 384])
+@pytest.mark.parametrize("split_len", [0, 128, 384, 768, 896])
 def test_prefix_states_per_split(split_len):
-    """Each split's state equals the oracle's attention over that split's keys."""
+    """Each split's state equals the oracle's attention over that split's keys
+    (splits of one to seven 128-key tiles; at 896 the one split is longer
+    than the 768-key prefix)."""
     sp = wl.shared_prefix_batch(device="cuda", batch=20, prefix_len=768, shared_tail=0,
                                 suffix_lo=1, suffix_hi=20, seed=95)
     shape = (sp.num_blocks, sp.block_size, sp.num_kv_heads, sp.head_dim)
