@@ -23,7 +23,8 @@
 //     directly and leaves one (O, LSE) record per cut piece, and the same
 //     reduction kernel merges them;
 //   * warp 0 streams each stage's K and V boxes by TMA (128-byte swizzle,
-//     the canonical layouts the MMA descriptors expect; one box per lane)
+//     row-group tiles of launch.h: one box brings a whole block, or a
+//     128-row slice of a larger one, both column halves; one box per lane)
 //     and a piece's Q rows at its first stage; warp 1 issues the MMAs; warps
 //     2-5 own one key row (S^T lane) and one head_dim row (O^T lane) each and
 //     run the online softmax: per-head maxima across the 128 keys by warp
@@ -52,7 +53,7 @@ constexpr int kTcD = 128;                     // head_dim = the PV MMA's M
 constexpr int kTcStages = 3;
 constexpr int kTcThreads = 6 * 32;            // producer, MMA, four softmax warps
 constexpr int kTcTile = kTcRows * kTcD * 2;   // 32 KiB: one K (or V) tile
-constexpr int kTcHalf = kTcRows * 128;        // 16 KiB: 64 columns of a tile
+constexpr int kTcGroup = kRowGroup * kTcD * 2;  // 2 KiB: one 8-row group, both halves
 constexpr int kQBytes = kTcN * kTcD * 2;      // 4 KiB: Q (or P^T) as 16 rows x 128
 constexpr int kQHalf = kTcN * 128;            // 2 KiB: 64 columns of it
 // Q buffers, one per piece in turn.  A piece's Q is loaded with its first
@@ -137,8 +138,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ============================================================ producer
     // Walks the CTA's stages (r, h, i) = (sequence, kv head, stage in the
     // segment).  A stage is nbk blocks (or a 128-row slice of a larger one)
-    // x 2 column halves of TMA boxes per tensor: lanes 0..15 issue K boxes,
-    // lanes 16..31 V boxes, each fetching its own block id.
+    // of TMA boxes per tensor, both column halves in each: lanes 0..7 issue
+    // K boxes, lanes 16..23 V boxes, each fetching its own block id.
     if (lane == 0) {
       prefetch_tensormap(&tmk);
       prefetch_tensormap(&tmv);
@@ -163,8 +164,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // table read then overlaps the wait for a free slot
     const int j = lane & 15;
     auto box_block = [&](int r_, int i_, int len_) -> int {
-      const int row = i_ * kTcRows + (j >> 1) * TB;
-      return row < len_ && (j >> 1) * TB < kTcRows
+      const int row = i_ * kTcRows + j * TB;
+      return row < len_ && j * TB < kTcRows
                  ? __ldg(a.block_tables + (int64_t)r_ * a.max_blocks + row / P)
                  : 0;
     };
@@ -191,8 +192,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int flags = (start ? kStart : 0) | (end ? kEnd : 0) |
                         (end && i == nt - 1 && dseg >= 0 ? kWholeSeg : 0) |
                         (dseg > 0 ? kSlotOne : 0) | (qb << 4);
-      const int nbox = 2 * ((nvalid + TB - 1) / TB);  // per tensor
-      int brow = (t0 + (j >> 1) * TB) % P;
+      const int nbox = (nvalid + TB - 1) / TB;  // per tensor
+      int brow = (t0 + j * TB) % P;
       const bool bad = j < nbox && (blk < 0 || (int64_t)blk >= a.num_blocks);
       if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.err, PKV_DEVERR_BLOCK);
       if (bad) {
@@ -202,13 +203,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) {
         sdesc[s] = make_int4(r, h, nvalid, flags);
         mbar_arrive_expect_tx(&full[s],
-                              (uint32_t)(2 * nbox * TB * 128 + (start ? 2 * G * 128 : 0)));
+                              (uint32_t)(2 * nbox * TB * kTcD * 2 + (start ? 2 * G * 128 : 0)));
       }
       __syncwarp();
       if (j < nbox)
-        tma_load_4d(ring + (size_t)s * 2 * kTcTile + (lane < 16 ? 0 : kTcTile) + (j & 1) * kTcHalf +
-                        (j >> 1) * TB * 128,
-                    lane < 16 ? &tmk : &tmv, (j & 1) * 64, h, brow, blk, &full[s]);
+        tma_load_5d(ring + (size_t)s * 2 * kTcTile + (lane < 16 ? 0 : kTcTile) + j * TB * kTcD * 2,
+                    lane < 16 ? &tmk : &tmv, 0, 0, 0, h,
+                    (int)((int64_t)blk * (P / kRowGroup) + brow / kRowGroup), &full[s]);
       if (start && lane == 0) {
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf)
@@ -249,8 +250,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const uint32_t pb = smem_u32(pt + term * kQBytes);
 #pragma unroll
           for (int kk = 0; kk < kTcRows / 16; ++kk) {
-            // V MN-major: 64-column d chunks kTcHalf apart, 8-key groups 1 KiB apart
-            const uint64_t ad = tc::smem_desc_sw128(vb + kk * 2048, kTcHalf, 1024);
+            // V MN-major: 64-column d chunks 1 KiB apart, 8-key groups 2 KiB apart
+            const uint64_t ad = tc::smem_desc_sw128(vb + kk * 2 * kTcGroup, 1024, kTcGroup);
             const uint64_t bd =
                 tc::smem_desc_sw128(pb + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
             tc::mma_bf16(tmem + 32, ad, bd, kIdPV,
@@ -275,7 +276,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t qb = smem_u32(qs + ((fl >> 4) & 3) * kQBytes);
 #pragma unroll
         for (int kk = 0; kk < kTcD / 16; ++kk) {
-          const uint64_t ad = tc::smem_desc_sw128(kb + (kk >> 2) * kTcHalf + (kk & 3) * 32, 16, 1024);
+          const uint64_t ad =
+              tc::smem_desc_sw128(kb + (kk >> 2) * 1024 + (kk & 3) * 32, 16, kTcGroup);
           const uint64_t bd = tc::smem_desc_sw128(qb + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
           tc::mma_bf16(tmem + 16 * b, ad, bd, kIdQK, kk > 0 ? 1u : 0u);
         }
@@ -396,12 +398,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       if (row >= nvalid) {  // zero this row of V: its weight is 0, its bytes may be NaN
-        unsigned char* vrow = ring + (size_t)s * 2 * kTcTile + kTcTile + row * 128;
+        unsigned char* vrow = ring + (size_t)s * 2 * kTcTile + kTcTile +
+                              (row / kRowGroup) * kTcGroup + (row % kRowGroup) * 128;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch)
-            *reinterpret_cast<uint4*>(vrow + hf * kTcHalf + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(vrow + hf * 1024 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
       }
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();

@@ -134,8 +134,8 @@ cudaError_t launch_decode_reduce(int dtype, int head_dim, const DecodeArgs& args
 
 // Tensor-core decode for eight query heads per kv head (decode_tc.cu): bf16,
 // head_dim 128, block sizes dividing 128 or multiples of it.  Stages are
-// decode_tc_rows() rows; one CTA per SM.  tmk / tmv: 128-byte-swizzled maps
-// whose box is 64 columns x 1 head x min(P, 128) rows x 1 block; tmq: a
+// decode_tc_rows() rows; one CTA per SM.  tmk / tmv: row-group maps (above)
+// whose box is min(P, 128) rows of one head, both halves; tmq: a
 // 128-byte-swizzled map over q [B, Hq, D] whose box is 64 columns x 8 heads
 // x 1 request.  Launches the reduction too.
 bool decode_tc_supported(int dtype, int head_dim, int group, int block_size);
@@ -206,6 +206,17 @@ struct TreeMergeArgs {
 };
 cudaError_t launch_tree_merge(int dtype, int head_dim, const TreeMergeArgs& args,
                               cudaStream_t stream);
+
+// Row-group tiles.  The tensor-core kernels stage K and V tiles of bf16 rows
+// with the 128-byte swizzle as 8-row atoms interleaved by row group: row r,
+// 64-column half h of a tile lies at (r / 8) * (D / 64) KiB + h KiB +
+// (r % 8) * 128 B.  A TMA box then brings whole blocks, both halves at once
+// (a 16-row block of head_dim 128 is one 4 KiB box instead of two 2 KiB
+// ones): the map is 5-D over the pool, (64 columns, 8 rows, D / 64 halves,
+// Hkv, NB * P / 8 row groups), and a block's box starts at row group
+// block * P / 8 + first row / 8.  K-major operands read it with 8-row groups
+// (D / 64) KiB apart; MN-major ones with 64-element halves 1 KiB apart.
+constexpr int kRowGroup = 8;
 
 // Query rows per CTA and keys per tile of the prefix kernel.
 constexpr int kPrefixRows = 128;

@@ -13,15 +13,17 @@
 // Design (GB300):
 //   * CTA = (key split, two 128-row query tiles A and B, kv head).  Both
 //     tiles use every K/V tile the CTA stages: the prefix blocks arrive as
-//     2 KiB TMA boxes (16 rows x 64 columns), and the TMA engine, not the
-//     tensor pipe, bounds a one-tile CTA, so each staged byte feeds two
+//     one TMA box each (a 16-row block of head_dim 128 is 4 KiB, both column
+//     halves, in the row-group tiles of launch.h), and the TMA engine, not
+//     the tensor pipe, bounds a one-tile CTA, so each staged byte feeds two
 //     128 x 128 x D MMAs;
 //   * thread t of a softmax warpgroup owns query row t of its tile, i.e. TMEM
 //     lane t, so the softmax needs no cross-thread reduction;
 //   * Q (128 rows x D per tile), K and V tiles (128 keys x D) arrive by TMA
-//     with 128-byte swizzle, directly in the canonical K-major layout the
-//     UMMA descriptors expect; each producer lane issues one box; keys past
-//     the prefix read a zero-filled out-of-range box;
+//     with 128-byte swizzle, directly in layouts the UMMA descriptors read
+//     (Q in 64-column halves, K and V in row groups); each producer lane
+//     issues one box; keys past the prefix read a zero-filled out-of-range
+//     box;
 //   * warp roles: warps 0-3 softmax of tile A, warps 4-7 softmax of tile B,
 //     warp 8 issues the MMAs, warp 9 streams K and V in the order the MMAs
 //     need them (K0, V0, K1, V1, ...: the TMA engine serves boxes in issue
@@ -127,12 +129,13 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
   __shared__ uint32_t tmem_base;
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  // The producer's block ids: lane l issues box l of every tile (block l / H,
-  // column half l % H), K and V alike; the ids of tiles 0 and 1 are requested
-  // before the set-up so their latency overlaps it.
+  // The producer's block ids: lane l issues box l of every tile (block l,
+  // both column halves), K and V alike; the ids of tiles 0 and 1 are
+  // requested before the set-up so their latency overlaps it.
   const int PB = P < kPrefixKeys ? P : kPrefixKeys;
-  const int nbox = (kPrefixKeys / PB) * H;
-  const int bsub = lane / H, hcol = lane % H;
+  const int nbox = kPrefixKeys / PB;
+  const int bsub = lane;
+  constexpr int kGroupBytes = kRowGroup * H * 128;  // one 8-row group of a K/V tile
   constexpr int kZeroFill = INT_MIN;  // no key here: read a zero-filled out-of-range box
   auto box_block = [&](int jt) -> int2 {  // (block, first row) of this lane's box of tile jt
     const int key = key0 + jt * kPrefixKeys + bsub * PB;
@@ -178,8 +181,8 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
   if (warp == 9) {
     // ============================================================ producer
     // K and V tiles in the order the MMAs consume them.  A tile is
-    // kPrefixKeys / PB blocks x H column halves of TMA boxes (PB rows x 128 B
-    // each), lane l issuing box l.  A stage is refilled as soon as the MMAs
+    // kPrefixKeys / PB TMA boxes (PB rows of both column halves each), lane
+    // l issuing box l.  A stage is refilled as soon as the MMAs
     // that read it have completed; keys past the split, and bad block ids
     // (reported), read a zero-filled out-of-range box.
     if (lane == 0) {
@@ -208,8 +211,9 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
         if (lane == 0) mbar_arrive_expect_tx(&fullb[st], kTile);
         __syncwarp();
         if (lane < nbox)
-          tma_load_4d((kv ? vs : ks) + st * kTile + hcol * kHalfBytes + bsub * PB * 128,
-                      kv ? &tmv : &tmk, hcol * 64, kvh, row, blk, &fullb[st]);
+          tma_load_5d((kv ? vs : ks) + st * kTile + bsub * PB * H * 128, kv ? &tmv : &tmk, 0, 0,
+                      0, kvh, (int)((int64_t)blk * (P / kRowGroup) + row / kRowGroup),
+                      &fullb[st]);
         if (jt == 0 && kv == 0 && hasB && lane == 0) {  // tile B's Q, after the first K tile
           mbar_arrive_expect_tx(&qbar[1], kTile);
 #pragma unroll
@@ -233,9 +237,11 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
         const uint32_t kb = smem_u32(ks + (jt & 1) * kTile), qb = smem_u32(qs + x * kTile);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-          tc::mma_bf16(tmem + x * 128, tc::smem_desc_sw128(qb + off, 16, 1024),
-                       tc::smem_desc_sw128(kb + off, 16, 1024), kIdQK, k > 0 ? 1u : 0u);
+          // Q in 64-column halves (8-row groups 1 KiB apart), K in row groups
+          tc::mma_bf16(tmem + x * 128,
+                       tc::smem_desc_sw128(qb + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024),
+                       tc::smem_desc_sw128(kb + (k >> 2) * 1024 + (k & 3) * 32, 16, kGroupBytes),
+                       kIdQK, k > 0 ? 1u : 0u);
         }
         tc::commit(&sfull[x]);
         if (x == 1 || !hasB) tc::commit(&kfree[jt & 1]);
@@ -250,8 +256,8 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
         for (int k = 0; k < kPrefixKeys / 16; ++k) {
           const uint64_t ad =
               tc::smem_desc_sw128(pb + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
-          // V is MN-major: 64-column d chunks kHalfBytes apart, 8-key groups 1 KiB apart
-          const uint64_t bd = tc::smem_desc_sw128(vb + k * 2048, kHalfBytes, 1024);
+          // V is MN-major: 64-column d chunks 1 KiB apart, 8-key groups kGroupBytes apart
+          const uint64_t bd = tc::smem_desc_sw128(vb + k * 2 * kGroupBytes, 1024, kGroupBytes);
           tc::mma_bf16(tmem + 256 + x * 128, ad, bd, kIdPV, (jt > 0 || k > 0) ? 1u : 0u);
         }
         tc::commit(&ofull[x]);
@@ -354,7 +360,8 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
         if (row >= kvalid) {
 #pragma unroll
           for (int h = 0; h < H; ++h) {
-            uint4* vr = reinterpret_cast<uint4*>(vs + (j & 1) * kTile + h * kHalfBytes + row * 128);
+            uint4* vr = reinterpret_cast<uint4*>(vs + (j & 1) * kTile + (row / kRowGroup) * kGroupBytes +
+                                                 h * 1024 + (row % kRowGroup) * 128);
 #pragma unroll
             for (int c16 = 0; c16 < 8; ++c16) vr[c16] = make_uint4(0u, 0u, 0u, 0u);
           }

@@ -223,8 +223,8 @@ int64_t decode_ctas(const pkv_cache_desc* c, int32_t num_seqs, int32_t num_q_hea
 
 pkv_status encode_q_map_sw128(CUtensorMap* map, const void* q, int32_t num_seqs,
                               int32_t num_q_heads, int32_t head_dim, int group, int rpb);
-pkv_status encode_cache_map_sw128(CUtensorMap* map, const pkv_cache_desc* c, const void* base,
-                                  int rows);
+pkv_status encode_cache_map_rg(CUtensorMap* map, const pkv_cache_desc* c, const void* base,
+                               int rows);
 
 // Encode the maps and launch the decode (partial kernel + reduction) on the
 // path use_tc_decode picks.
@@ -263,8 +263,8 @@ pkv_status launch_decode(const pkv_cache_desc* cache, int G, const void* q, cons
       e = pkv::launch_paged_decode_tc_mx(G, tmk, tmv, tmq, a, stream);
       return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
     }
-    if ((st = encode_cache_map_sw128(&tmk, cache, k_cache, rows)) != PKV_OK) return st;
-    if ((st = encode_cache_map_sw128(&tmv, cache, v_cache, rows)) != PKV_OK) return st;
+    if ((st = encode_cache_map_rg(&tmk, cache, k_cache, rows)) != PKV_OK) return st;
+    if ((st = encode_cache_map_rg(&tmv, cache, v_cache, rows)) != PKV_OK) return st;
     if ((st = encode_q_map_sw128(&tmq, q, q_seqs > 0 ? q_seqs : a.num_seqs, a.num_q_heads,
                                  cache->head_dim, G, 1)) !=
         PKV_OK)
@@ -318,26 +318,35 @@ pkv_status encode_q_map_sw128(CUtensorMap* map, const void* q, int32_t num_seqs,
   return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_UNSUPPORTED;
 }
 
-// 4-D map over a bf16 pool with 128-byte swizzle; box = 64 columns x 1 head x
-// `rows` token rows x 1 block.
-pkv_status encode_cache_map_sw128(CUtensorMap* map, const pkv_cache_desc* c, const void* base,
-                                  int rows) {
-  cuuint64_t dims[4] = {(cuuint64_t)c->head_dim, (cuuint64_t)c->num_kv_heads,
-                        (cuuint64_t)c->block_size, (cuuint64_t)c->num_blocks};
-  cuuint64_t strides[3] = {dims[0] * 2, dims[0] * dims[1] * 2, dims[0] * dims[1] * dims[2] * 2};
-  cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
-  CUresult r = encode_tiled_cached(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base),
+// Row-group map over a bf16 pool (kernels/launch.h): 5-D (64 columns, 8
+// rows, D / 64 halves, Hkv, NB * P / 8 row groups) with 128-byte swizzle;
+// box = `rows` token rows (a multiple of 8) of one head, every half.
+pkv_status encode_cache_map_rg(CUtensorMap* map, const pkv_cache_desc* c, const void* base,
+                               int rows) {
+  const cuuint64_t row_bytes = (cuuint64_t)c->num_kv_heads * c->head_dim * 2;
+  const int rg = pkv::kRowGroup;
+  // the kernels address row groups with int32 coordinates
+  if ((int64_t)c->num_blocks * (c->block_size / rg) > INT32_MAX || c->block_size % rg != 0)
+    return PKV_ERR_UNSUPPORTED;
+  cuuint64_t dims[5] = {64, (cuuint64_t)rg, (cuuint64_t)(c->head_dim / 64),
+                        (cuuint64_t)c->num_kv_heads,
+                        (cuuint64_t)c->num_blocks * (cuuint64_t)(c->block_size / rg)};
+  cuuint64_t strides[4] = {row_bytes, 128, (cuuint64_t)c->head_dim * 2, row_bytes * rg};
+  cuuint32_t box[5] = {64, (cuuint32_t)rg, (cuuint32_t)(c->head_dim / 64), 1,
+                       (cuuint32_t)(rows / rg)};
+  CUresult r = encode_tiled_cached(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base),
                                    dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
   if (r == CUDA_ERROR_NOT_INITIALIZED) return PKV_ERR_CUDA;
   return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_UNSUPPORTED;
 }
 
+
 // Prefix K/V maps: one box is one block (or 128 rows of a larger one).
 pkv_status encode_prefix_maps(CUtensorMap* tmk, CUtensorMap* tmv, const pkv_cache_desc* c,
                               const void* k_cache, const void* v_cache) {
   const int rows = c->block_size < pkv::kPrefixKeys ? c->block_size : pkv::kPrefixKeys;
-  pkv_status st = encode_cache_map_sw128(tmk, c, k_cache, rows);
-  return st != PKV_OK ? st : encode_cache_map_sw128(tmv, c, v_cache, rows);
+  pkv_status st = encode_cache_map_rg(tmk, c, k_cache, rows);
+  return st != PKV_OK ? st : encode_cache_map_rg(tmv, c, v_cache, rows);
 }
 
 // Prefix state outputs [B, Hq, parts_stride, D] fp32 as the 5-D tensor
