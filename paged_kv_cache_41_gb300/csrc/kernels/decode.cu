@@ -308,6 +308,47 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
       for (int j = 0; j < EP2; ++j) q2[g][j] = make_float2(f[2 * j] * a.qscale, f[2 * j + 1] * a.qscale);
     }
   };
+  // The same in two halves, for a piece end: the raw loads are issued before
+  // the merge (from q row qr, the descriptor's) and widened after it, so the
+  // merge covers their latency.  The raw words wait in q2's own registers
+  // (bf16: in the upper half of each head's q2; fp32: the values themselves),
+  // so the hot loop loses no registers to them.
+  auto load_q_raw = [&](int64_t qr, int h) {
+    const TQ* qp = static_cast<const TQ*>(a.q) + (qr * a.num_q_heads + (int64_t)h * G) * D + l16 * EPL;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      if constexpr (sizeof(TQ) == 4) {
+#pragma unroll
+        for (int j = 0; j < EP2; ++j) q2[g][j] = __ldg(reinterpret_cast<const float2*>(qp + g * D) + j);
+      } else {
+#pragma unroll
+        for (int i = 0; i < EPL / 4; ++i) {
+          const uint2 x = __ldg(reinterpret_cast<const uint2*>(qp + g * D) + i);
+          q2[g][EP2 / 2 + i] = make_float2(__uint_as_float(x.x), __uint_as_float(x.y));
+        }
+      }
+    }
+  };
+  auto finish_q = [&]() {
+    const float2 s2 = make_float2(a.qscale, a.qscale);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      if constexpr (sizeof(TQ) == 4) {
+#pragma unroll
+        for (int j = 0; j < EP2; ++j) q2[g][j] = __fmul2_rn(q2[g][j], s2);
+      } else {
+        uint32_t wv[EP2];  // the EPL bf16 as EP2 words
+#pragma unroll
+        for (int i = 0; i < EPL / 4; ++i) {
+          wv[2 * i] = __float_as_uint(q2[g][EP2 / 2 + i].x);
+          wv[2 * i + 1] = __float_as_uint(q2[g][EP2 / 2 + i].y);
+        }
+#pragma unroll
+        for (int j = 0; j < EP2; ++j)
+          q2[g][j] = make_float2(bf16lo(wv[j]) * a.qscale, bf16hi(wv[j]) * a.qscale);
+      }
+    }
+  };
   const bool d0_exact = a.stage_units == 1 && a.piece_units == 0;
   if (d0_exact) load_q(d0.x, d0.y);
 
@@ -361,7 +402,9 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
         prefetch_l2_bulk(static_cast<const TQ*>(a.q) + (qr * a.num_q_heads + (int64_t)h * G) * D,
                          (uint32_t)(G * D * sizeof(TQ)));
       }
-      dA[k & 63] = make_int4(id0, id1, row0 - b0 * P, nbox);
+      // the piece's q row rides in the box-count word (nbox is 1 or 2)
+      const int qrow = a.q_rows ? __ldg(a.q_rows + r) : r;
+      dA[k & 63] = make_int4(id0, id1, row0 - b0 * P, nbox | (qrow << 2));
       dB[k & 63] = make_int4(r, h, nvalid, flags);
     }
     // the cursor moves to the stage after lane 31's
@@ -376,10 +419,14 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
   auto issue_stage = [&](int st, int k) {
     const int4 da = dA[k & 63];
     const int4 db = dB[k & 63];
-    const int nbox = da.w;
+    const int nbox = da.w & 3;
     const bool valid = da.x >= 0 && (int64_t)da.x < a.num_blocks &&
                        (nbox < 2 || (da.y >= 0 && (int64_t)da.y < a.num_blocks));
     if (lane == 0) sdesc[st] = db;
+    if ((db.w & kPieceStart) && lane == 31)  // refresh the piece's q in L2 shortly before use
+      prefetch_l2_bulk(static_cast<const TQ*>(a.q) +
+                           ((int64_t)(da.w >> 2) * a.num_q_heads + (int64_t)db.y * G) * D,
+                       (uint32_t)(G * D * sizeof(TQ)));
     if (!valid) {
       if (lane == 0) {
         atomicOr(a.err, PKV_DEVERR_BLOCK);
@@ -489,13 +536,12 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
       }
     }
     if (flags & kPieceEnd) {
-      // The next stage starts the next piece: fetch its q now (this piece's
-      // is no longer needed).  Its descriptor was written before this
+      // The next stage starts the next piece: issue its q loads now (this
+      // piece's is no longer needed) and widen them after the merge, which
+      // covers their latency.  Its descriptor was written before this
       // stage's was published (the same batch, or an earlier one).
-      if (k + 1 < n) {
-        const int4 nd = dB[(k + 1) & 63];
-        load_q(nd.x, nd.y);
-      }
+      const bool next_q = k + 1 < n;
+      if (next_q) load_q_raw(dA[(k + 1) & 63].w >> 2, dB[(k + 1) & 63].y);
       // ---- merge the four warps through this stage's tile, then write
       if (!merge_sync()) break;  // every warp is done with the tile
       float* macc = reinterpret_cast<float*>(const_cast<T*>(kt));  // [4][G][D]
@@ -551,6 +597,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
           if (e == 0 && a.lse_out) a.lse_out[rh] = lse2 * kLn2;
         }
       }
+      if (next_q) finish_q();
       // No barrier here: each warp releases the tile below once its own merge
       // reads are done, and the producer refills it only after all four have;
       // mm / ml are rewritten only after the next piece's first barrier.

@@ -10,6 +10,8 @@ workspace, within the attention tolerance |a - b| <= 2e-3 + 1e-2 |b|.  It also
 checks that sizes beyond the array are refused.  The file is named to be
 collected last.
 """
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -95,13 +97,22 @@ def test_static_calls_allocate_no_device_memory():
     ref = pkv.paged_attention_decode(b.q, kc, vc, bt, sl, b.scale, lse=ref_lse)
     pkv.paged_attention_decode_static(b.q, kc, vc, bt, sl, b.scale, out=out, lse=lse)
     torch.cuda.synchronize()
-    alloc0 = torch.cuda.memory_allocated()
-    free0, _ = torch.cuda.mem_get_info()
-    for _ in range(5):
-        got = pkv.paged_attention_decode_static(b.q, kc, vc, bt, sl, b.scale, out=out, lse=lse)
-        assert got.data_ptr() == out.data_ptr()
-    torch.cuda.synchronize()
-    assert torch.cuda.memory_allocated() == alloc0
-    assert torch.cuda.mem_get_info()[0] == free0
+    # tensors of earlier tests must not be freed by the garbage collector
+    # inside the measured calls: that would move the counts the other way
+    gc.collect()
+    gc.disable()
+    try:
+        alloc0 = torch.cuda.memory_allocated()
+        free0, _ = torch.cuda.mem_get_info()
+        for _ in range(5):
+            got = pkv.paged_attention_decode_static(b.q, kc, vc, bt, sl, b.scale, out=out, lse=lse)
+            assert got.data_ptr() == out.data_ptr()
+        torch.cuda.synchronize()
+        alloc1 = torch.cuda.memory_allocated()
+        free1, _ = torch.cuda.mem_get_info()
+    finally:
+        gc.enable()
+    assert alloc1 == alloc0
+    assert free1 == free0
     assert pkv.get_device_error() == 0
     assert _close(out, ref) and _close(lse, ref_lse)
