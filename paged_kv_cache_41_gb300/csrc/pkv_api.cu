@@ -236,19 +236,21 @@ pkv_status launch_decode(const pkv_cache_desc* cache, int G, const void* q, cons
   cudaError_t e;
   pkv::DecodeArgs a = args;
   // Work units of the split (kernels/plan.cuh).  A piece's fixed cost (its
-  // q, merge and record) is about half a 32-row stage of the CUDA-core
-  // decode, so there a piece weighs one unit and a stage two.  Where
-  // segments are short this decides the balance; where they are long it
-  // costs nothing (measured: the churn trace 4,960 -> 5,030 GB/s, the
-  // Llama-shaped layer unchanged).  The tensor-core decode's 128-row stages
-  // dwarf a piece.
+  // q, the merge of the four warps and its record) is about one and a half
+  // 32-row stages of the CUDA-core decode, so there a piece weighs three
+  // units and a stage two.  Where segments are short this decides the
+  // balance; where they are long it costs nothing.  Measured against equal
+  // stage shares: churn trace 4,960 -> 5,080 GB/s, shared-prefix call
+  // 69 -> 65.5 us, prefix-tree call 77 -> 72 us, the long-context decode
+  // unchanged; a piece worth 1/4, 1/3, 1/2, 3/4, 1 or 2 stages measured no
+  // better overall.  The tensor-core decode's 128-row stages dwarf a piece.
   const bool tc = use_tc_decode(cache, G);
   if (cache->dtype == PKV_MXFP8) {  // the scale planes follow the element planes
     a.k_scales = static_cast<const uint8_t*>(k_cache) + mx_plane_bytes(cache);
     a.v_scales = static_cast<const uint8_t*>(v_cache) + mx_plane_bytes(cache);
   }
   a.stage_units = tc ? 1 : 2;
-  a.piece_units = tc ? 0 : 1;
+  a.piece_units = tc ? 0 : 3;
   if (tc) {
     const int rows = cache->block_size < pkv::decode_tc_rows() ? cache->block_size
                                                                : pkv::decode_tc_rows();
