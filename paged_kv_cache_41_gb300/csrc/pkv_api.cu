@@ -216,7 +216,9 @@ int64_t decode_ctas(const pkv_cache_desc* c, int32_t num_seqs, int32_t num_q_hea
     const int64_t need = (smax + cap - 1) / cap;
     if (need > C) C = need;
   }
-  const int64_t fit = (3 * smax + (1LL << 30) - 1) >> 30;  // work units per CTA fit an int
+  // work units per CTA fit an int: at most 2 per stage plus 3 per piece,
+  // 5 per stage when every segment is one stage
+  const int64_t fit = (5 * smax + (1LL << 30) - 1) >> 30;
   if (fit > C) C = fit;
   return C < 1 ? 1 : C;
 }
