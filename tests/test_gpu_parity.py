@@ -476,6 +476,19 @@ def test_shared_prefix_small(batch, prefix, hq, hkv, d):
     _shared_prefix_run(sp)
 
 
+@pytest.mark.parametrize("batch,prefix,hq,hkv,d,p", [
+    (20, 256, 32, 8, 128, 32), (12, 512, 16, 4, 64, 64), (9, 512, 32, 8, 128, 128),
+    (7, 512, 16, 2, 128, 256),
+])
+def test_shared_prefix_block_sizes(batch, prefix, hq, hkv, d, p):
+    # the prefix kernel's 8-row-group boxes over blocks of 32 to 256 rows
+    # (one box per block, or per 128-row slice of a larger one)
+    sp = wl.shared_prefix_batch(device="cuda", batch=batch, prefix_len=prefix, shared_tail=8,
+                                suffix_lo=8, suffix_hi=300, hq=hq, hkv=hkv, d=d, p=p,
+                                seed=300 + batch + p)
+    _shared_prefix_run(sp)
+
+
 @pytest.mark.parametrize("hq", [32, 64])  # 64 / 8: the suffixes decode on the tensor cores
 def test_shared_prefix_pool_past_2_31_elements(hq):
     """Every block the batch uses lies past element 2^31 of the pool: the
