@@ -152,6 +152,9 @@ int decode_num_stages(int head_dim, int elem_bytes) {
 // lanes that read 2G
 // consecutive partials each and combine with 8/G - 1 shuffles.  Lane l16 ends
 // up holding value j = l16 / (8/G): row tk = l16 >> 3, head g = j % G.
+//
+// l_run is this lane's share of its head's softmax sum: the weights of its
+// own rows (one per chunk); the piece end adds the four row lanes' shares.
 template <typename T, int D, int G, bool kTail>
 __device__ __forceinline__ void decode_chunk(const T* __restrict__ kt, const T* __restrict__ vt,
                                              const uint8_t* __restrict__ ksc,
@@ -164,16 +167,13 @@ __device__ __forceinline__ void decode_chunk(const T* __restrict__ kt, const T* 
   constexpr int NV = 2 * G;    // values per half-warp and chunk
   constexpr int LPV = 16 / NV; // lanes summing one value
   // MXFP8: this lane's EPL elements lie in one 32-element scale group; its
-  // K scale multiplies the lane's partial dot product, its V scale the
-  // weights (both powers of two)
-  float kscale[2] = {1.f, 1.f}, vscale[2] = {1.f, 1.f};
+  // V scale multiplies the weights (a power of two).  The K scales are
+  // applied in the cross-lane sum, once per group of partials.
+  float vscale[2] = {1.f, 1.f};
   if constexpr (kIsMx<T>) {
     const int grp = l16 * EPL / 32;
 #pragma unroll
-    for (int tk = 0; tk < 2; ++tk) {
-      kscale[tk] = e8m0_value(ksc[(row0 + tk) * (D / 32) + grp]);
-      vscale[tk] = e8m0_value(vsc[(row0 + tk) * (D / 32) + grp]);
-    }
+    for (int tk = 0; tk < 2; ++tk) vscale[tk] = e8m0_value(vsc[(row0 + tk) * (D / 32) + grp]);
   }
   // ---- q . k partial sums for rows row0, row0 + 1 and the G heads
   float v[NV];
@@ -186,7 +186,7 @@ __device__ __forceinline__ void decode_chunk(const T* __restrict__ kt, const T* 
       float2 d2 = __fmul2_rn(q2[g][0], make_float2(kf[0], kf[1]));
 #pragma unroll
       for (int j = 1; j < EP2; ++j) d2 = __ffma2_rn(q2[g][j], make_float2(kf[2 * j], kf[2 * j + 1]), d2);
-      v[tk * G + g] = kIsMx<T> ? (d2.x + d2.y) * kscale[tk] : d2.x + d2.y;
+      v[tk * G + g] = d2.x + d2.y;
     }
   }
   // ---- sum each value over the 16 lanes of the half-warp
@@ -197,26 +197,42 @@ __device__ __forceinline__ void decode_chunk(const T* __restrict__ kt, const T* 
   float part[NV];
   VecLoad<float, NV>::run(red + red_row<G, kIsMx<T>>(hw, j) + sub * NV, part);
   __syncwarp();  // the next chunk rewrites red
-  float s2 = part[0];
+  float s2;
+  if constexpr (kIsMx<T>) {
+    // the NV partials span NG scale groups of the row of value j: sum each
+    // group's partials, then scale it by that group's K scale
+    constexpr int NG = NV * EPL >= 64 ? NV * EPL / 32 : 1;
+    constexpr int PPG = NV / NG;  // partials per group
+    const int rowj = row0 + j / G;
+    s2 = 0.f;
 #pragma unroll
-  for (int k = 1; k < NV; ++k) s2 += part[k];
+    for (int q = 0; q < NG; ++q) {
+      float gs = part[q * PPG];
+#pragma unroll
+      for (int k = 1; k < PPG; ++k) gs += part[q * PPG + k];
+      const int grp = (sub * NV + q * PPG) * EPL / 32;
+      s2 = fmaf(gs, e8m0_value(ksc[rowj * (D / 32) + grp]), s2);
+    }
+  } else {
+    s2 = part[0];
+#pragma unroll
+    for (int k = 1; k < NV; ++k) s2 += part[k];
+  }
 #pragma unroll
   for (int o = LPV / 2; o >= 1; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
   // ---- online softmax over the warp's 4 rows (rows differ in lane bits 3, 4)
   const float sc = (!kTail || row0 + (l16 >> 3) < nvalid) ? s2 : -INFINITY;
-  float cmax = fmaxf(sc, __shfl_xor_sync(0xffffffffu, sc, 8));
-  cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 16));
-  const float m_new = fmaxf(m_used, cmax);
-  const bool need = m_new > m_used + kRescaleLog2;
-  const bool any = __any_sync(0xffffffffu, need);
-  const float alpha = need ? exp2f(m_used - m_new) : 1.f;
-  m_used = need ? m_new : m_used;
-  l_run *= alpha;
-  const float p = (kTail && sc == -INFINITY) ? 0.f : exp2f(sc - m_used);
-  float psum = p + __shfl_xor_sync(0xffffffffu, p, 8);
-  psum += __shfl_xor_sync(0xffffffffu, psum, 16);
-  l_run += psum;
-  if (any) {
+  // The exponent base of a head moves only when one of its scores passes it
+  // by more than 2^8 (m_used = -inf before a piece's first row), so most
+  // chunks need neither the cross-row max nor a rescale.
+  if (__any_sync(0xffffffffu, sc > m_used + kRescaleLog2)) {
+    float cmax = fmaxf(sc, __shfl_xor_sync(0xffffffffu, sc, 8));
+    cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 16));
+    const float m_new = fmaxf(m_used, cmax);
+    const bool need = m_new > m_used + kRescaleLog2;
+    const float alpha = need ? exp2f(m_used - m_new) : 1.f;
+    m_used = need ? m_new : m_used;
+    l_run *= alpha;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       const float al = __shfl_sync(0xffffffffu, alpha, g * LPV, 16);
@@ -225,6 +241,8 @@ __device__ __forceinline__ void decode_chunk(const T* __restrict__ kt, const T* 
       for (int e = 0; e < EP2; ++e) acc[g][e] = __fmul2_rn(acc[g][e], al2);
     }
   }
+  const float p = (kTail && sc == -INFINITY) ? 0.f : exp2f(sc - m_used);
+  l_run += p;
   // ---- P . V for this half-warp's two rows
   float pg[2][G];
 #pragma unroll
@@ -489,7 +507,8 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
 
   // ------------------------------------------------------------------ consumers
   if (!d0_exact) load_q(dB[0].x, dB[0].y);
-  // (m_used, l_run): softmax state of head (l16 / (8 / G)) % G of this lane.
+  // (m_used, l_run): softmax state of head (l16 / (8 / G)) % G of this lane
+  // (l_run: the weights of this lane's own rows).
   float m_used = -INFINITY, l_run = 0.f;
   float* red = scratch + warp * red_warp_floats(G, (int)sizeof(T));
   const int rbase = warp * 4 + hw * 2;
@@ -560,9 +579,11 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
           }
         }
       constexpr int LPV = 8 / G;  // lanes per (row, head) value
+      float lsum = l_run + __shfl_xor_sync(0xffffffffu, l_run, 8);  // the warp's four rows
+      lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);
       if (lane < 8 && lane % LPV == 0) {  // row 0 of half-warp 0, first lane of each head
         mm[warp * G + lane / LPV] = m_used;
-        ml[warp * G + lane / LPV] = l_run;
+        ml[warp * G + lane / LPV] = lsum;
       }
       if (!merge_sync()) break;
       const int64_t rh0 = (int64_t)dsc.x * a.num_q_heads + (int64_t)dsc.y * G;
