@@ -81,11 +81,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   static_assert(G <= kTcN, "at most 16 query heads per kv head");
   constexpr uint32_t kIdQK = tc::idesc_bf16_f32(kTcRows, kTcN, 0, 0);
   constexpr uint32_t kIdPV = tc::idesc_bf16_f32(kTcD, kTcN, 1, 0);
-  // full/kvfree: a stage's K, V (and Q) landed / its PV completed; sfull/sfree:
-  // S^T buffer written / read; pfull: P^T written; ofull: a PV completed;
-  // ofree: a piece's epilogue read O^T; rsync: exchange among the softmax warps.
-  __shared__ uint64_t full[kTcStages], kvfree[kTcStages], sfull[2], sfree[2], pfull, ofull, ofree,
-      rsync;
+  // kfull/kfree: a stage's K (and Q) landed / its QK completed; dfree: the
+  // softmax warps read its descriptor (so the slot's next K may go out
+  // without a softmax warp yet to wait for this phase); vfull/vfree: its V
+  // landed / its PV completed; sfull/sfree: S^T buffer written / read;
+  // pfull: P^T written; ofull: a PV completed; ofree: a piece's epilogue read
+  // O^T; rsync: exchange among the softmax warps.
+  __shared__ uint64_t kfull[kTcStages], kfree[kTcStages], dfree[kTcStages], vfull[kTcStages],
+      vfree[kTcStages], sfull[2], sfree[2], pfull, ofull, ofree, rsync;
   __shared__ int4 sdesc[kTcStages];
   __shared__ float redm[2][4][kTcN], redl[4][kTcN];
   __shared__ int4 redf[2];  // per stage parity: each softmax warp's "a score passed m + 8"
@@ -115,8 +118,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     reinterpret_cast<uint4*>(qs)[i] = make_uint4(0u, 0u, 0u, 0u);
   if (t == 0) {
     for (int s = 0; s < kTcStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&kvfree[s], 1);
+      mbar_init(&kfull[s], 1);
+      mbar_init(&kfree[s], 1);
+      mbar_init(&dfree[s], 4);
+      mbar_init(&vfull[s], 1);
+      mbar_init(&vfree[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sfull[b], 1);
@@ -134,14 +140,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;  // S^T buffers at columns 0 and 16, O^T at 32
-  int issued = 0;                   // stages whose copies warp 0 started
+  int issued_k = 0, issued_v = 0;   // stages whose K / V copies warp 0 started
 
   if (warp == 0) {
     // ============================================================ producer
     // Walks the CTA's stages (r, h, i) = (sequence, kv head, stage in the
     // segment).  A stage is nbk blocks (or a 128-row slice of a larger one)
     // of TMA boxes per tensor, both column halves in each: lanes 0..7 issue
-    // K boxes, lanes 16..23 V boxes, each fetching its own block id.
+    // K boxes, lanes 16..23 V boxes, each fetching its own block id.  K runs
+    // one stage ahead of V: a K slot is free once its QK has run, a V slot
+    // only once its PV has, so stage k's K boxes go out before stage k - 1's
+    // V boxes (and the QK and softmax of a stage overlap its V's landing).
     if (lane == 0) {
       prefetch_tensormap(&tmk);
       prefetch_tensormap(&tmv);
@@ -173,16 +182,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     };
     int blk_next = box_block(r, i, len);
     int pieces = 0;
+    // the previous stage's V boxes: this lane's block and first row, the box
+    // count and the kv head
+    int v_blk = 0, v_brow = 0, v_nbox = 0, v_h = 0;
+    auto issue_v = [&](int kv) -> bool {
+      const int sv = kv % kTcStages;
+      if (kv >= kTcStages) {
+        int ok = 1;
+        if (lane == 0 && !mbar_wait(&vfree[sv], ((kv / kTcStages) - 1) & 1)) {
+          atomicOr(a.err, PKV_DEVERR_TIMEOUT);
+          ok = 0;
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&vfull[sv], (uint32_t)(v_nbox * TB * kTcD * 2));
+      __syncwarp();
+      if (lane >= 16 && j < v_nbox)
+        tma_load_5d(ring + (size_t)sv * 2 * kTcTile + kTcTile + j * TB * kTcD * 2, &tmv, 0, 0, 0, v_h,
+                    (int)((int64_t)v_blk * (P / kRowGroup) + v_brow / kRowGroup), &vfull[sv]);
+      issued_v = kv + 1;
+      return true;
+    };
+    bool v_ok = true;
     for (int k = 0; k < n; ++k) {
       const int s = k % kTcStages;
       int blk = blk_next;
       if (k >= kTcStages) {
         int ok = 1;
-        if (lane == 0 && !mbar_wait(&kvfree[s], ((k / kTcStages) - 1) & 1)) {
+        if (lane == 0 && (!mbar_wait(&kfree[s], ((k / kTcStages) - 1) & 1) ||
+                          !mbar_wait(&dfree[s], ((k / kTcStages) - 1) & 1))) {
           atomicOr(a.err, PKV_DEVERR_TIMEOUT);
           ok = 0;
         }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          v_ok = false;
+          break;
+        }
       }
       const int t0 = i * kTcRows;
       const int nvalid = min(kTcRows, len - t0);
@@ -204,21 +239,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (lane == 0) {
         sdesc[s] = make_int4(r, h, nvalid, flags);
-        mbar_arrive_expect_tx(&full[s],
-                              (uint32_t)(2 * nbox * TB * kTcD * 2 + (start ? 2 * G * 128 : 0)));
+        mbar_arrive_expect_tx(&kfull[s], (uint32_t)(nbox * TB * kTcD * 2 + (start ? 2 * G * 128 : 0)));
       }
       __syncwarp();
-      if (j < nbox)
-        tma_load_5d(ring + (size_t)s * 2 * kTcTile + (lane < 16 ? 0 : kTcTile) + j * TB * kTcD * 2,
-                    lane < 16 ? &tmk : &tmv, 0, 0, 0, h,
-                    (int)((int64_t)blk * (P / kRowGroup) + brow / kRowGroup), &full[s]);
+      if (lane < 16 && j < nbox)
+        tma_load_5d(ring + (size_t)s * 2 * kTcTile + j * TB * kTcD * 2, &tmk, 0, 0, 0, h,
+                    (int)((int64_t)blk * (P / kRowGroup) + brow / kRowGroup), &kfull[s]);
       if (start && lane == 0) {
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf)
           tma_load_3d(qs + qb * kQBytes + hf * kQHalf, &tmq, hf * 64, h * G,
-                      a.q_rows ? __ldg(a.q_rows + r) : r, &full[s]);
+                      a.q_rows ? __ldg(a.q_rows + r) : r, &kfull[s]);
       }
-      issued = k + 1;
+      issued_k = k + 1;
+      if (k >= 1 && !issue_v(k - 1)) {
+        v_ok = false;
+        break;
+      }
+      v_blk = blk;
+      v_brow = brow;
+      v_nbox = nbox;
+      v_h = h;
       if (k + 1 < n && ++i == nt) {  // on to the next non-empty segment
         i = 0;
         if (++h == Hkv) {
@@ -232,6 +273,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (k + 1 < n) blk_next = box_block(r, i, len);
     }
+    if (v_ok) issue_v(n - 1);
   } else if (warp == 1) {
     // ============================================================ MMA issue
     // QK of stage k, then PV of stage k - 1 (whose P^T the softmax wrote
@@ -241,7 +283,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool ok = true;
       int pflags = 0, pieces_done = 0;
       auto issue_pv = [&](int j, int fl) -> bool {
-        if (!mbar_wait(&pfull, j & 1)) return false;
+        if (!mbar_wait(&pfull, j & 1) || !mbar_wait(&vfull[j % kTcStages], (j / kTcStages) & 1))
+          return false;
         if ((fl & kStart) && pieces_done > 0 && !mbar_wait(&ofree, (pieces_done - 1) & 1))
           return false;
         tc::fence_after_sync();
@@ -261,13 +304,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         tc::commit(&ofull);
-        tc::commit(&kvfree[j % kTcStages]);
+        tc::commit(&vfree[j % kTcStages]);
         if (fl & kEnd) ++pieces_done;
         return true;
       };
       for (int k = 0; k < n; ++k) {
         const int s = k % kTcStages, b = k & 1;
-        if (!mbar_wait(&full[s], (k / kTcStages) & 1) ||
+        if (!mbar_wait(&kfull[s], (k / kTcStages) & 1) ||
             (k >= 2 && !mbar_wait(&sfree[b], ((k - 2) >> 1) & 1))) {
           ok = false;
           break;
@@ -284,6 +327,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc::mma_bf16(tmem + 16 * b, ad, bd, kIdQK, kk > 0 ? 1u : 0u);
         }
         tc::commit(&sfull[b]);
+        tc::commit(&kfree[s]);
         if (k >= 1 && !issue_pv(k - 1, pflags)) {
           ok = false;
           break;
@@ -315,7 +359,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     };
     for (int k = 0; k < n; ++k) {
       const int s = k % kTcStages, b = k & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (k / kTcStages) & 1)) ||
+      if (!__all_sync(0xffffffffu, mbar_wait(&kfull[s], (k / kTcStages) & 1)) ||
           !__all_sync(0xffffffffu, mbar_wait(&sfull[b], (k >> 1) & 1))) {
         if (lane == 0) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
         break;
@@ -335,7 +379,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::wait_ld();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sfree[b]);
+      if (lane == 0) {
+        mbar_arrive(&sfree[b]);
+        mbar_arrive(&dfree[s]);  // this warp is done with the slot's descriptor
+      }
       // ---- the exponent base of a head moves only when one of its scores
       // passes it by more than 2^8 (m = -inf before a piece's first row): the
       // four warps first agree on whether any score does, and only then
@@ -417,7 +464,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           *reinterpret_cast<__nv_bfloat16*>(at + kQBytes) = lo;
         }
       }
-      if (row >= nvalid) {  // zero this row of V: its weight is 0, its bytes may be NaN
+      // zero the rows of V past the tail (weight 0, bytes maybe NaN), once
+      // the stage's V has landed
+      if (nvalid < kTcRows &&
+          !__all_sync(0xffffffffu, mbar_wait(&vfull[s], (k / kTcStages) & 1))) {
+        if (lane == 0) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
+        break;
+      }
+      if (row >= nvalid) {
         unsigned char* vrow = ring + (size_t)s * 2 * kTcTile + kTcTile +
                               (row / kRowGroup) * kTcGroup + (row % kRowGroup) * 128;
 #pragma unroll
@@ -482,8 +536,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (t == 0) {
     // if anything left early, copies may still be in flight into the ring:
     // wait for them (bounded) before the CTA's shared memory is released
-    for (int kk = issued > kTcStages ? issued - kTcStages : 0; kk < issued; ++kk)
-      mbar_wait(&full[kk % kTcStages], (kk / kTcStages) & 1);
+    for (int kk = issued_k > kTcStages ? issued_k - kTcStages : 0; kk < issued_k; ++kk)
+      mbar_wait(&kfull[kk % kTcStages], (kk / kTcStages) & 1);
+    for (int kk = issued_v > kTcStages ? issued_v - kTcStages : 0; kk < issued_v; ++kk)
+      mbar_wait(&vfull[kk % kTcStages], (kk / kTcStages) & 1);
   }
   if (warp == 0) tc::tmem_dealloc(tmem, 64);
 }

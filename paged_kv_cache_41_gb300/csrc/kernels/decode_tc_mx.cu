@@ -131,6 +131,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   // QK(k + 2), which waits for the softmax of stage k to have read its own
   __shared__ int4 sdesc_raw[kMxRaw], sdesc_bf[4];
   __shared__ float redm[2][4][kMxN], redl[4][kMxN];
+  __shared__ int4 redf[2];  // per stage parity: each softmax warp's "a score passed m + 8"
   __shared__ long long wsum[2 * (kMxThreads / 32) + 4];
   __shared__ uint32_t tmem_base;
 
@@ -445,32 +446,49 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sfree[b]);
-      float sg[G], mx[G];
+      // the four warps agree on whether any score passes its head's base
+      // by 2^8 before taking the per-head max (as in decode_tc.cu)
+      float sg[G];
+      bool pass = false;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         sg[g] = row < nvalid ? __uint_as_float(v[g]) * cs : -INFINITY;
-        mx[g] = sg[g];
+        pass |= sg[g] > m[g] + 8.0f;
       }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1)
-#pragma unroll
-        for (int g = 0; g < G; ++g) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], o));
-#pragma unroll
-      for (int g = 0; g < G; ++g)
-        if (lane == g) redm[b][q4][g] = mx[g];
+      const bool wpass = __any_sync(0xffffffffu, pass);
+      if (lane == 0) reinterpret_cast<int*>(&redf[b])[q4] = wpass ? 1 : 0;
       if (!group_sync()) break;
+      const int4 fl = redf[b];
       bool any = false;
       float alpha[G], p[G];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float mt = fmaxf(fmaxf(redm[b][0][g], redm[b][1][g]), fmaxf(redm[b][2][g], redm[b][3][g]));
-        const float mn = fmaxf(m[g], mt);
-        const bool need = mn > m[g] + 8.0f;
-        alpha[g] = need ? exp2f(m[g] - mn) : 1.f;
-        if (need) {
-          m[g] = mn;
-          any = true;
+      for (int g = 0; g < G; ++g) alpha[g] = 1.f;
+      if (fl.x | fl.y | fl.z | fl.w) {  // the same for all four warps
+        float mx[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) mx[g] = sg[g];
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1)
+#pragma unroll
+          for (int g = 0; g < G; ++g) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], o));
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+          if (lane == g) redm[b][q4][g] = mx[g];
+        if (!group_sync()) break;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float mt = fmaxf(fmaxf(redm[b][0][g], redm[b][1][g]), fmaxf(redm[b][2][g], redm[b][3][g]));
+          const float mn = fmaxf(m[g], mt);
+          const bool need = mn > m[g] + 8.0f;
+          alpha[g] = need ? exp2f(m[g] - mn) : 1.f;
+          if (need) {
+            m[g] = mn;
+            any = true;
+          }
         }
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
         p[g] = exp2f(sg[g] - m[g]);
         lp[g] = lp[g] * alpha[g] + p[g];
       }
