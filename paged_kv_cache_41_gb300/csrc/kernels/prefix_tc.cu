@@ -393,9 +393,10 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
     // pair (tile A: the K stages, every QK^T has completed; tile B: the V
     // stages, its last PV has completed) as D / 32 planes of [128 rows][32
     // floats] with the 128-byte swizzle (16-byte chunk c of row t at
-    // c ^ (t % 8)); then one thread stores the planes with TMA (rows of
-    // requests past the batch are clipped).  Every warp of the group takes
-    // this path, so the group barrier always completes.
+    // c ^ (t % 8)).  One thread stores each plane with TMA as soon as the
+    // group has staged it, while the group stages the next (rows of requests
+    // past the batch are clipped).  Every warp of the group takes this path,
+    // so each group barrier always completes.
     unsigned char* stage = x == 0 ? ks : vs;
     const float sc = done ? inv : 0.f;
 #pragma unroll
@@ -409,17 +410,15 @@ __global__ void __launch_bounds__(kPrefixThreads, 1)
                                    ((ch ^ (row & 7)) << 4)) =
             make_float4(__uint_as_float(v[4 * ch]) * sc, __uint_as_float(v[4 * ch + 1]) * sc,
                         __uint_as_float(v[4 * ch + 2]) * sc, __uint_as_float(v[4 * ch + 3]) * sc);
-    }
-    tc::fence_proxy_async_smem();
-    named_barrier_sync(1 + x, 128);
-    if (row == 0) {
-#pragma unroll
-      for (int plane = 0; plane < D / 32; ++plane)
+      tc::fence_proxy_async_smem();
+      named_barrier_sync(1 + x, 128);
+      if (row == 0) {
         tma_store_5d(&tmo, plane * 32, split, 0, kvh, st_req0 + x * RPB,
                      stage + plane * kPlaneBytes);
-      bulk_commit_group();
-      bulk_wait_group_read0();
+        bulk_commit_group();
+      }
     }
+    if (row == 0) bulk_wait_group_read0();
     if (row_ok) a.part_lse[slot] = l_run > 0.f ? (m_run + log2f(l_run)) * a.lse_scale : -INFINITY;
   }
   tc::fence_before_sync();
