@@ -114,8 +114,9 @@ struct DecodeArgs {
   int32_t stage_units;   // work units of one stage (>= 1) ...
   int32_t piece_units;   // ... and of a piece's fixed cost (>= 0): the split of plan.cuh
   // 1: the length scan of the split (seq_lens in, plan_pre out) runs before
-  // the wait on the preceding kernel, under its tail.  Set only where that
-  // kernel is this library's prefix kernel, which writes neither.
+  // the wait on the preceding kernel, under its tail.  Set where that kernel
+  // is this library's (the prefix kernel, kv_append), which writes neither,
+  // or, for the plain decode, as its interface documents for seq_lens.
   int32_t plan_before_wait;
   float qscale;          // softmax scale * log2(e)
 };

@@ -563,6 +563,9 @@ pkv_status pkv_paged_attention_decode(const pkv_cache_desc* cache, void* out, fl
   a.num_ctas = (int32_t)C;
   a.num_stages = pkv::decode_num_stages(cache->head_dim, elem_bytes(cache->dtype));
   a.qscale = scale * 1.4426950408889634f;
+  // The length scan runs under the preceding kernel's tail where that kernel
+  // lets its dependents start early (kv_append: it writes rows, never lengths)
+  a.plan_before_wait = 1;
   return launch_decode(cache, G, q, k_cache, v_cache, a, as_stream(stream));
 }
 
