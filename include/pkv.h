@@ -175,12 +175,13 @@ int32_t pkv_decode_num_ctas(const pkv_cache_desc* cache, int32_t num_seqs,
  *   q:             [num_seqs, Hq, D].
  *   block_tables:  int32 [num_seqs, max_blocks_per_seq]; entries past
  *                  ceil(seq_lens[r] / P) are never read.
- *   seq_lens:      int32 [num_seqs].  The kernel may read it while the
- *                  preceding kernel on `stream` still runs, where that kernel
- *                  allows its dependents to start early (programmatic
- *                  dependent launch; this library's kv_append does): the
- *                  lengths must not be written by such a kernel.  Everything
- *                  else is read only after the preceding work has completed.
+ *   seq_lens:      int32 [num_seqs].  The kernel may read it, and
+ *                  block_tables, while the preceding kernel on `stream` still
+ *                  runs, where that kernel allows its dependents to start
+ *                  early (programmatic dependent launch; this library's
+ *                  kv_append does): neither may be written by such a kernel.
+ *                  Everything else is read only after the preceding work has
+ *                  completed.
  *   partition_size: 0, or a multiple of block_size.  The work is split into
  *                  pieces (M5.3 0x0A: allocator block, kernel block and
  *                  reduction partition are three levels): the token rows of

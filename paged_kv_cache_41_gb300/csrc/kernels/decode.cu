@@ -305,7 +305,6 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
   int4 d0;
   const int n = plan_cta_stages<kDecodeThreads, kStageRows>(
       a, reinterpret_cast<long long*>(scratch), &d0);
-  if (a.plan_before_wait) pdl_wait();
   if (n <= 0) return;  // no stages: the whole CTA leaves before any barrier
   const int hw = lane >> 4, l16 = lane & 15;
   float2 q2[G][EP2];
@@ -368,7 +367,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
     }
   };
   const bool d0_exact = a.stage_units == 1 && a.piece_units == 0;
-  if (d0_exact) load_q(d0.x, d0.y);
+  if (d0_exact && !a.plan_before_wait) load_q(d0.x, d0.y);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -495,10 +494,16 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
     }
     cT = effective_len(__ldg(a.seq_lens + cr), a.max_blocks, P, a.err, false);
     cpnt = (cT + kStageRows - 1) / kStageRows;
-    compute_batch(0);
-    if (d0_exact)
-      for (int st = 0; st < NS && st < n; ++st) issue_stage(st, st);
+    compute_batch(0);  // lengths, block tables and q rows only
   }
+  // With plan_before_wait, what the preceding kernel may still write (K/V
+  // rows, q) is read only from here on.
+  if (a.plan_before_wait) {
+    pdl_wait();
+    if (d0_exact) load_q(d0.x, d0.y);
+  }
+  if (d0_exact && warp == 0)
+    for (int st = 0; st < NS && st < n; ++st) issue_stage(st, st);
   if (!d0_exact) {
     __syncthreads();  // the first batch's descriptors: every warp reads its first piece there
     if (warp == 0)

@@ -100,7 +100,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   pdl_launch_dependents();  // the reduction may be scheduled as CTAs retire
   int4 d0;
   const int n = plan_cta_stages<kTcThreads, kTcRows>(a, wsum, &d0);
-  if (a.plan_before_wait) pdl_wait();
   if (n <= 0) return;  // no stages: the whole CTA leaves before any barrier
   const int Hkv = a.num_kv_heads, P = a.block_size;
   const int TB = P < kTcRows ? P : kTcRows;  // rows per TMA box
@@ -140,6 +139,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;  // S^T buffers at columns 0 and 16, O^T at 32
+  // With plan_before_wait, what the preceding kernel may still write is read
+  // only after the wait: the producer's first block ids come before it.
+  if (a.plan_before_wait && warp != 0) pdl_wait();
   int issued_k = 0, issued_v = 0;   // stages whose K / V copies warp 0 started
 
   if (warp == 0) {
@@ -181,6 +183,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                  : 0;
     };
     int blk_next = box_block(r, i, len);
+    if (a.plan_before_wait) pdl_wait();  // the K/V rows and q are read from here on
     int pieces = 0;
     // the previous stage's V boxes: this lane's block and first row, the box
     // count and the kv head

@@ -113,10 +113,11 @@ struct DecodeArgs {
   int32_t num_stages;    // shared-memory ring depth
   int32_t stage_units;   // work units of one stage (>= 1) ...
   int32_t piece_units;   // ... and of a piece's fixed cost (>= 0): the split of plan.cuh
-  // 1: the length scan of the split (seq_lens in, plan_pre out) runs before
+  // 1: the length scan of the split (seq_lens in, plan_pre out) and the
+  // first batch of stage descriptors (block_tables, q_rows in) run before
   // the wait on the preceding kernel, under its tail.  Set where that kernel
-  // is this library's (the prefix kernel, kv_append), which writes neither,
-  // or, for the plain decode, as its interface documents for seq_lens.
+  // is this library's (the prefix kernel, kv_append), which writes none of
+  // them, or, for the plain decode, as its interface documents.
   int32_t plan_before_wait;
   float qscale;          // softmax scale * log2(e)
 };
