@@ -155,6 +155,41 @@ int decode_num_stages(int head_dim, int elem_bytes) {
 //
 // l_run is this lane's share of its head's softmax sum: the weights of its
 // own rows (one per chunk); the piece end adds the four row lanes' shares.
+// Store N consecutive outputs (fp32, or bf16 rounded to nearest even) with
+// the widest aligned vector stores: the destination is aligned to N elements.
+template <int N>
+__device__ __forceinline__ void store_vec(float* p, const float (&o)[N]) {
+  if constexpr (N % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < N / 4; ++i)
+      reinterpret_cast<float4*>(p)[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+  } else if constexpr (N == 2) {
+    *reinterpret_cast<float2*>(p) = make_float2(o[0], o[1]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) p[i] = o[i];
+  }
+}
+template <int N>
+__device__ __forceinline__ void store_vec(__nv_bfloat16* p, const float (&o)[N]) {
+  if constexpr (N % 2 == 0) {
+    uint32_t w[N / 2];
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+    if constexpr (N == 8)
+      *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    else if constexpr (N == 4)
+      *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+    else
+      *reinterpret_cast<uint32_t*>(p) = w[0];
+  } else {
+    *p = __float2bfloat16_rn(o[0]);
+  }
+}
+
 template <typename T, int D, int G, bool kTail>
 __device__ __forceinline__ void decode_chunk(const T* __restrict__ kt, const T* __restrict__ vt,
                                              const uint8_t* __restrict__ ksc,
@@ -593,35 +628,51 @@ __global__ void __launch_bounds__(kDecodeThreads, (G >= 8 ? 2 : 4))
       if (!merge_sync()) break;
       const int64_t rh0 = (int64_t)dsc.x * a.num_q_heads + (int64_t)dsc.y * G;
       const int64_t rec = (int64_t)2 * c + ((flags & kSlot1) ? 1 : 0);
-      for (int j = threadIdx.x; j < G * D; j += kDecodeThreads) {
-        const int g = j / D, e = j % D;
+      // Each thread takes EPT consecutive outputs of one head: the head's
+      // weights once, then vector loads, one reciprocal and vector stores.
+      constexpr int kOut = G * D;
+      constexpr int EPT = kOut >= kDecodeThreads ? kOut / kDecodeThreads : 1;
+      const int j0 = threadIdx.x * EPT;
+      if (j0 < kOut) {
+        const int g = j0 / D, e0 = j0 % D;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mm[w * G + g]);
-        float Lsum = 0.f, o = 0.f;
+        float Lsum = 0.f, o[EPT];
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) o[i] = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
           for (int w = 0; w < kConsumerWarps; ++w) {
             const float wt = exp2f(mm[w * G + g] - M);
             Lsum = fmaf(wt, ml[w * G + g], Lsum);
-            o = fmaf(wt, macc[(w * G + g) * D + e], o);
+            float x[EPT];
+            if constexpr (EPT == 1)
+              x[0] = macc[(w * G + g) * D + e0];
+            else
+              VecLoad<float, EPT>::run(macc + (w * G + g) * D + e0, x);
+#pragma unroll
+            for (int i = 0; i < EPT; ++i) o[i] = fmaf(wt, x[i], o[i]);
           }
         }
         const bool nonempty = Lsum > 0.f;
-        o = nonempty ? o / Lsum : 0.f;
-        const float lse2 = nonempty ? M + log2f(Lsum) : -INFINITY;
+        const float inv = nonempty ? 1.f / Lsum : 0.f;
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) o[i] *= inv;
         const int64_t rh = rh0 + g;
+        float* dst32 = nullptr;
         if (!(flags & kWhole)) {
-          a.rec_o[(rec * G + g) * D + e] = o;
-          if (e == 0) a.rec_lse[rec * G + g] = lse2;
+          dst32 = a.rec_o + (rec * G + g) * D + e0;
+          if (e0 == 0) a.rec_lse[rec * G + g] = nonempty ? M + log2f(Lsum) : -INFINITY;
         } else if (a.st_o) {
           const int64_t slot = rh * a.st_stride + a.st_slot;
-          a.st_o[slot * D + e] = o;
-          if (e == 0) a.st_lse[slot] = lse2;
+          dst32 = a.st_o + slot * D + e0;
+          if (e0 == 0) a.st_lse[slot] = nonempty ? M + log2f(Lsum) : -INFINITY;
         } else {
-          store_out(static_cast<TQ*>(a.out) + rh * D + e, o);
-          if (e == 0 && a.lse_out) a.lse_out[rh] = lse2 * kLn2;
+          store_vec(static_cast<TQ*>(a.out) + rh * D + e0, o);
+          if (e0 == 0 && a.lse_out) a.lse_out[rh] = nonempty ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
         }
+        if (dst32) store_vec(dst32, o);
       }
       if (next_q) finish_q();
       // No barrier here: each warp releases the tile below once its own merge
