@@ -13,10 +13,10 @@
 //   * persistent, balanced CTAs: the work is the list of 32-row stages of
 //     every (sequence, kv head) segment, sequence-major; every CTA scans the
 //     lengths itself (a block-wide prefix sum, no planning launch), and CTA c
-//     of C (one wave: four per SM) streams stages [c S / C, (c + 1) S / C) of
-//     the S in the list.  Every CTA moves
-//     the same bytes whatever the length mix, there is no tail wave, and a
-//     CTA crosses segment boundaries without draining its pipeline;
+//     of C (one wave: four per SM) takes the c-th equal share of the work
+//     units (plan.cuh: a stage costs two, a piece's fixed cost three).  Every
+//     CTA does the same work whatever the length mix, there is no tail wave,
+//     and a CTA crosses segment boundaries without draining its pipeline;
 //   * a segment a CTA covers whole is finished there (output written
 //     directly); a segment cut by CTA boundaries leaves one (O, LSE) record
 //     per piece -- at most two per CTA, for its first and last segments --
@@ -32,8 +32,10 @@
 //   * warps consume 16-row chunks: each half-warp owns two token rows, each
 //     lane 1/16 of head_dim; the 2G (row, head) partial dot products are
 //     summed across the 16 lanes through a small per-warp shared scratch;
-//     the row lands in lane bit 3, so the softmax max and sum over the warp's
-//     four rows are two shuffles each; q . k and P . V use packed fp32x2 FMAs;
+//     the row lands in lane bit 3; a vote on each lane's own score decides
+//     whether the chunk needs the max over the warp's four rows (two
+//     shuffles) and a rescale, and each lane sums its own rows' weights until
+//     the piece end adds them; q . k and P . V use packed fp32x2 FMAs;
 //   * full stages take a straight-line path with no row masking;
 //   * at a piece's end the four warps merge through the stage's own tile
 //     (released only afterwards), so the ring keeps streaming the next piece;

@@ -25,7 +25,9 @@
 //   * warp 0 streams each stage's K and V boxes by TMA (128-byte swizzle,
 //     row-group tiles of launch.h: one box brings a whole block, or a
 //     128-row slice of a larger one, both column halves; one box per lane)
-//     and a piece's Q rows at its first stage; warp 1 issues the MMAs; warps
+//     and a piece's Q rows at its first stage, K one stage ahead of V (a K
+//     slot is refilled once its QK has run, a V slot once its PV has, on
+//     separate K and V barriers); warp 1 issues the MMAs; warps
 //     2-5 own one key row (S^T lane) and one head_dim row (O^T lane) each and
 //     run the online softmax: a four-warp vote on whether any score passes
 //     its head's base by 2^8 (then per-head maxima across the 128 keys by

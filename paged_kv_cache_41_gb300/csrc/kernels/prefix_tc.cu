@@ -42,7 +42,8 @@
 //     exponential with one FMA (scale and shift), masks only a split's last
 //     tile, and sums on packed fp32 pairs;
 //   * each warpgroup stages its normalised O tile in shared memory with the
-//     128-byte swizzle and writes it with TMA stores.
+//     128-byte swizzle, 32 columns at a time, and writes each 32-column plane
+//     with a TMA store as soon as it is staged.
 #include <limits.h>
 #include <math.h>
 
